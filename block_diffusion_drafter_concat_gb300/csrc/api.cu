@@ -1,0 +1,884 @@
+// C ABI of libdflash (declared in include/dflash.h): argument validation, workspace
+// carving, TMA descriptor encoding and the kernel launch chains of each entry point.
+// Every launch carries the programmatic-stream-serialization attribute so that each
+// kernel's weight prefetch overlaps the tail of the kernel before it.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <type_traits>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "host.h"
+#include "misc.cuh"
+
+using namespace dflash;
+
+// ------------------------------------------------------------------ error plumbing
+namespace {
+thread_local std::string g_last_error;
+thread_local int g_launches = 0;
+}  // namespace
+
+namespace dflash {
+dflash_status fail(dflash_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+void count_launch() { ++g_launches; }
+}  // namespace dflash
+
+namespace {
+
+#define CUDA_TRY(expr)                                                                   \
+  do {                                                                                   \
+    cudaError_t e_ = (expr);                                                             \
+    if (e_ != cudaSuccess)                                                               \
+      return fail(DFLASH_ECUDA, "%s failed: %s", #expr, cudaGetErrorString(e_));         \
+  } while (0)
+
+#define TRY(expr) DFLASH_TRY(expr)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// ------------------------------------------------------------------ TMA descriptors
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, inner] with row stride `ld` elements, read in boxes of
+// box_rows x 64 elements (128 bytes) with 128-byte swizzle; out-of-range reads give 0.
+dflash_status encode_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t inner,
+                          uint64_t ld, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(DFLASH_ECUDA, "cuTensorMapEncodeTiled unavailable");
+  if (!aligned16(ptr) || (ld * 2) % 16 != 0 || rows == 0 || inner == 0)
+    return fail(DFLASH_EINVAL, "tensor %p (%llu x %llu, ld %llu) not TMA-compatible", ptr,
+                (unsigned long long)rows, (unsigned long long)inner, (unsigned long long)ld);
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DFLASH_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return DFLASH_OK;
+}
+
+// ------------------------------------------------------------------ workspace carving
+struct Carve {
+  char* base;
+  size_t off = 0;
+  template <typename T>
+  T* take(size_t n) {
+    off = (off + 255) & ~size_t(255);
+    T* p = reinterpret_cast<T*>(base ? base + off : nullptr);
+    off += n * sizeof(T);
+    return p;
+  }
+};
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+}  // namespace
+
+// ------------------------------------------------------------------ the handle
+struct dflash_handle_s {
+  dflash_config c;
+  bool bf16;
+  int dev = 0, sms = 148;
+  const void *w_fuse, *g_fuse, *g_final, *embed, *lm_head;
+  std::vector<const void*> g_attn, w_q, w_k, w_v, w_o, g_mlp, w_gate, w_up, w_down;
+  CUtensorMap m_fuse, m_lm;
+  std::vector<CUtensorMap> m_q, m_k, m_v, m_o, m_gate, m_up, m_down;
+  int* d_err = nullptr;
+  float2* d_rope = nullptr;
+};
+
+namespace {
+
+using H = dflash_handle_s;
+
+// ------------------------------------------------------------------ GEMM planning
+struct WSet {
+  const CUtensorMap* maps[kMaxSeg];
+  const void* ptrs[kMaxSeg];
+  int rows[kMaxSeg];
+  int nseg = 0;
+  bool paired = false;
+  void add(const CUtensorMap* m, const void* p, int r) {
+    maps[nseg] = m;
+    ptrs[nseg] = p;
+    rows[nseg] = r;
+    ++nseg;
+  }
+};
+
+int pick_bn(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
+
+GemmShape plan_shape(const H* h, const WSet& w, int M, int K, bool tc, int* grid_out) {
+  GemmShape g = {};
+  g.M = M;
+  g.K = K;
+  g.paired = w.paired;
+  g.nseg = w.nseg;
+  int t = 0;
+  for (int s = 0; s < w.nseg; ++s) {
+    g.seg_tile0[s] = t;
+    g.seg_rows[s] = w.rows[s];
+    t += w.paired ? (s == 0 ? ceil_div(w.rows[0], kBM / 2) : 0) : ceil_div(w.rows[s], kBM);
+  }
+  g.seg_tile0[w.nseg] = t;
+  if (w.paired) g.seg_tile0[1] = t;  // both halves of every tile come from segment 0's range
+  g.n_tiles = t;
+  const int bn = tc ? pick_bn(M) : kF32BN;
+  g.m_blocks = ceil_div(M, bn);
+  g.ks = ceil_div(K, kBK);
+  g.units = (long long)g.m_blocks * g.n_tiles * g.ks;
+  int grid = static_cast<int>(std::min<long long>(h->sms, (g.units + 3) / 4));
+  *grid_out = std::max(1, grid);
+  return g;
+}
+
+size_t gemm_part_floats(const H* h) { return (size_t)h->sms * 2 * 128 * kBM; }
+
+// Runs one projection: y = A W^T over the weight segments of `w`, epilogue EPI.
+template <int EPI, typename T>
+dflash_status gemm(const H* h, const void* A, int M, int K, const WSet& w, EpiArgs<T> e,
+                   float* part, int* ctr, cudaStream_t st) {
+  if (M == 0) return DFLASH_OK;
+  int grid;
+  const bool tc = h->bf16;
+  GemmShape g = plan_shape(h, w, M, K, tc, &grid);
+  g.part = part;
+  g.counters = ctr;
+  e.M = M;
+  if (EPI == EPI_F32 || EPI == EPI_RESID || EPI == EPI_ARGMAX) e.N = w.rows[0];
+  if (g.m_blocks * g.n_tiles > kCtlWords)
+    return fail(DFLASH_EUNSUPPORTED, "GEMM with %d tiles exceeds the control words",
+                g.m_blocks * g.n_tiles);
+  if constexpr (std::is_same<T, bf16>::value) {
+    CUtensorMap tmA;
+    const int bn = pick_bn(M);
+    TRY(encode_bf16(&tmA, A, M, K, K, bn));
+    WMaps wm;
+    for (int s = 0; s < w.nseg; ++s) wm.m[s] = *w.maps[s];
+    if (bn <= 32) return launch_gemm_tc_lo(bn, EPI, tmA, wm, g, grid, e, st);
+    return launch_gemm_tc_hi(bn, EPI, tmA, wm, g, grid, e, st);
+  } else {
+    WPtrs p = {};
+    for (int s = 0; s < w.nseg; ++s) p.p[s] = static_cast<const float*>(w.ptrs[s]);
+    return launch_gemm_f32(EPI, dim3(g.m_blocks * g.n_tiles), static_cast<const float*>(A), K, p,
+                           g, e, st);
+  }
+}
+
+// ------------------------------------------------------------------ small launches
+template <typename T, typename Tin>
+dflash_status rmsnorm(const H* h, const Tin* x, const void* gain, T* y, int rows,
+                      cudaStream_t st) {
+  if (rows == 0) return DFLASH_OK;
+  return launch(k_rmsnorm<T, Tin>, dim3(rows), dim3(kRowThreads), 0, st, x,
+                static_cast<float*>(nullptr), static_cast<const T*>(gain), y, h->c.d_model,
+                h->c.rms_eps, static_cast<const int*>(nullptr), static_cast<const T*>(nullptr), 0,
+                static_cast<const int*>(nullptr), 1, 0, static_cast<int*>(nullptr), h->d_err);
+}
+
+// ------------------------------------------------------------------ attention plan
+struct AttnPlan {
+  int pps, nsplit;
+};
+
+AttnPlan plan_attn(const H* h, int B, int max_pages) {
+  const int kp = max_pages + 1;
+  const int groups = B * h->c.n_kv_heads;
+  int want = std::max(1, ceil_div(h->sms, groups));
+  int pps = std::max(8, ceil_div(kp, want));
+  int ns = ceil_div(kp, pps);
+  const int QR = h->c.block_size * (h->c.n_q_heads / h->c.n_kv_heads);
+  // the combine weights (ns x QR floats) reuse the K/V ring of the bf16 kernel
+  const int ring = 4 * 2 * kPage * h->c.head_dim * 2;
+  const int cap = std::min(64, h->bf16 ? ring / (QR * 4) : h->c.head_dim);
+  if (ns > cap) {
+    pps = ceil_div(kp, cap);
+    ns = ceil_div(kp, pps);
+  }
+  return {pps, ns};
+}
+
+// ------------------------------------------------------------------ workspace plans
+struct DraftWs {
+  int* ctl;
+  float* x;
+  void* n;
+  int* pos;
+  void *q, *kb, *vb, *o, *act;
+  float *part_o, *part_ml, *gpart;
+};
+
+size_t elt(const H* h) { return h->bf16 ? 2 : 4; }
+
+DraftWs carve_draft(const H* h, Carve& cv, int B, int max_pages) {
+  const auto& c = h->c;
+  const size_t M = (size_t)B * c.block_size;
+  const AttnPlan ap = plan_attn(h, B, max_pages);
+  const int QR = c.block_size * (c.n_q_heads / c.n_kv_heads);
+  DraftWs w;
+  w.ctl = cv.take<int>(kCtlWords);
+  w.x = cv.take<float>(M * c.d_model);
+  w.n = cv.take<char>(M * c.d_model * elt(h));
+  w.pos = cv.take<int>(M);
+  w.q = cv.take<char>(M * c.n_q_heads * c.head_dim * elt(h));
+  w.kb = cv.take<char>((M + 16) * c.n_kv_heads * c.head_dim * elt(h));
+  w.vb = cv.take<char>((M + 16) * c.n_kv_heads * c.head_dim * elt(h));
+  w.o = cv.take<char>(M * c.n_q_heads * c.head_dim * elt(h));
+  w.act = cv.take<char>(M * c.ffn_dim * elt(h));
+  w.part_o = cv.take<float>((size_t)B * c.n_kv_heads * ap.nsplit * QR * c.head_dim);
+  w.part_ml = cv.take<float>((size_t)B * c.n_kv_heads * ap.nsplit * QR * 2);
+  w.gpart = cv.take<float>(gemm_part_floats(h));
+  return w;
+}
+
+struct InjectWs {
+  int* ctl;
+  float* u;
+  void* fused;
+  float* gpart;
+};
+
+InjectWs carve_inject(const H* h, Carve& cv, int n) {
+  InjectWs w;
+  w.ctl = cv.take<int>(kCtlWords);
+  w.u = cv.take<float>((size_t)n * h->c.d_model);
+  w.fused = cv.take<char>((size_t)n * h->c.d_model * elt(h));
+  w.gpart = cv.take<float>(gemm_part_floats(h));
+  return w;
+}
+
+struct HeadWs {
+  int* ctl;
+  float *am_max, *am_sum;
+  int* am_idx;
+  float* gpart;
+};
+
+HeadWs carve_head(const H* h, Carve& cv, int rows) {
+  const size_t t = (size_t)ceil_div(h->c.vocab, kBM) * rows;
+  HeadWs w;
+  w.ctl = cv.take<int>(kCtlWords);
+  w.am_max = cv.take<float>(t);
+  w.am_sum = cv.take<float>(t);
+  w.am_idx = cv.take<int>(t);
+  w.gpart = cv.take<float>(gemm_part_floats(h));
+  return w;
+}
+
+int verify_chunks(const H* h, int rows) {
+  const int V = h->c.vocab;
+  int nch = std::max(1, ceil_div(2 * h->sms, rows));
+  int chunk = std::max(2048, ceil_div(ceil_div(V, nch), 2048) * 2048);
+  return ceil_div(V, chunk);
+}
+int chunk_of(const H* h, int nch) {
+  int c = ceil_div(h->c.vocab, nch);
+  return ceil_div(c, 8) * 8;
+}
+
+struct VerifyWs {
+  int* ctl;
+  float *pv, *pv2, *lse_t, *zr;
+  int* pi;
+  int* rej;
+  void* hrow;
+  float* gpart;
+};
+
+VerifyWs carve_verify(const H* h, Carve& cv, int B, bool sample) {
+  const int rows = B * h->c.block_size;
+  const int nch = verify_chunks(h, rows);
+  VerifyWs w = {};
+  w.ctl = cv.take<int>(kCtlWords);
+  w.pv = cv.take<float>((size_t)rows * nch);
+  w.pv2 = cv.take<float>((size_t)rows * nch);
+  w.pi = cv.take<int>((size_t)rows * nch);
+  if (sample) {
+    w.lse_t = cv.take<float>(rows);
+    w.rej = cv.take<int>(B);
+    w.hrow = cv.take<char>((size_t)B * h->c.d_model * elt(h));
+    w.zr = cv.take<float>((size_t)B * h->c.vocab);
+    w.gpart = cv.take<float>(gemm_part_floats(h));
+  }
+  return w;
+}
+
+dflash_status check_ws(const void* ws, size_t have, size_t need) {
+  if (!ws) return fail(DFLASH_EINVAL, "workspace is NULL");
+  if (!aligned16(ws)) return fail(DFLASH_EINVAL, "workspace not 16-byte aligned");
+  if (have < need)
+    return fail(DFLASH_EWORKSPACE, "workspace %zu bytes < %zu needed", have, need);
+  return DFLASH_OK;
+}
+
+#define NEED(p, what)                                                                    \
+  do {                                                                                   \
+    if (!(p)) return fail(DFLASH_EINVAL, "%s is NULL", what);                            \
+    if (!aligned16(p)) return fail(DFLASH_EINVAL, "%s not 16-byte aligned", what);       \
+  } while (0)
+
+}  // namespace
+
+static dflash_status fuse_impl(H* h, const void* x_cat, int n, void* fused, float* u,
+                               float* gpart, int* ctl, cudaStream_t st) {
+  const int kin = h->c.n_target_layers * h->c.target_width;
+  WSet w;
+  w.add(&h->m_fuse, h->w_fuse, h->c.d_model);
+  if (h->bf16) {
+    EpiArgs<bf16> e = {};
+    e.y = u;
+    e.ldy = h->c.d_model;
+    e.err = h->d_err;
+    TRY((gemm<EPI_F32, bf16>(h, x_cat, n, kin, w, e, gpart, ctl, st)));
+    return rmsnorm<bf16, float>(h, u, h->g_fuse, static_cast<bf16*>(fused), n, st);
+  }
+  EpiArgs<float> e = {};
+  e.y = u;
+  e.ldy = h->c.d_model;
+  e.err = h->d_err;
+  TRY((gemm<EPI_F32, float>(h, x_cat, n, kin, w, e, gpart, ctl, st)));
+  return rmsnorm<float, float>(h, u, h->g_fuse, static_cast<float*>(fused), n, st);
+}
+
+template <typename T>
+static dflash_status draft_impl(H* h, const int32_t* block_ids, const int32_t* ctx_lens,
+                                const int32_t* page_table, int32_t max_pages, int32_t B,
+                                int32_t num_pages, void* const* k_pool, void* const* v_pool,
+                                void* final_hidden, const DraftWs& w, cudaStream_t st) {
+  const auto& c = h->c;
+  const int S = c.block_size, M = B * S, d = c.d_model;
+  const int qw = c.n_q_heads * c.head_dim, kvw = c.n_kv_heads * c.head_dim;
+  const int G = c.n_q_heads / c.n_kv_heads, QR = S * G;
+  T* n = static_cast<T*>(w.n);
+  // block embedding + first pre-attention norm + positions
+  TRY(launch(k_rmsnorm<T, float>, dim3(M), dim3(kRowThreads), 0, st,
+             static_cast<const float*>(nullptr), w.x, static_cast<const T*>(h->g_attn[0]), n, d,
+             c.rms_eps, block_ids, static_cast<const T*>(h->embed), c.vocab, ctx_lens, S,
+             c.max_position, w.pos, h->d_err));
+  const AttnPlan ap = plan_attn(h, B, max_pages);
+  for (int l = 0; l < c.n_layers; ++l) {
+    {  // Q, K, V with RoPE
+      WSet ws_;
+      ws_.add(h->bf16 ? &h->m_q[l] : nullptr, h->w_q[l], qw);
+      ws_.add(h->bf16 ? &h->m_k[l] : nullptr, h->w_k[l], kvw);
+      ws_.add(h->bf16 ? &h->m_v[l] : nullptr, h->w_v[l], kvw);
+      EpiArgs<T> e = {};
+      e.pos = w.pos;
+      e.rope = h->d_rope;
+      e.max_pos = c.max_position;
+      e.S = S;
+      e.hq = c.n_q_heads;
+      e.hkv = c.n_kv_heads;
+      e.hd = c.head_dim;
+      e.q = static_cast<T*>(w.q);
+      e.kb = static_cast<T*>(w.kb);
+      e.vb = static_cast<T*>(w.vb);
+      e.err = h->d_err;
+      TRY((gemm<EPI_QKV, T>(h, n, M, d, ws_, e, w.gpart, w.ctl, st)));
+    }
+    {  // attention over [context pages ; block]
+      AttnArgs<T> a = {};
+      a.q = static_cast<const T*>(w.q);
+      a.kb = static_cast<const T*>(w.kb);
+      a.vb = static_cast<const T*>(w.vb);
+      a.kpool = static_cast<const T*>(k_pool[l]);
+      a.vpool = static_cast<const T*>(v_pool[l]);
+      a.page_table = page_table;
+      a.max_pages = max_pages;
+      a.ctx_lens = ctx_lens;
+      a.num_pages = num_pages;
+      a.S = S;
+      a.hq = c.n_q_heads;
+      a.hkv = c.n_kv_heads;
+      a.hd = c.head_dim;
+      a.QR = QR;
+      a.pps = ap.pps;
+      a.nsplit = ap.nsplit;
+      a.part_o = w.part_o;
+      a.part_ml = w.part_ml;
+      a.counters = w.ctl;
+      a.out = static_cast<T*>(w.o);
+      a.err = h->d_err;
+      dim3 grid(ap.nsplit, c.n_kv_heads, B);
+      if constexpr (std::is_same<T, bf16>::value) {
+        AttnMaps mp;
+        const uint64_t pool_rows = (uint64_t)num_pages * c.n_kv_heads * kPage;
+        TRY(encode_bf16(&mp.k, k_pool[l], pool_rows, c.head_dim, c.head_dim, kPage));
+        TRY(encode_bf16(&mp.v, v_pool[l], pool_rows, c.head_dim, c.head_dim, kPage));
+        const uint64_t blk_rows = (uint64_t)B * c.n_kv_heads * S;
+        TRY(encode_bf16(&mp.kb, w.kb, blk_rows, c.head_dim, c.head_dim, kPage));
+        TRY(encode_bf16(&mp.vb, w.vb, blk_rows, c.head_dim, c.head_dim, kPage));
+        const int smem = 1024 + 4 * 2 * kPage * c.head_dim * 2 + 2 * 4 * 8 + 16;
+        TRY(launch_attn_tc(c.head_dim, QR / 16, grid, smem, mp, a, st));
+      } else {
+        const int smem = (2 * QR * c.head_dim + 2 * kPage * c.head_dim + QR * kPage + 3 * QR) * 4;
+        TRY(launch_attn_f32(grid, smem, a, st));
+      }
+    }
+    {  // output projection + residual
+      WSet ws_;
+      ws_.add(h->bf16 ? &h->m_o[l] : nullptr, h->w_o[l], d);
+      EpiArgs<T> e = {};
+      e.y = w.x;
+      e.ldy = d;
+      e.err = h->d_err;
+      TRY((gemm<EPI_RESID, T>(h, w.o, M, qw, ws_, e, w.gpart, w.ctl, st)));
+    }
+    TRY((rmsnorm<T, float>(h, w.x, h->g_mlp[l], n, M, st)));
+    {  // gate | up with SwiGLU
+      WSet ws_;
+      ws_.add(h->bf16 ? &h->m_gate[l] : nullptr, h->w_gate[l], c.ffn_dim);
+      ws_.add(h->bf16 ? &h->m_up[l] : nullptr, h->w_up[l], c.ffn_dim);
+      ws_.paired = true;
+      EpiArgs<T> e = {};
+      e.act = static_cast<T*>(w.act);
+      e.F = c.ffn_dim;
+      e.err = h->d_err;
+      TRY((gemm<EPI_SWIGLU, T>(h, n, M, d, ws_, e, w.gpart, w.ctl, st)));
+    }
+    {  // down projection + residual
+      WSet ws_;
+      ws_.add(h->bf16 ? &h->m_down[l] : nullptr, h->w_down[l], d);
+      EpiArgs<T> e = {};
+      e.y = w.x;
+      e.ldy = d;
+      e.err = h->d_err;
+      TRY((gemm<EPI_RESID, T>(h, w.act, M, c.ffn_dim, ws_, e, w.gpart, w.ctl, st)));
+    }
+    if (l + 1 < c.n_layers)
+      TRY((rmsnorm<T, float>(h, w.x, h->g_attn[l + 1], n, M, st)));
+    else
+      TRY((rmsnorm<T, float>(h, w.x, h->g_final, static_cast<T*>(final_hidden), M, st)));
+  }
+  return DFLASH_OK;
+}
+
+template <typename T>
+static dflash_status head_impl(H* h, const void* hidden, int rows, float temperature,
+                               int32_t* tokens, float* max_logit, float* lse, const HeadWs& w,
+                               cudaStream_t st) {
+  WSet ws_;
+  ws_.add(h->bf16 ? &h->m_lm : nullptr, h->lm_head, h->c.vocab);
+  EpiArgs<T> e = {};
+  e.am_max = w.am_max;
+  e.am_idx = w.am_idx;
+  e.am_sum = w.am_sum;
+  e.inv_temp = 1.0f / temperature;
+  e.want_sum = lse != nullptr;
+  e.err = h->d_err;
+  TRY((gemm<EPI_ARGMAX, T>(h, hidden, rows, h->c.d_model, ws_, e, w.gpart, w.ctl, st)));
+  const int n_tiles = ceil_div(h->c.vocab, kBM);
+  return launch(k_argmax_finalize, dim3(ceil_div(rows, kRowThreads / 32)), dim3(kRowThreads), 0,
+                st, static_cast<const float*>(w.am_max), static_cast<const int*>(w.am_idx),
+                static_cast<const float*>(w.am_sum), n_tiles, rows, 1.0f / temperature, tokens,
+                max_logit, lse);
+}
+
+template <typename T>
+static dflash_status sample_impl(H* h, const int32_t* draft, const void* final_hidden,
+                                 const float* dmax, const float* dlse, const void* logits,
+                                 const float* u, float temperature, int B, int32_t* out_tokens,
+                                 int32_t* n_acc, int32_t* n_emit, const VerifyWs& w,
+                                 cudaStream_t st) {
+  const int S = h->c.block_size, V = h->c.vocab, d = h->c.d_model, rows = B * S;
+  const float it = 1.0f / temperature;
+  const int nch = verify_chunks(h, rows), chunk = chunk_of(h, nch);
+  TRY(launch(k_verify_sample_accept<T>, dim3(nch, rows), dim3(kRowThreads), 0, st,
+             static_cast<const T*>(logits), draft, dmax, dlse, u,
+             static_cast<const T*>(final_hidden), d, S, V, chunk, it, w.pv, w.pv2, w.lse_t, w.ctl,
+             w.rej, static_cast<T*>(w.hrow), out_tokens, n_acc, n_emit, h->d_err));
+  {  // drafter logits of each sequence's first rejected slot
+    WSet ws_;
+    ws_.add(h->bf16 ? &h->m_lm : nullptr, h->lm_head, V);
+    EpiArgs<T> e = {};
+    e.y = w.zr;
+    e.ldy = V;
+    e.err = h->d_err;
+    TRY((gemm<EPI_F32, T>(h, w.hrow, B, d, ws_, e, w.gpart, w.ctl, st)));
+  }
+  const int nch2 = verify_chunks(h, B), chunk2 = chunk_of(h, nch2);
+  return launch(k_verify_sample_residual<T>, dim3(nch2, B), dim3(kRowThreads), 0, st,
+                static_cast<const T*>(logits), static_cast<const float*>(w.zr),
+                static_cast<const float*>(w.lse_t), dlse, u, static_cast<const int*>(w.rej), S, V,
+                chunk2, it, w.pv, w.pv2, w.ctl, out_tokens);
+}
+
+// ===================================================================== entry points
+extern "C" {
+
+const char* dflash_last_error(void) { return g_last_error.c_str(); }
+int32_t dflash_last_launch_count(void) { return g_launches; }
+
+dflash_status dflash_create(const dflash_config* cfg, const dflash_weights* w,
+                            dflash_handle* out) {
+  g_launches = 0;
+  if (!cfg || !w || !out) return fail(DFLASH_EINVAL, "null argument");
+  *out = nullptr;
+  const dflash_config& c = *cfg;
+  if (c.d_model <= 0 || c.n_layers <= 0 || c.n_q_heads <= 0 || c.n_kv_heads <= 0 ||
+      c.head_dim <= 0 || c.ffn_dim <= 0 || c.vocab <= 0 || c.block_size <= 0 ||
+      c.n_target_layers <= 0 || c.target_width <= 0 || c.max_position <= 0)
+    return fail(DFLASH_EINVAL, "non-positive dimension in config");
+  if (c.page_size != kPage) return fail(DFLASH_EUNSUPPORTED, "page_size must be 16");
+  if (c.n_q_heads % c.n_kv_heads) return fail(DFLASH_EINVAL, "n_q_heads %% n_kv_heads != 0");
+  if (c.head_dim % 2) return fail(DFLASH_EINVAL, "head_dim must be even");
+  if (!(c.rope_theta > 0.f) || !(c.rms_eps >= 0.f)) return fail(DFLASH_EINVAL, "bad theta/eps");
+  if (c.dtype != DFLASH_BF16 && c.dtype != DFLASH_F32) return fail(DFLASH_EINVAL, "bad dtype");
+  const int QR = c.block_size * (c.n_q_heads / c.n_kv_heads);
+  const int kin = c.n_target_layers * c.target_width;
+  if (c.dtype == DFLASH_BF16) {
+    if (c.head_dim != 64 && c.head_dim != 128)
+      return fail(DFLASH_EUNSUPPORTED, "bf16 kernels need head_dim 64 or 128");
+    if ((c.n_q_heads * c.head_dim) % kBM || (c.n_kv_heads * c.head_dim) % kBM)
+      return fail(DFLASH_EUNSUPPORTED, "q and kv widths must be multiples of 128");
+    if (c.d_model % 8 || c.ffn_dim % 8 || kin % 8)
+      return fail(DFLASH_EUNSUPPORTED, "widths must be multiples of 8");
+    if (QR % 16 || QR > 128 || c.block_size > 16)
+      return fail(DFLASH_EUNSUPPORTED, "block_size*group must be a multiple of 16 <= 128");
+  } else {
+    if (QR > 128 || c.head_dim > 128 || c.block_size > 16)
+      return fail(DFLASH_EUNSUPPORTED, "fp32 path: block*group <= 128, head_dim <= 128");
+  }
+  const void* const* arrs[] = {w->g_attn, w->w_q, w->w_k, w->w_v, w->w_o,
+                               w->g_mlp, w->w_gate, w->w_up, w->w_down};
+  for (auto a : arrs)
+    if (!a) return fail(DFLASH_EINVAL, "per-layer weight array is NULL");
+  const void* singles[] = {w->w_fuse, w->g_fuse, w->g_final, w->embed, w->lm_head};
+  for (auto p : singles) NEED(p, "weight");
+  for (auto a : arrs)
+    for (int l = 0; l < c.n_layers; ++l) NEED(a[l], "layer weight");
+
+  H* h = new H();
+  h->c = c;
+  h->bf16 = c.dtype == DFLASH_BF16;
+  cudaGetDevice(&h->dev);
+  cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->dev);
+  h->w_fuse = w->w_fuse; h->g_fuse = w->g_fuse; h->g_final = w->g_final;
+  h->embed = w->embed; h->lm_head = w->lm_head;
+  auto cp = [&](std::vector<const void*>& v, const void* const* a) { v.assign(a, a + c.n_layers); };
+  cp(h->g_attn, w->g_attn); cp(h->w_q, w->w_q); cp(h->w_k, w->w_k); cp(h->w_v, w->w_v);
+  cp(h->w_o, w->w_o); cp(h->g_mlp, w->g_mlp); cp(h->w_gate, w->w_gate); cp(h->w_up, w->w_up);
+  cp(h->w_down, w->w_down);
+
+  auto bail = [&](dflash_status s) {
+    if (h->d_err) cudaFree(h->d_err);
+    if (h->d_rope) cudaFree(h->d_rope);
+    delete h;
+    return s;
+  };
+  if (h->bf16) {
+    const int d = c.d_model, qw = c.n_q_heads * c.head_dim, kvw = c.n_kv_heads * c.head_dim;
+    dflash_status s = encode_bf16(&h->m_fuse, h->w_fuse, d, kin, kin, kBM);
+    if (s == DFLASH_OK) s = encode_bf16(&h->m_lm, h->lm_head, c.vocab, d, d, kBM);
+    h->m_q.resize(c.n_layers); h->m_k.resize(c.n_layers); h->m_v.resize(c.n_layers);
+    h->m_o.resize(c.n_layers); h->m_gate.resize(c.n_layers); h->m_up.resize(c.n_layers);
+    h->m_down.resize(c.n_layers);
+    for (int l = 0; l < c.n_layers && s == DFLASH_OK; ++l) {
+      s = encode_bf16(&h->m_q[l], h->w_q[l], qw, d, d, kBM);
+      if (s == DFLASH_OK) s = encode_bf16(&h->m_k[l], h->w_k[l], kvw, d, d, kBM);
+      if (s == DFLASH_OK) s = encode_bf16(&h->m_v[l], h->w_v[l], kvw, d, d, kBM);
+      if (s == DFLASH_OK) s = encode_bf16(&h->m_o[l], h->w_o[l], d, qw, qw, kBM);
+      if (s == DFLASH_OK) s = encode_bf16(&h->m_gate[l], h->w_gate[l], c.ffn_dim, d, d, kBM / 2);
+      if (s == DFLASH_OK) s = encode_bf16(&h->m_up[l], h->w_up[l], c.ffn_dim, d, d, kBM / 2);
+      if (s == DFLASH_OK) s = encode_bf16(&h->m_down[l], h->w_down[l], d, c.ffn_dim, c.ffn_dim, kBM);
+    }
+    if (s != DFLASH_OK) return bail(s);
+  }
+  if (cudaMalloc(&h->d_err, sizeof(int)) != cudaSuccess ||
+      cudaMemset(h->d_err, 0, sizeof(int)) != cudaSuccess)
+    return bail(fail(DFLASH_ECUDA, "cannot allocate the error word"));
+  // RoPE table: angle p * theta^(-2j/hd) in double, stored as fp32 (cos, sin)
+  const int half = c.head_dim / 2;
+  std::vector<float2> tab((size_t)c.max_position * half);
+  for (int p = 0; p < c.max_position; ++p)
+    for (int j = 0; j < half; ++j) {
+      double ang = p * std::pow((double)c.rope_theta, -2.0 * j / c.head_dim);
+      tab[(size_t)p * half + j] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+    }
+  if (cudaMalloc(&h->d_rope, tab.size() * sizeof(float2)) != cudaSuccess ||
+      cudaMemcpy(h->d_rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) !=
+          cudaSuccess)
+    return bail(fail(DFLASH_ECUDA, "cannot allocate the RoPE table"));
+  *out = h;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_destroy(dflash_handle h) {
+  if (!h) return fail(DFLASH_EINVAL, "null handle");
+  cudaFree(h->d_err);
+  cudaFree(h->d_rope);
+  delete h;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_workspace_size(dflash_handle h, int32_t max_rows, int32_t max_batch,
+                                    int32_t max_pages, size_t* bytes) {
+  if (!h || !bytes) return fail(DFLASH_EINVAL, "null argument");
+  if (max_rows < 0 || max_batch < 0 || max_pages < 0) return fail(DFLASH_EINVAL, "negative size");
+  size_t need = 0;
+  {
+    Carve cv{nullptr};
+    carve_inject(h, cv, std::max(max_rows, 1));
+    need = std::max(need, cv.off);
+  }
+  {
+    Carve cv{nullptr};
+    carve_draft(h, cv, std::max(max_batch, 1), std::max(max_pages, 1));
+    need = std::max(need, cv.off);
+  }
+  {
+    Carve cv{nullptr};
+    carve_head(h, cv, std::max(max_rows, 1));
+    need = std::max(need, cv.off);
+  }
+  {
+    Carve cv{nullptr};
+    carve_verify(h, cv, std::max(max_batch, 1), true);
+    need = std::max(need, cv.off);
+  }
+  *bytes = need;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_workspace_init(dflash_handle h, void* ws, size_t ws_bytes, void* stream) {
+  if (!h) return fail(DFLASH_EINVAL, "null handle");
+  TRY(check_ws(ws, ws_bytes, kCtlWords * sizeof(int)));
+  CUDA_TRY(cudaMemsetAsync(ws, 0, kCtlWords * sizeof(int), static_cast<cudaStream_t>(stream)));
+  return DFLASH_OK;
+}
+
+dflash_status dflash_fuse_features(dflash_handle h, const void* x_cat, int32_t n, void* fused,
+                                   void* ws, size_t ws_bytes, void* stream) {
+  g_launches = 0;
+  if (!h) return fail(DFLASH_EINVAL, "null handle");
+  if (n < 0) return fail(DFLASH_EINVAL, "n < 0");
+  if (n == 0) return DFLASH_OK;
+  NEED(x_cat, "x_cat");
+  NEED(fused, "fused");
+  Carve cv{static_cast<char*>(ws)};
+  InjectWs w = carve_inject(h, cv, n);
+  TRY(check_ws(ws, ws_bytes, cv.off));
+  return fuse_impl(h, x_cat, n, fused, w.u, w.gpart, w.ctl, static_cast<cudaStream_t>(stream));
+}
+
+dflash_status dflash_inject_kv(dflash_handle h, const void* x_cat, const void* fused, int32_t n,
+                               const int32_t* positions, const int32_t* slots, int32_t num_pages,
+                               void* const* k_pool, void* const* v_pool, void* fused_out,
+                               void* ws, size_t ws_bytes, void* stream) {
+  g_launches = 0;
+  if (!h) return fail(DFLASH_EINVAL, "null handle");
+  if (n < 0 || num_pages <= 0) return fail(DFLASH_EINVAL, "bad n or num_pages");
+  if (n == 0) return DFLASH_OK;
+  if ((x_cat == nullptr) == (fused == nullptr))
+    return fail(DFLASH_EINVAL, "exactly one of x_cat and fused must be given");
+  if (x_cat) NEED(x_cat, "x_cat");
+  if (fused) NEED(fused, "fused");
+  if (fused_out) NEED(fused_out, "fused_out");
+  NEED(positions, "positions");
+  NEED(slots, "slots");
+  if (!k_pool || !v_pool) return fail(DFLASH_EINVAL, "pool arrays are NULL");
+  for (int l = 0; l < h->c.n_layers; ++l) {
+    NEED(k_pool[l], "k_pool[l]");
+    NEED(v_pool[l], "v_pool[l]");
+  }
+  const auto& c = h->c;
+  Carve cv{static_cast<char*>(ws)};
+  InjectWs w = carve_inject(h, cv, n);
+  TRY(check_ws(ws, ws_bytes, cv.off));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const void* f = fused;
+  if (x_cat) {
+    void* dst = fused_out ? fused_out : w.fused;
+    TRY(fuse_impl(h, x_cat, n, dst, w.u, w.gpart, w.ctl, st));
+    f = dst;
+  }
+  // one GEMM per group of up to 4 layers: segments k_l | v_l
+  for (int l0 = 0; l0 < c.n_layers; l0 += kMaxSeg / 2) {
+    const int nl = std::min(kMaxSeg / 2, c.n_layers - l0);
+    WSet ws_;
+    for (int l = l0; l < l0 + nl; ++l) {
+      ws_.add(h->bf16 ? &h->m_k[l] : nullptr, h->w_k[l], c.n_kv_heads * c.head_dim);
+      ws_.add(h->bf16 ? &h->m_v[l] : nullptr, h->w_v[l], c.n_kv_heads * c.head_dim);
+    }
+    auto fill = [&](auto& e, auto* tag) {
+      using T = std::remove_pointer_t<decltype(tag)>;
+      e.pos = positions;
+      e.rope = h->d_rope;
+      e.max_pos = c.max_position;
+      e.S = c.block_size;
+      e.hq = c.n_q_heads;
+      e.hkv = c.n_kv_heads;
+      e.hd = c.head_dim;
+      for (int l = 0; l < nl; ++l) {
+        e.kpool[l] = static_cast<T*>(k_pool[l0 + l]);
+        e.vpool[l] = static_cast<T*>(v_pool[l0 + l]);
+      }
+      e.slots = slots;
+      e.num_slots = (long long)num_pages * kPage;
+      e.err = h->d_err;
+    };
+    if (h->bf16) {
+      EpiArgs<bf16> e = {};
+      fill(e, static_cast<bf16*>(nullptr));
+      TRY((gemm<EPI_KV, bf16>(h, f, n, c.d_model, ws_, e, w.gpart, w.ctl, st)));
+    } else {
+      EpiArgs<float> e = {};
+      fill(e, static_cast<float*>(nullptr));
+      TRY((gemm<EPI_KV, float>(h, f, n, c.d_model, ws_, e, w.gpart, w.ctl, st)));
+    }
+  }
+  return DFLASH_OK;
+}
+
+dflash_status dflash_draft_block(dflash_handle h, const int32_t* block_ids,
+                                 const int32_t* ctx_lens, const int32_t* page_table,
+                                 int32_t max_pages, int32_t batch, int32_t num_pages,
+                                 void* const* k_pool, void* const* v_pool, void* final_hidden,
+                                 void* ws, size_t ws_bytes, void* stream) {
+  g_launches = 0;
+  if (!h) return fail(DFLASH_EINVAL, "null handle");
+  if (batch < 0 || max_pages < 0 || num_pages <= 0) return fail(DFLASH_EINVAL, "bad sizes");
+  if (batch == 0) return DFLASH_OK;
+  NEED(block_ids, "block_ids");
+  NEED(ctx_lens, "ctx_lens");
+  if (max_pages > 0) NEED(page_table, "page_table");
+  NEED(final_hidden, "final_hidden");
+  if (!k_pool || !v_pool) return fail(DFLASH_EINVAL, "pool arrays are NULL");
+  for (int l = 0; l < h->c.n_layers; ++l) {
+    NEED(k_pool[l], "k_pool[l]");
+    NEED(v_pool[l], "v_pool[l]");
+  }
+  if ((long long)batch * h->c.block_size > (1 << 20)) return fail(DFLASH_EUNSUPPORTED, "batch too large");
+  Carve cv{static_cast<char*>(ws)};
+  DraftWs w = carve_draft(h, cv, batch, max_pages);
+  TRY(check_ws(ws, ws_bytes, cv.off));
+  if ((long long)batch * h->c.n_kv_heads > kCtlWords) return fail(DFLASH_EUNSUPPORTED, "batch too large");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (h->bf16)
+    return draft_impl<bf16>(h, block_ids, ctx_lens, page_table, max_pages, batch, num_pages,
+                            k_pool, v_pool, final_hidden, w, st);
+  return draft_impl<float>(h, block_ids, ctx_lens, page_table, max_pages, batch, num_pages,
+                           k_pool, v_pool, final_hidden, w, st);
+}
+
+dflash_status dflash_lm_head_argmax(dflash_handle h, const void* hidden, int32_t rows,
+                                    float temperature, int32_t* tokens, float* max_logit,
+                                    float* lse, void* ws, size_t ws_bytes, void* stream) {
+  g_launches = 0;
+  if (!h) return fail(DFLASH_EINVAL, "null handle");
+  if (rows < 0) return fail(DFLASH_EINVAL, "rows < 0");
+  if (rows == 0) return DFLASH_OK;
+  NEED(hidden, "hidden");
+  NEED(tokens, "tokens");
+  if (max_logit) NEED(max_logit, "max_logit");
+  if (lse) NEED(lse, "lse");
+  if (lse && !(temperature > 0.f)) return fail(DFLASH_EINVAL, "temperature must be > 0");
+  if (!(temperature > 0.f)) temperature = 1.0f;
+  Carve cv{static_cast<char*>(ws)};
+  HeadWs w = carve_head(h, cv, rows);
+  TRY(check_ws(ws, ws_bytes, cv.off));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (h->bf16) return head_impl<bf16>(h, hidden, rows, temperature, tokens, max_logit, lse, w, st);
+  return head_impl<float>(h, hidden, rows, temperature, tokens, max_logit, lse, w, st);
+}
+
+dflash_status dflash_verify_greedy(dflash_handle h, const int32_t* draft,
+                                   const void* target_logits, int32_t batch, int32_t* out_tokens,
+                                   int32_t* n_accepted, int32_t* n_emitted, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  g_launches = 0;
+  if (!h) return fail(DFLASH_EINVAL, "null handle");
+  if (batch < 0) return fail(DFLASH_EINVAL, "batch < 0");
+  if (batch == 0) return DFLASH_OK;
+  NEED(draft, "draft");
+  NEED(target_logits, "target_logits");
+  NEED(out_tokens, "out_tokens");
+  NEED(n_accepted, "n_accepted");
+  NEED(n_emitted, "n_emitted");
+  const int S = h->c.block_size, V = h->c.vocab, rows = batch * S;
+  if (S > 64) return fail(DFLASH_EUNSUPPORTED, "block_size > 64");
+  if (rows > 65535) return fail(DFLASH_EUNSUPPORTED, "batch*block_size > 65535");
+  Carve cv{static_cast<char*>(ws)};
+  VerifyWs w = carve_verify(h, cv, batch, false);
+  TRY(check_ws(ws, ws_bytes, cv.off));
+  const int nch = verify_chunks(h, rows), chunk = chunk_of(h, nch);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (h->bf16)
+    return launch(k_verify_greedy<bf16>, dim3(nch, rows), dim3(kRowThreads), 0, st,
+                  static_cast<const bf16*>(target_logits), draft, S, V, chunk, w.pv, w.pi, w.ctl,
+                  out_tokens, n_accepted, n_emitted, h->d_err);
+  return launch(k_verify_greedy<float>, dim3(nch, rows), dim3(kRowThreads), 0, st,
+                static_cast<const float*>(target_logits), draft, S, V, chunk, w.pv, w.pi, w.ctl,
+                out_tokens, n_accepted, n_emitted, h->d_err);
+}
+
+dflash_status dflash_verify_sample(dflash_handle h, const int32_t* draft, const void* final_hidden,
+                                   const float* draft_max, const float* draft_lse,
+                                   const void* target_logits, const float* uniforms,
+                                   float temperature, int32_t batch, int32_t* out_tokens,
+                                   int32_t* n_accepted, int32_t* n_emitted, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  g_launches = 0;
+  if (!h) return fail(DFLASH_EINVAL, "null handle");
+  if (batch < 0) return fail(DFLASH_EINVAL, "batch < 0");
+  if (!(temperature > 0.f)) return fail(DFLASH_EINVAL, "temperature must be > 0");
+  if (batch == 0) return DFLASH_OK;
+  NEED(draft, "draft");
+  NEED(final_hidden, "final_hidden");
+  NEED(draft_max, "draft_max");
+  NEED(draft_lse, "draft_lse");
+  NEED(target_logits, "target_logits");
+  NEED(uniforms, "uniforms");
+  NEED(out_tokens, "out_tokens");
+  NEED(n_accepted, "n_accepted");
+  NEED(n_emitted, "n_emitted");
+  const int rows = batch * h->c.block_size;
+  if (rows > 65535 || rows + batch > kCtlWords) return fail(DFLASH_EUNSUPPORTED, "batch too large");
+  Carve cv{static_cast<char*>(ws)};
+  VerifyWs w = carve_verify(h, cv, batch, true);
+  TRY(check_ws(ws, ws_bytes, cv.off));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (h->bf16)
+    return sample_impl<bf16>(h, draft, final_hidden, draft_max, draft_lse, target_logits, uniforms,
+                             temperature, batch, out_tokens, n_accepted, n_emitted, w, st);
+  return sample_impl<float>(h, draft, final_hidden, draft_max, draft_lse, target_logits, uniforms,
+                            temperature, batch, out_tokens, n_accepted, n_emitted, w, st);
+}
+
+dflash_status dflash_get_device_error(dflash_handle h, int32_t* code, int32_t clear) {
+  if (!h || !code) return fail(DFLASH_EINVAL, "null argument");
+  CUDA_TRY(cudaDeviceSynchronize());
+  CUDA_TRY(cudaMemcpy(code, h->d_err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (clear) CUDA_TRY(cudaMemset(h->d_err, 0, sizeof(int)));
+  return DFLASH_OK;
+}
+
+}  // extern "C"

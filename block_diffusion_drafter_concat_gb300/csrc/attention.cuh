@@ -1,0 +1,364 @@
+// Block attention of the drafter over the paged context cache plus the block itself.
+//
+// For sequence b and kv head g the S*G query rows (block slot i, q head g*G + hh, row
+// i*G + hh) attend, with no mask, to the sequence's ctx_len cached context keys
+// (injected target features) followed by the block's own S keys.  Keys are walked a
+// 16-token page at a time; the work of one (b, g) is split over CTAs by contiguous
+// ranges of pages (split-context, "flash-decoding"), each CTA keeps an online softmax
+// (running max in the log2 domain, running sum, unnormalised output) and publishes
+// it; the last CTA of the group combines them in split order and writes the bf16
+// attention output in [B*S, hq*hd] layout for the output projection.
+//
+// bf16 kernel: K and V pages arrive by TMA (two-dimensional view of the pool,
+// 16 x 64 boxes, 128-byte swizzle) in a ring of mbarrier-tracked stages; QK^T and PV
+// run on mma.sync.m16n8k16 with the probabilities re-used from the score registers.
+#pragma once
+
+#include "common.cuh"
+
+namespace dflash {
+
+template <typename T>
+struct AttnArgs {
+  const T* q;        // [B][hkv][QR][hd]
+  const T* kb;       // [B][hkv][S][hd]  (fp32 path reads these directly)
+  const T* vb;
+  const T* kpool;    // fp32 path: the layer's pools
+  const T* vpool;
+  const int* page_table;
+  int max_pages;
+  const int* ctx_lens;
+  int num_pages;
+  int S, hq, hkv, hd, QR;
+  int pps;           // key pages per split
+  int nsplit;
+  float* part_o;     // [B][hkv][nsplit][QR][hd]
+  float* part_ml;    // [B][hkv][nsplit][QR][2]
+  int* counters;     // [B*hkv]
+  T* out;            // [B*S][hq*hd]
+  int* err;
+};
+
+struct AttnMaps {
+  CUtensorMap k, v, kb, vb;
+};
+
+// Combine the published splits of group (b, g): out = sum_s w_s o_s / sum_s w_s l_s.
+template <typename T>
+__device__ void attn_combine(const AttnArgs<T>& a, int b, int g, int ns, float* wsm,
+                             int tid, int nthr) {
+  const int QR = a.QR, hd = a.hd, G = a.hq / a.hkv;
+  const long long grp = (long long)b * a.hkv + g;
+  const float* ml = a.part_ml + grp * a.nsplit * QR * 2;
+  for (int r = tid; r < QR; r += nthr) {
+    float M = -INFINITY;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(ml + ((long long)s * QR + r) * 2));
+    float L = 0.f;
+    for (int s = 0; s < ns; ++s) {
+      float w = exp2f(__ldcg(ml + ((long long)s * QR + r) * 2) - M);
+      wsm[s * QR + r] = w;
+      L += w * __ldcg(ml + ((long long)s * QR + r) * 2 + 1);
+    }
+    float inv = 1.f / L;
+    for (int s = 0; s < ns; ++s) wsm[s * QR + r] *= inv;
+  }
+  __syncthreads();
+  const float* po = a.part_o + grp * a.nsplit * QR * hd;
+  for (int x = tid; x < QR * hd; x += nthr) {
+    int r = x / hd, d = x % hd;
+    float acc = 0.f;
+    for (int s = 0; s < ns; ++s) acc += wsm[s * QR + r] * __ldcg(po + (long long)s * QR * hd + x);
+    int i = r / G, hh = r % G;
+    a.out[((long long)b * a.S + i) * (a.hq * hd) + (g * G + hh) * hd + d] = from_f32<T>(acc);
+  }
+}
+
+// ------------------------------------------------------------------ bf16 tensor core
+template <int HD>
+struct AttnCfg {
+  static constexpr int NS = 4;
+  static constexpr int TILE = kPage * HD * 2;   // one K (or V) page of one head
+  static constexpr int STAGE = 2 * TILE;
+  static constexpr int MAXSPLIT = 64;
+};
+
+template <int HD, int NW>
+__global__ void __launch_bounds__((NW + 1) * 32)
+    k_attn_tc(const __grid_constant__ AttnMaps maps, const AttnArgs<bf16> a) {
+  using C = AttnCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::NS * C::STAGE);
+  uint64_t* empty = full + C::NS;
+  int* flag = reinterpret_cast<int*>(empty + C::NS);
+  float* wsm = reinterpret_cast<float*>(smem);  // combine weights reuse the ring
+
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_launch_dependents();
+  pdl_wait();
+
+  const int T = a.ctx_lens[b];
+  if (T < 0 || T > a.max_pages * kPage) {
+    if (tid == 0) raise_error(a.err, DFLASH_DEV_BAD_INDEX);
+    return;
+  }
+  const int np = (T + kPage - 1) / kPage;   // context pages
+  const int kp = np + 1;                    // + the block's own keys
+  const int ns = (kp + a.pps - 1) / a.pps;
+  if (split >= ns) return;                  // this split is past the sequence's keys
+  const int p0 = split * a.pps, p1 = min(kp, p0 + a.pps);
+  const int nmy = p1 - p0;
+
+  if (tid == 0) {
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NW);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == NW) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < nmy; ++i) {
+        const int s = i % C::NS;
+        if (i >= C::NS && !mbar_wait(&empty[s], ((i / C::NS) - 1) & 1)) {
+          raise_error(a.err, DFLASH_DEV_TIMEOUT);
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], C::STAGE);
+        uint8_t* kd = stages + s * C::STAGE;
+        uint8_t* vd = kd + C::TILE;
+        const int pg = p0 + i;
+        const CUtensorMap *mk, *mv;
+        int row;
+        if (pg < np) {
+          int page = a.page_table[(long long)b * a.max_pages + pg];
+          if (page < 0 || page >= a.num_pages) {
+            raise_error(a.err, DFLASH_DEV_BAD_INDEX);
+            page = 0;
+          }
+          mk = &maps.k; mv = &maps.v;
+          row = (page * a.hkv + g) * kPage;
+        } else {
+          mk = &maps.kb; mv = &maps.vb;
+          row = (b * a.hkv + g) * a.S;
+        }
+#pragma unroll
+        for (int bx = 0; bx < HD / 64; ++bx) {
+          tma_load_2d(kd + bx * 2048, mk, &full[s], bx * 64, row);
+          tma_load_2d(vd + bx * 2048, mv, &full[s], bx * 64, row);
+        }
+        issued = i + 1;
+      }
+      for (int i = max(0, issued - C::NS); i < issued; ++i) mbar_wait(&full[i % C::NS], (i / C::NS) & 1);
+    }
+  } else {
+    // ------------------------------------------------------------------ consumers
+    const int g8 = lane >> 2, t4 = lane & 3, mi = lane >> 3, r8 = lane & 7;
+    const int qr0 = warp * 16;
+    const bf16* qb = a.q + (((long long)b * a.hkv + g) * a.QR + qr0) * HD;
+    uint32_t qf[HD / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      qf[kk][0] = *reinterpret_cast<const uint32_t*>(qb + (g8)*HD + kk * 16 + 2 * t4);
+      qf[kk][1] = *reinterpret_cast<const uint32_t*>(qb + (g8 + 8) * HD + kk * 16 + 2 * t4);
+      qf[kk][2] = *reinterpret_cast<const uint32_t*>(qb + (g8)*HD + kk * 16 + 8 + 2 * t4);
+      qf[kk][3] = *reinterpret_cast<const uint32_t*>(qb + (g8 + 8) * HD + kk * 16 + 8 + 2 * t4);
+    }
+    float o[HD / 8][4];
+#pragma unroll
+    for (int j = 0; j < HD / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const float sc = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
+    for (int i = 0; i < nmy; ++i) {
+      const int s = i % C::NS;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (i / C::NS) & 1))) {
+        if (lane == 0) raise_error(a.err, DFLASH_DEV_TIMEOUT);
+        break;
+      }
+      const int pg = p0 + i;
+      const int valid = (pg < np) ? min(kPage, T - pg * kPage) : a.S;
+      const uint32_t kbase = smem_u32(stages + s * C::STAGE);
+      const uint32_t vbase = kbase + C::TILE;
+      float sacc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        uint32_t kf[4];
+        const int key = (mi >> 1) * 8 + r8;
+        const int ch = kk * 2 + (mi & 1);
+        ldsm_x4(kf, kbase + (ch >> 3) * 2048 + swz128(key, ch & 7));
+        mma_bf16(sacc[0], qf[kk], kf[0], kf[1]);
+        mma_bf16(sacc[1], qf[kk], kf[2], kf[3]);
+      }
+      // scores -> log2 domain, mask keys past `valid`
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          int key = n * 8 + 2 * t4 + (c & 1);
+          sacc[n][c] = key < valid ? sacc[n][c] * sc : -INFINITY;
+        }
+      float mx0 = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
+      float mx1 = fmaxf(fmaxf(sacc[0][2], sacc[0][3]), fmaxf(sacc[1][2], sacc[1][3]));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
+      const float al0 = exp2f(m0 - nm0), al1 = exp2f(m1 - nm1);
+      m0 = nm0;
+      m1 = nm1;
+      float p[2][4];
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        p[n][0] = exp2f(sacc[n][0] - nm0);
+        p[n][1] = exp2f(sacc[n][1] - nm0);
+        p[n][2] = exp2f(sacc[n][2] - nm1);
+        p[n][3] = exp2f(sacc[n][3] - nm1);
+      }
+      l0 = l0 * al0 + p[0][0] + p[0][1] + p[1][0] + p[1][1];
+      l1 = l1 * al1 + p[0][2] + p[0][3] + p[1][2] + p[1][3];
+#pragma unroll
+      for (int j = 0; j < HD / 8; ++j) {
+        o[j][0] *= al0; o[j][1] *= al0;
+        o[j][2] *= al1; o[j][3] *= al1;
+      }
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(p[0][0], p[0][1]);
+      pa[1] = pack_bf16x2(p[0][2], p[0][3]);
+      pa[2] = pack_bf16x2(p[1][0], p[1][1]);
+      pa[3] = pack_bf16x2(p[1][2], p[1][3]);
+#pragma unroll
+      for (int dj = 0; dj < HD / 16; ++dj) {
+        uint32_t vf[4];
+        const int key = (mi & 1) * 8 + r8;
+        const int ch = dj * 2 + (mi >> 1);
+        ldsm_x4_trans(vf, vbase + (ch >> 3) * 2048 + swz128(key, ch & 7));
+        mma_bf16(o[2 * dj], pa, vf[0], vf[1]);
+        mma_bf16(o[2 * dj + 1], pa, vf[2], vf[3]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const long long grp = (long long)b * a.hkv + g;
+    float* po = a.part_o + ((grp * a.nsplit + split) * a.QR + qr0) * HD;
+#pragma unroll
+    for (int j = 0; j < HD / 8; ++j) {
+      int d = j * 8 + 2 * t4;
+      *reinterpret_cast<float2*>(po + g8 * HD + d) = make_float2(o[j][0], o[j][1]);
+      *reinterpret_cast<float2*>(po + (g8 + 8) * HD + d) = make_float2(o[j][2], o[j][3]);
+    }
+    if (t4 == 0) {
+      float* pm = a.part_ml + ((grp * a.nsplit + split) * a.QR + qr0) * 2;
+      pm[g8 * 2] = m0;
+      pm[g8 * 2 + 1] = l0;
+      pm[(g8 + 8) * 2] = m1;
+      pm[(g8 + 8) * 2 + 1] = l1;
+    }
+  }
+  if (elect_last(&a.counters[(long long)b * a.hkv + g], ns, flag))
+    attn_combine<bf16>(a, b, g, ns, wsm, tid, (NW + 1) * 32);
+}
+
+// ---------------------------------------------------------------------- fp32 path
+// Plain FFMA attention for fp32 workloads (small shapes), same splits and combine.
+static __global__ void __launch_bounds__(128) k_attn_f32(const AttnArgs<float> a) {
+  extern __shared__ float sm[];
+  const int QR = a.QR, hd = a.hd;
+  float* Qs = sm;                    // [QR][hd]
+  float* Os = Qs + QR * hd;          // [QR][hd]
+  float* Ks = Os + QR * hd;          // [16][hd]
+  float* Vs = Ks + kPage * hd;       // [16][hd]
+  float* Ss = Vs + kPage * hd;       // [QR][16]
+  float* mrow = Ss + QR * kPage;     // [QR]
+  float* lrow = mrow + QR;
+  float* arow = lrow + QR;
+  __shared__ int flag;
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int T = a.ctx_lens[b];
+  if (T < 0 || T > a.max_pages * kPage) {
+    if (tid == 0) raise_error(a.err, DFLASH_DEV_BAD_INDEX);
+    return;
+  }
+  const int np = (T + kPage - 1) / kPage, kp = np + 1;
+  const int ns = (kp + a.pps - 1) / a.pps;
+  if (split >= ns) return;
+  const int p0 = split * a.pps, p1 = min(kp, p0 + a.pps);
+  const long long grp = (long long)b * a.hkv + g;
+  for (int x = tid; x < QR * hd; x += 128) {
+    Qs[x] = a.q[grp * QR * hd + x];
+    Os[x] = 0.f;
+  }
+  for (int r = tid; r < QR; r += 128) { mrow[r] = -INFINITY; lrow[r] = 0.f; }
+  const float sc = 1.4426950408889634f / sqrtf(static_cast<float>(hd));
+  __syncthreads();
+  for (int pg = p0; pg < p1; ++pg) {
+    int valid;
+    const float *ksrc, *vsrc;
+    if (pg < np) {
+      int page = a.page_table[(long long)b * a.max_pages + pg];
+      if (page < 0 || page >= a.num_pages) {
+        if (tid == 0) raise_error(a.err, DFLASH_DEV_BAD_INDEX);
+        page = 0;
+      }
+      valid = min(kPage, T - pg * kPage);
+      ksrc = a.kpool + ((long long)page * a.hkv + g) * kPage * hd;
+      vsrc = a.vpool + ((long long)page * a.hkv + g) * kPage * hd;
+    } else {
+      valid = a.S;
+      ksrc = a.kb + grp * a.S * hd;
+      vsrc = a.vb + grp * a.S * hd;
+    }
+    for (int x = tid; x < kPage * hd; x += 128) {
+      bool in = x / hd < valid;
+      Ks[x] = in ? ksrc[x] : 0.f;
+      Vs[x] = in ? vsrc[x] : 0.f;
+    }
+    __syncthreads();
+    for (int x = tid; x < QR * kPage; x += 128) {
+      int r = x / kPage, k = x % kPage;
+      float s = 0.f;
+      for (int d = 0; d < hd; ++d) s = fmaf(Qs[r * hd + d], Ks[k * hd + d], s);
+      Ss[x] = k < valid ? s * sc : -INFINITY;
+    }
+    __syncthreads();
+    for (int r = tid; r < QR; r += 128) {
+      float mx = mrow[r];
+      for (int k = 0; k < kPage; ++k) mx = fmaxf(mx, Ss[r * kPage + k]);
+      float al = exp2f(mrow[r] - mx), sum = 0.f;
+      for (int k = 0; k < kPage; ++k) {
+        float p = exp2f(Ss[r * kPage + k] - mx);
+        Ss[r * kPage + k] = p;
+        sum += p;
+      }
+      lrow[r] = lrow[r] * al + sum;
+      mrow[r] = mx;
+      arow[r] = al;
+    }
+    __syncthreads();
+    for (int x = tid; x < QR * hd; x += 128) {
+      int r = x / hd, d = x % hd;
+      float acc = Os[x] * arow[r];
+      for (int k = 0; k < kPage; ++k) acc = fmaf(Ss[r * kPage + k], Vs[k * hd + d], acc);
+      Os[x] = acc;
+    }
+    __syncthreads();
+  }
+  float* po = a.part_o + (grp * a.nsplit + split) * QR * hd;
+  for (int x = tid; x < QR * hd; x += 128) po[x] = Os[x];
+  float* pm = a.part_ml + (grp * a.nsplit + split) * QR * 2;
+  for (int r = tid; r < QR; r += 128) { pm[2 * r] = mrow[r]; pm[2 * r + 1] = lrow[r]; }
+  if (elect_last(&a.counters[grp], ns, &flag)) attn_combine<float>(a, b, g, ns, Qs, tid, 128);
+}
+
+}  // namespace dflash

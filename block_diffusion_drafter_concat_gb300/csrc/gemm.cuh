@@ -1,0 +1,480 @@
+// Weight-streaming GEMM  Y[M, N] = A[M, K] * W[N, K]^T  with fused epilogues.
+//
+// Every projection of the drafter step is one of these: the fused-feature projection,
+// the injected K/V projections, Q/K/V, O, gate/up, down and the LM head.  At batch 1
+// the block has 16 rows, so the contraction is a stream of weights past a small
+// activation tile: the tensor-core kernel puts 128 weight rows on the MMA's M side and
+// the activation rows on its N side (swap-AB), pulls 128x64 weight boxes and BNx64
+// activation boxes into a shared-memory ring with TMA (128-byte swizzle, mbarrier
+// completion), and runs ldmatrix + mma.sync.m16n8k16 (bf16 in, fp32 accumulate).
+//
+// Work is split "stream-K" style: the (m-block, n-tile, k-stage) units are cut into
+// one contiguous range per persistent CTA, so every SM streams the same number of
+// weight bytes whatever the shape.  A tile cut between CTAs is finished by the last
+// contributor to arrive, which sums the published partial tiles in contributor order
+// (deterministic) and runs the epilogue.  Weight boxes of the first stages are issued
+// before griddepcontrol.wait, overlapping the previous kernel's tail.
+#pragma once
+
+#include "common.cuh"
+
+namespace dflash {
+
+constexpr int kMaxSeg = 8;
+
+enum Epi : int {
+  EPI_F32 = 0,    // y[m, n] = v (fp32)
+  EPI_QKV = 1,    // segments q | k | v: RoPE on q and k, bf16 into attention layouts
+  EPI_KV = 2,     // segments k0 | v0 | k1 | v1 ...: RoPE on k, scatter into cache pages
+  EPI_RESID = 3,  // x[m, n] += v (fp32 residual stream)
+  EPI_SWIGLU = 4, // paired tiles (64 gate rows | 64 up rows): act = silu(g) * u
+  EPI_ARGMAX = 5  // per-tile (max, argmax, sum exp) of each row for the LM head
+};
+
+struct WMaps {
+  CUtensorMap m[kMaxSeg];
+};
+
+template <typename T>
+struct EpiArgs {
+  int M, N;
+  float* y;
+  int ldy;
+  // rotary / attention layouts
+  const int* pos;
+  const float2* rope;  // [max_position][head_dim/2] (cos, sin)
+  int max_pos;
+  int S, hq, hkv, hd;
+  T* q;    // [B][hkv][S*G][hd]
+  T* kb;   // [B][hkv][S][hd]
+  T* vb;   // [B][hkv][S][hd]
+  // cache injection
+  T* kpool[kMaxSeg / 2];
+  T* vpool[kMaxSeg / 2];
+  const int* slots;
+  long long num_slots;
+  // SwiGLU
+  T* act;
+  int F;
+  // LM-head argmax partials, [n_tiles][M]
+  float* am_max;
+  int* am_idx;
+  float* am_sum;
+  float inv_temp;
+  int want_sum;
+  int* err;
+};
+
+struct GemmShape {
+  int M, K, n_tiles, ks, m_blocks, paired, nseg;
+  long long units;
+  int seg_tile0[kMaxSeg + 1];
+  int seg_rows[kMaxSeg];  // rows of each weight matrix
+  float* part;      // [grid][2][BN][kBM] partial tiles
+  int* counters;    // one per output tile
+};
+
+// ---------------------------------------------------------------------------- epilogue
+// Cs: the finished fp32 tile, Cs[r * pitch + c] for activation row m0 + r and output
+// column c of n-tile nt.  Runs on `nthr` threads (thread index `tid`).
+template <typename T, int EPI>
+__device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt,
+                              const GemmShape& g, const EpiArgs<T>& e, int tid, int nthr) {
+  int seg = 0;
+  while (seg + 1 < g.nseg && nt >= g.seg_tile0[seg + 1]) ++seg;
+  const int rows_per_tile = g.paired ? kBM / 2 : kBM;
+  const int r0 = (nt - g.seg_tile0[seg]) * rows_per_tile;  // first row within the segment
+  const int mr = min(BN, e.M - m0);
+
+  if constexpr (EPI == EPI_F32 || EPI == EPI_RESID) {
+    const int nc = min(kBM, e.N - nt * kBM);
+    for (int i = tid; i < mr * kBM; i += nthr) {
+      int r = i / kBM, c = i % kBM;
+      if (c >= nc) continue;
+      float v = Cs[r * pitch + c];
+      float* dst = e.y + (long long)(m0 + r) * e.ldy + nt * kBM + c;
+      if constexpr (EPI == EPI_RESID) *dst += v; else *dst = v;
+    }
+  } else if constexpr (EPI == EPI_SWIGLU) {
+    for (int i = tid; i < mr * 64; i += nthr) {
+      int r = i / 64, c = i % 64;
+      int f = r0 + c;
+      if (f >= e.F) continue;
+      float gt = Cs[r * pitch + c], up = Cs[r * pitch + 64 + c];
+      float s = gt / (1.0f + __expf(-gt));
+      e.act[(long long)(m0 + r) * e.F + f] = from_f32<T>(s * up);
+    }
+  } else if constexpr (EPI == EPI_QKV || EPI == EPI_KV) {
+    const int hd = e.hd, half = hd >> 1;
+    // segment kind: 0 = q, 1 = k, 2 = v
+    int kind, layer = 0;
+    if constexpr (EPI == EPI_QKV) kind = seg;
+    else { layer = seg >> 1; kind = 1 + (seg & 1); }
+    const int G = e.hq / e.hkv;
+    if (kind == 2) {
+      for (int i = tid; i < mr * kBM; i += nthr) {
+        int r = i / kBM, c = i % kBM;
+        int f = r0 + c, m = m0 + r;
+        int head = f / hd, j = f % hd;
+        if (head >= e.hkv) continue;
+        T v = from_f32<T>(Cs[r * pitch + c]);
+        if constexpr (EPI == EPI_QKV) {
+          int b = m / e.S, ii = m % e.S;
+          e.vb[(((long long)b * e.hkv + head) * e.S + ii) * hd + j] = v;
+        } else {
+          int slot = e.slots[m];
+          if (slot < 0 || slot >= e.num_slots) { raise_error(e.err, DFLASH_DEV_BAD_INDEX); continue; }
+          long long page = slot / kPage, off = slot % kPage;
+          e.vpool[layer][((page * e.hkv + head) * kPage + off) * hd + j] = v;
+        }
+      }
+    } else {
+      // rotary pairs (j, j + hd/2) of one head lie in the same 128-column tile
+      for (int i = tid; i < mr * (kBM / 2); i += nthr) {
+        int r = i / (kBM / 2), cc = i % (kBM / 2);
+        int hl = cc / half, j = cc % half;
+        int c = hl * hd + j;
+        int f = r0 + c, m = m0 + r;
+        int head = f / hd;
+        int nheads = (kind == 0) ? e.hq : e.hkv;
+        if (head >= nheads) continue;
+        int p = e.pos[m];
+        if (p < 0 || p >= e.max_pos) { raise_error(e.err, DFLASH_DEV_BAD_POSITION); continue; }
+        float2 cs = e.rope[(long long)p * half + j];
+        float x0 = Cs[r * pitch + c], x1 = Cs[r * pitch + c + half];
+        T y0 = from_f32<T>(x0 * cs.x - x1 * cs.y);
+        T y1 = from_f32<T>(x1 * cs.x + x0 * cs.y);
+        long long base;
+        if constexpr (EPI == EPI_QKV) {
+          int b = m / e.S, ii = m % e.S;
+          if (kind == 0) {
+            int gk = head / G, hh = head % G;
+            base = ((((long long)b * e.hkv + gk) * e.S + ii) * G + hh) * hd;
+            e.q[base + j] = y0;
+            e.q[base + j + half] = y1;
+          } else {
+            base = (((long long)b * e.hkv + head) * e.S + ii) * hd;
+            e.kb[base + j] = y0;
+            e.kb[base + j + half] = y1;
+          }
+        } else {
+          int slot = e.slots[m];
+          if (slot < 0 || slot >= e.num_slots) { raise_error(e.err, DFLASH_DEV_BAD_INDEX); continue; }
+          long long page = slot / kPage, off = slot % kPage;
+          base = ((page * e.hkv + head) * kPage + off) * hd;
+          e.kpool[layer][base + j] = y0;
+          e.kpool[layer][base + j + half] = y1;
+        }
+      }
+    }
+  } else if constexpr (EPI == EPI_ARGMAX) {
+    // one warp per row: lanes cover the 128 columns, then a (max, idx) shuffle reduce
+    const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
+    const int nc = min(kBM, e.N - nt * kBM);
+    for (int r = warp; r < mr; r += nw) {
+      float best = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int c = lane; c < nc; c += 32) {
+        float v = Cs[r * pitch + c];
+        if (v > best) { best = v; bi = nt * kBM + c; }
+      }
+      warp_argmax(best, bi);
+      float s = 0.f;
+      if (e.want_sum) {
+        for (int c = lane; c < nc; c += 32) s += __expf((Cs[r * pitch + c] - best) * e.inv_temp);
+        s = warp_sum(s);
+      }
+      if (lane == 0) {
+        long long o = (long long)nt * e.M + m0 + r;
+        e.am_max[o] = best;
+        e.am_idx[o] = bi;
+        e.am_sum[o] = s;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------- tensor-core kernel
+template <int BN>
+struct TcCfg {
+  static constexpr int NS = BN == 16 ? 10 : BN == 32 ? 8 : BN == 64 ? 6 : 4;
+  static constexpr int W_BYTES = kBM * kBK * 2;
+  static constexpr int A_BYTES = BN * kBK * 2;
+  static constexpr int STAGE = W_BYTES + A_BYTES;
+  static constexpr int PITCH = kBM + 4;
+  static constexpr int CS_BYTES = BN * PITCH * 4;
+  static constexpr int SMEM = 1024 /*align slack*/ + NS * STAGE + CS_BYTES + 2 * NS * 8 + 16;
+  static constexpr int THREADS = 160;  // 4 consumer warps + 1 TMA producer warp
+};
+
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// Range of units [u0, u1) of CTA c out of `grid`.
+__device__ __forceinline__ void cta_range(long long units, int c, int grid, long long& u0,
+                                          long long& u1) {
+  u0 = units * c / grid;
+  u1 = units * (c + 1) / grid;
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(160, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ WMaps wm,
+              const GemmShape g, const EpiArgs<bf16> e) {
+  using C = TcCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  float* Cs = reinterpret_cast<float*>(smem + C::NS * C::STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::NS * C::STAGE + C::CS_BYTES);
+  uint64_t* empty = full + C::NS;
+  int* flag = reinterpret_cast<int*>(empty + C::NS);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int grid = gridDim.x, cta = blockIdx.x;
+  long long u0, u1;
+  cta_range(g.units, cta, grid, u0, u1);
+  const int n_my = static_cast<int>(u1 - u0);
+
+  if (tid == 0) {
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 4);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      const uint64_t pol = policy_evict_first();
+      auto unit_coords = [&](long long u, int& t, int& ks, int& mb, int& nt) {
+        t = static_cast<int>(u / g.ks);
+        ks = static_cast<int>(u % g.ks);
+        mb = t / g.n_tiles;
+        nt = t % g.n_tiles;
+      };
+      auto issue_w = [&](int i, long long u) {
+        int t, ks, mb, nt;
+        unit_coords(u, t, ks, mb, nt);
+        uint8_t* st = stages + (i % C::NS) * C::STAGE;
+        int seg = 0;
+        while (seg + 1 < g.nseg && nt >= g.seg_tile0[seg + 1]) ++seg;
+        if (g.paired) {
+          int row = (nt - g.seg_tile0[seg]) * (kBM / 2);
+          tma_load_2d_hint(st, &wm.m[0], &full[i % C::NS], ks * kBK, row, pol);
+          tma_load_2d_hint(st + C::W_BYTES / 2, &wm.m[1], &full[i % C::NS], ks * kBK, row, pol);
+        } else {
+          int row = (nt - g.seg_tile0[seg]) * kBM;
+          tma_load_2d_hint(st, &wm.m[seg], &full[i % C::NS], ks * kBK, row, pol);
+        }
+      };
+      auto issue_a = [&](int i, long long u) {
+        int t, ks, mb, nt;
+        unit_coords(u, t, ks, mb, nt);
+        uint8_t* st = stages + (i % C::NS) * C::STAGE + C::W_BYTES;
+        tma_load_2d(st, &tmA, &full[i % C::NS], ks * kBK, mb * BN);
+      };
+      const int pre = min(C::NS, n_my);
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], C::STAGE);
+        issue_w(i, u0 + i);
+      }
+      pdl_wait();  // activations are written by the previous kernel
+      for (int i = 0; i < pre; ++i) issue_a(i, u0 + i);
+      int issued = pre;
+      for (int i = pre; i < n_my; ++i) {
+        if (!mbar_wait(&empty[i % C::NS], ((i / C::NS) - 1) & 1)) {
+          raise_error(e.err, DFLASH_DEV_TIMEOUT);
+          break;
+        }
+        mbar_arrive_expect_tx(&full[i % C::NS], C::STAGE);
+        issue_w(i, u0 + i);
+        issue_a(i, u0 + i);
+        issued = i + 1;
+      }
+      // never leave with copies in flight
+      for (int i = max(0, issued - C::NS); i < issued; ++i) mbar_wait(&full[i % C::NS], (i / C::NS) & 1);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------------- consumers
+  pdl_wait();
+  constexpr int NB = BN / 8;  // n8 tiles of activation rows
+  float acc[2][NB][4];
+  const int g8 = lane >> 2, t4 = lane & 3, mi = lane >> 3, r8 = lane & 7;
+  bool ok = true;
+  long long u = u0;
+  int i = 0;
+  while (u < u1) {
+    const int t = static_cast<int>(u / g.ks);
+    const int ks0 = static_cast<int>(u % g.ks);
+    const long long tile_end = static_cast<long long>(t + 1) * g.ks;
+    const long long seg_end = min(tile_end, u1);
+    const int nk = static_cast<int>(seg_end - u);
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.f;
+    for (int k = 0; k < nk; ++k, ++i) {
+      const int s = i % C::NS;
+      // After a timeout the warp keeps walking the same units and barriers (without
+      // waiting or computing) so that no named barrier is left short of a warp.
+      if (ok && !__all_sync(0xffffffffu, mbar_wait(&full[s], (i / C::NS) & 1))) {
+        if (lane == 0) raise_error(e.err, DFLASH_DEV_TIMEOUT);
+        ok = false;
+      }
+      if (!ok) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        continue;
+      }
+      const uint32_t wbase = smem_u32(stages + s * C::STAGE);
+      const uint32_t abase = wbase + C::W_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t a[2][4];
+#pragma unroll
+        for (int ms = 0; ms < 2; ++ms) {
+          int row = warp * 32 + ms * 16 + (mi & 1) * 8 + r8;
+          ldsm_x4(a[ms], wbase + swz128(row, kk * 2 + (mi >> 1)));
+        }
+#pragma unroll
+        for (int nb = 0; nb < BN / 16; ++nb) {
+          uint32_t b[4];
+          int row = nb * 16 + (mi >> 1) * 8 + r8;
+          ldsm_x4(b, abase + swz128(row, kk * 2 + (mi & 1)));
+#pragma unroll
+          for (int ms = 0; ms < 2; ++ms) {
+            mma_bf16(acc[ms][nb * 2 + 0], a[ms], b[0], b[1]);
+            mma_bf16(acc[ms][nb * 2 + 1], a[ms], b[2], b[3]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // ---- tile (or piece of tile) done: accumulators -> Cs
+#pragma unroll
+    for (int ms = 0; ms < 2; ++ms)
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        int wr = warp * 32 + ms * 16 + g8;
+        int ar = j * 8 + 2 * t4;
+        Cs[ar * C::PITCH + wr] = acc[ms][j][0];
+        Cs[(ar + 1) * C::PITCH + wr] = acc[ms][j][1];
+        Cs[ar * C::PITCH + wr + 8] = acc[ms][j][2];
+        Cs[(ar + 1) * C::PITCH + wr + 8] = acc[ms][j][3];
+      }
+    consumer_sync();
+    const bool whole = (ks0 == 0) && (seg_end == tile_end);
+    bool mine = true;
+    if (!whole) {
+      // publish this piece, then let the last contributor of the tile finish it
+      const int slot = (u == u0) ? 0 : 1;
+      float* dst = g.part + ((long long)cta * 2 + slot) * BN * kBM;
+      for (int x = tid; x < BN * kBM; x += 128) dst[x] = Cs[(x / kBM) * C::PITCH + x % kBM];
+      // contributors: the CTAs whose unit ranges intersect [ts, tile_end)
+      const long long ts = static_cast<long long>(t) * g.ks;
+      int clo = static_cast<int>((ts * grid) / g.units);
+      while ((g.units * (clo + 1)) / grid <= ts) ++clo;
+      int chi = clo;
+      while (chi + 1 < grid && (g.units * (chi + 1)) / grid < tile_end) ++chi;
+      __threadfence();
+      consumer_sync();
+      if (tid == 0) {
+        int prev = atomicAdd(&g.counters[t], 1);
+        int last = (prev == chi - clo);
+        if (last) { atomicExch(&g.counters[t], 0); __threadfence(); }
+        *flag = last;
+      }
+      consumer_sync();
+      mine = *flag != 0;
+      if (mine) {
+        for (int x = tid; x < BN * kBM; x += 128) {
+          float v = 0.f;
+          for (int c = clo; c <= chi; ++c) {
+            long long cu0 = g.units * c / grid;
+            int sl = (cu0 / g.ks == t) ? 0 : 1;
+            if (c == cta) sl = slot;
+            v += __ldcg(g.part + ((long long)c * 2 + sl) * BN * kBM + x);
+          }
+          Cs[(x / kBM) * C::PITCH + x % kBM] = v;
+        }
+        consumer_sync();
+      }
+    }
+    if (mine) {
+      const int mb = t / g.n_tiles, nt = t % g.n_tiles;
+      tile_epilogue<bf16, EPI>(Cs, C::PITCH, BN, mb * BN, nt, g, e, tid, 128);
+    }
+    consumer_sync();
+    u = seg_end;
+  }
+}
+
+// ------------------------------------------------------------------- fp32 SIMT kernel
+// fp32 workloads keep full fp32 products (no TF32): one CTA per (m-block, n-tile) of
+// 16 rows x 128 columns, FFMA over K, then the same epilogues.
+constexpr int kF32BN = 16;
+constexpr int kF32BK = 32;
+
+struct WPtrs {
+  const float* p[kMaxSeg];
+};
+
+template <int EPI>
+__global__ void __launch_bounds__(256)
+    k_gemm_f32(const float* __restrict__ A, int lda, const WPtrs Wseg, const GemmShape g,
+               const EpiArgs<float> e) {
+  __shared__ float As[kF32BN][kF32BK + 1];
+  __shared__ float Ws[kBM][kF32BK + 1];
+  __shared__ float Cs[kF32BN * (kBM + 4)];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int t = blockIdx.x;
+  const int mb = t / g.n_tiles, nt = t % g.n_tiles;
+  int seg = 0;
+  while (seg + 1 < g.nseg && nt >= g.seg_tile0[seg + 1]) ++seg;
+  const int tid = threadIdx.x;
+  const int rows_per_tile = g.paired ? kBM / 2 : kBM;
+  const int r0 = (nt - g.seg_tile0[seg]) * rows_per_tile;
+  // thread -> (act row ar, 8 weight rows wr..wr+7 strided by 16)
+  const int ar = tid % kF32BN, wr0 = tid / kF32BN;
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int k0 = 0; k0 < g.K; k0 += kF32BK) {
+    for (int x = tid; x < kF32BN * kF32BK; x += 256) {
+      int r = x / kF32BK, k = x % kF32BK;
+      int m = mb * kF32BN + r;
+      As[r][k] = (m < g.M && k0 + k < g.K) ? A[(long long)m * lda + k0 + k] : 0.f;
+    }
+    for (int x = tid; x < kBM * kF32BK; x += 256) {
+      int r = x / kF32BK, k = x % kF32BK;
+      int sg = g.paired ? (r < kBM / 2 ? 0 : 1) : seg;
+      int row = r0 + (g.paired ? r % (kBM / 2) : r);
+      Ws[r][k] = (row < g.seg_rows[sg] && k0 + k < g.K)
+                     ? Wseg.p[sg][(long long)row * g.K + k0 + k] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int k = 0; k < kF32BK; ++k) {
+      float a = As[ar][k];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = fmaf(a, Ws[wr0 + 16 * j][k], acc[j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) Cs[ar * (kBM + 4) + wr0 + 16 * j] = acc[j];
+  __syncthreads();
+  tile_epilogue<float, EPI>(Cs, kBM + 4, kF32BN, mb * kF32BN, nt, g, e, tid, 256);
+}
+
+}  // namespace dflash

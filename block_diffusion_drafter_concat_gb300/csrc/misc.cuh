@@ -1,0 +1,383 @@
+// Row kernels of the drafter step: block embedding + RMSNorm, RMSNorm, the LM-head
+// argmax finalisation, and the verification kernels (greedy, temperature tau).
+#pragma once
+
+#include "common.cuh"
+
+namespace dflash {
+
+constexpr int kRowThreads = 256;
+
+// Block-wide sum over kRowThreads threads (fixed tree: deterministic).
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kRowThreads / 32; ++w) t += red[w];
+  return t;
+}
+
+// y[m] = x[m] / sqrt(mean(x[m]^2) + eps) * g, one CTA per row.
+// With `ids`, x[m] is first set to the embedding row ids[m] (block embedding) and the
+// block position ctx_lens[m / S] + m % S is written to pos[m].
+template <typename T, typename Tin>
+__global__ void __launch_bounds__(kRowThreads)
+    k_rmsnorm(const Tin* __restrict__ xin, float* __restrict__ xout, const T* __restrict__ gain,
+              T* __restrict__ y, int d, float eps, const int* __restrict__ ids,
+              const T* __restrict__ embed, int vocab, const int* __restrict__ ctx_lens, int S,
+              int max_position, int* __restrict__ pos, int* err) {
+  __shared__ float red[kRowThreads / 32];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int m = blockIdx.x;
+  const Tin* src = xin + (long long)m * d;
+  if (ids) {
+    int id = ids[m];
+    const int b = m / S, i = m % S;
+    const int p = ctx_lens[b] + i;
+    if (threadIdx.x == 0) {
+      pos[m] = p;
+      if (p < 0 || p >= max_position || ctx_lens[b] < 0) raise_error(err, DFLASH_DEV_BAD_POSITION);
+    }
+    if (id < 0 || id >= vocab) {
+      if (threadIdx.x == 0) raise_error(err, DFLASH_DEV_BAD_INDEX);
+      id = 0;
+    }
+    src = nullptr;
+    const T* e = embed + (long long)id * d;
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < d; c += kRowThreads) {
+      float v = to_f32<T>(e[c]);
+      xout[(long long)m * d + c] = v;
+      ss += v * v;
+    }
+    const float rs = 1.0f / sqrtf(block_sum(ss, red) / d + eps);
+    for (int c = threadIdx.x; c < d; c += kRowThreads)
+      y[(long long)m * d + c] = from_f32<T>(to_f32<T>(e[c]) * rs * to_f32<T>(gain[c]));
+    return;
+  }
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < d; c += kRowThreads) {
+    float v = to_f32<Tin>(src[c]);
+    ss += v * v;
+  }
+  const float rs = 1.0f / sqrtf(block_sum(ss, red) / d + eps);
+  for (int c = threadIdx.x; c < d; c += kRowThreads)
+    y[(long long)m * d + c] = from_f32<T>(to_f32<Tin>(src[c]) * rs * to_f32<T>(gain[c]));
+}
+
+// Reduce the LM head's per-tile (max, argmax, sum exp) partials of each row in tile
+// order: tokens = argmax (lowest index), max_logit, lse = max/tau + log(sum).
+static __global__ void __launch_bounds__(kRowThreads)
+    k_argmax_finalize(const float* __restrict__ am_max, const int* __restrict__ am_idx,
+                      const float* __restrict__ am_sum, int n_tiles, int M, float inv_temp,
+                      int* __restrict__ tokens, float* __restrict__ max_logit,
+                      float* __restrict__ lse) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m = blockIdx.x * (kRowThreads / 32) + warp;
+  if (m >= M) return;
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int t = lane; t < n_tiles; t += 32) {
+    float v = am_max[(long long)t * M + m];
+    int i = am_idx[(long long)t * M + m];
+    if (v > best || (v == best && i < bi)) { best = v; bi = i; }
+  }
+  warp_argmax(best, bi);
+  if (lane == 0) tokens[m] = bi;
+  if (lse) {
+    // each lane sums its tiles rescaled to the row maximum, lanes in a fixed tree
+    float s = 0.f;
+    for (int t = lane; t < n_tiles; t += 32)
+      s += am_sum[(long long)t * M + m] * __expf((am_max[(long long)t * M + m] - best) * inv_temp);
+    s = warp_sum(s);
+    if (lane == 0) lse[m] = best * inv_temp + logf(s);
+  }
+  if (max_logit && lane == 0) max_logit[m] = best;
+}
+
+// ------------------------------------------------------------------ greedy verify
+// grid (chunks, B*S).  Each CTA takes the argmax (lowest index) of one vocab chunk of
+// one target row; the last CTA of a sequence reduces the chunks, walks the block and
+// writes the accepted prefix plus the bonus token.
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads)
+    k_verify_greedy(const T* __restrict__ logits, const int* __restrict__ draft, int S, int V,
+                    int chunk, float* __restrict__ part_v, int* __restrict__ part_i,
+                    int* __restrict__ counters, int* __restrict__ out_tokens,
+                    int* __restrict__ n_acc, int* __restrict__ n_emit, int* err) {
+  __shared__ float sv[kRowThreads / 32];
+  __shared__ int si[kRowThreads / 32];
+  __shared__ int flag;
+  __shared__ int tok[64];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int c = blockIdx.x, row = blockIdx.y, nch = gridDim.x;
+  const int b = row / S;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const T* src = logits + (long long)row * V;
+  const int v0 = c * chunk, v1 = min(V, v0 + chunk);
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+  constexpr int VEC = 16 / sizeof(T);
+  const bool vec_ok = ((reinterpret_cast<uintptr_t>(src + v0) & 15) == 0);
+  if (vec_ok) {
+    const int nv = (v1 - v0) / VEC;
+    for (int k = threadIdx.x; k < nv; k += kRowThreads) {
+      uint4 raw = __ldcs(reinterpret_cast<const uint4*>(src + v0) + k);
+      const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) {
+        float v = to_f32<T>(e[j]);
+        if (v > best) { best = v; bi = v0 + k * VEC + j; }
+      }
+    }
+    for (int v = v0 + nv * VEC + threadIdx.x; v < v1; v += kRowThreads) {
+      float x = to_f32<T>(src[v]);
+      if (x > best) { best = x; bi = v; }
+    }
+  } else {
+    for (int v = v0 + threadIdx.x; v < v1; v += kRowThreads) {
+      float x = to_f32<T>(src[v]);
+      if (x > best) { best = x; bi = v; }
+    }
+  }
+  warp_argmax(best, bi);
+  if (lane == 0) { sv[warp] = best; si[warp] = bi; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kRowThreads / 32; ++w)
+      if (sv[w] > best || (sv[w] == best && si[w] < bi)) { best = sv[w]; bi = si[w]; }
+    part_v[(long long)row * nch + c] = best;
+    part_i[(long long)row * nch + c] = bi;
+  }
+  if (!elect_last(&counters[b], S * nch, &flag)) return;
+  // last CTA of sequence b: one warp per block slot
+  for (int i = warp; i < S; i += kRowThreads / 32) {
+    float bv = -INFINITY;
+    int bx = 0x7fffffff;
+    const long long r = (long long)b * S + i;
+    for (int k = lane; k < nch; k += 32) {
+      float v = __ldcg(part_v + r * nch + k);
+      int x = __ldcg(part_i + r * nch + k);
+      if (v > bv || (v == bv && x < bx)) { bv = v; bx = x; }
+    }
+    warp_argmax(bv, bx);
+    if (lane == 0) tok[i] = bx;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int n = 0;
+    while (n < S) {
+      int dft = draft[(long long)b * S + n];
+      if (dft < 0 || dft >= V) { raise_error(err, DFLASH_DEV_BAD_INDEX); break; }
+      if (dft != tok[n]) break;
+      ++n;
+    }
+    const int ne = min(n + 1, S);
+    for (int i = 0; i < S; ++i) out_tokens[(long long)b * S + i] = i < ne ? tok[i] : -1;
+    n_acc[b] = n;
+    n_emit[b] = ne;
+  }
+}
+
+// ------------------------------------------------------------ temperature-tau verify
+// Pass 1, grid (chunks, B*S): per chunk of target row r the max and sum exp of
+// logits/tau; the last CTA of a row forms lse_t[r] and p_r(d_r); the last row of a
+// sequence walks the acceptance test u[i,0] < p_i(d_i) / q_i(d_i), writes the accepted
+// prefix, and records the first rejected slot (or S) in rej[b]; it also copies that
+// slot's hidden row into hrow[b] for the drafter-logit recompute.
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads)
+    k_verify_sample_accept(const T* __restrict__ logits, const int* __restrict__ draft,
+                           const float* __restrict__ dmax, const float* __restrict__ dlse,
+                           const float* __restrict__ u, const T* __restrict__ hidden, int d,
+                           int S, int V, int chunk, float inv_temp,
+                           float* __restrict__ part_m, float* __restrict__ part_s,
+                           float* __restrict__ lse_t, int* __restrict__ counters,
+                           int* __restrict__ rej, T* __restrict__ hrow,
+                           int* __restrict__ out_tokens, int* __restrict__ n_acc,
+                           int* __restrict__ n_emit, int* err) {
+  __shared__ float red[kRowThreads / 32];
+  __shared__ float redm[kRowThreads / 32];
+  __shared__ int flag;
+  __shared__ int nrej;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int c = blockIdx.x, row = blockIdx.y, nch = gridDim.x;
+  const int b = row / S;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const T* src = logits + (long long)row * V;
+  const int v0 = c * chunk, v1 = min(V, v0 + chunk);
+  float mx = -INFINITY;
+  for (int v = v0 + threadIdx.x; v < v1; v += kRowThreads) mx = fmaxf(mx, to_f32<T>(src[v]));
+  mx = warp_max(mx);
+  if (lane == 0) redm[warp] = mx;
+  __syncthreads();
+  mx = -INFINITY;
+  for (int w = 0; w < kRowThreads / 32; ++w) mx = fmaxf(mx, redm[w]);
+  float s = 0.f;
+  for (int v = v0 + threadIdx.x; v < v1; v += kRowThreads)
+    s += __expf((to_f32<T>(src[v]) - mx) * inv_temp);
+  s = block_sum(s, red);
+  if (threadIdx.x == 0) {
+    part_m[(long long)row * nch + c] = mx;
+    part_s[(long long)row * nch + c] = s;
+  }
+  // last chunk of this row -> the row's log-sum-exp
+  if (!elect_last(&counters[row], nch, &flag)) return;
+  if (threadIdx.x == 0) {
+    float M = -INFINITY;
+    for (int k = 0; k < nch; ++k) M = fmaxf(M, __ldcg(part_m + (long long)row * nch + k));
+    float L = 0.f;
+    for (int k = 0; k < nch; ++k)
+      L += __ldcg(part_s + (long long)row * nch + k) *
+           __expf((__ldcg(part_m + (long long)row * nch + k) - M) * inv_temp);
+    lse_t[row] = M * inv_temp + logf(L);
+  }
+  // last row of the sequence -> acceptance walk
+  const int seq_counter = gridDim.y + b;  // counters after the per-row ones
+  if (!elect_last(&counters[seq_counter], S, &flag)) return;
+  if (threadIdx.x == 0) {
+    int n = 0;
+    for (; n < S; ++n) {
+      const long long r = (long long)b * S + n;
+      const int dt = draft[r];
+      if (dt < 0 || dt >= V) { raise_error(err, DFLASH_DEV_BAD_INDEX); break; }
+      const float lp = to_f32<T>(logits[r * V + dt]) * inv_temp - __ldcg(lse_t + r);
+      const float lq = dmax[r] * inv_temp - dlse[r];  // the draft is the drafter's argmax
+      // accept iff u < p/q, compared as log u < log p - log q
+      const float uu = u[r * 2];
+      if (!(uu < __expf(lp - lq))) break;
+      out_tokens[r] = dt;
+    }
+    for (int i = n; i < S; ++i) out_tokens[(long long)b * S + i] = -1;
+    rej[b] = n;
+    n_acc[b] = n;
+    n_emit[b] = n < S ? n + 1 : S;
+    nrej = n;
+  }
+  __syncthreads();
+  const int rs = min(nrej, S - 1);
+  for (int k = threadIdx.x; k < d; k += kRowThreads)
+    hrow[(long long)b * d + k] = hidden[((long long)b * S + rs) * d + k];
+}
+
+// Pass 2, grid (chunks, B), after the drafter logits zr [B, V] of each rejected slot
+// were recomputed: r_v = max(0, p_v - q_v) per chunk; the last chunk of a sequence
+// finds the chunk holding u[n,1] * sum(r) and scans it for the sampled token.
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads)
+    k_verify_sample_residual(const T* __restrict__ logits, const float* __restrict__ zr,
+                             const float* __restrict__ lse_t, const float* __restrict__ dlse,
+                             const float* __restrict__ u, const int* __restrict__ rej, int S,
+                             int V, int chunk, float inv_temp, float* __restrict__ part_r,
+                             float* __restrict__ part_p, int* __restrict__ counters,
+                             int* __restrict__ out_tokens) {
+  __shared__ float red[kRowThreads / 32];
+  __shared__ int flag;
+  __shared__ float scan[kRowThreads];
+  __shared__ int found;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int c = blockIdx.x, b = blockIdx.y, nch = gridDim.x;
+  const int n = rej[b];
+  if (n >= S) return;  // everything accepted: nothing to sample (counter unused)
+  const long long r = (long long)b * S + n;
+  const T* lt = logits + r * V;
+  const float* lz = zr + (long long)b * V;
+  const float lset = lse_t[r], lsez = dlse[r];
+  const int v0 = c * chunk, v1 = min(V, v0 + chunk);
+  float sr = 0.f, sp = 0.f;
+  for (int v = v0 + threadIdx.x; v < v1; v += kRowThreads) {
+    float p = __expf(to_f32<T>(lt[v]) * inv_temp - lset);
+    float q = __expf(lz[v] * inv_temp - lsez);
+    sr += fmaxf(0.f, p - q);
+    sp += p;
+  }
+  sr = block_sum(sr, red);
+  sp = block_sum(sp, red);
+  if (threadIdx.x == 0) {
+    part_r[(long long)b * nch + c] = sr;
+    part_p[(long long)b * nch + c] = sp;
+  }
+  if (!elect_last(&counters[b], nch, &flag)) return;
+  // choose the residual (or p itself when the residual is all zero)
+  __shared__ int use_p;
+  __shared__ float target;
+  __shared__ int cstar;
+  __shared__ float before;
+  if (threadIdx.x == 0) {
+    float Z = 0.f;
+    for (int k = 0; k < nch; ++k) Z += __ldcg(part_r + (long long)b * nch + k);
+    const float* pr = part_r;
+    use_p = (Z <= 0.f);
+    if (use_p) {
+      Z = 0.f;
+      for (int k = 0; k < nch; ++k) Z += __ldcg(part_p + (long long)b * nch + k);
+      pr = part_p;
+    }
+    target = u[r * 2 + 1] * Z;
+    float acc = 0.f;
+    int k = 0, last_nz = -1;
+    for (; k < nch; ++k) {
+      float w = __ldcg(pr + (long long)b * nch + k);
+      if (w > 0.f) last_nz = k;
+      if (acc + w >= target && w > 0.f) break;
+      acc += w;
+    }
+    if (k == nch) { k = last_nz < 0 ? 0 : last_nz; acc = -1.f; }  // rounding: take the last mass
+    cstar = k;
+    before = acc;
+    found = -1;
+  }
+  __syncthreads();
+  // inclusive scan of chunk cstar in index order, kRowThreads elements at a time
+  const int w0 = cstar * chunk, w1 = min(V, w0 + chunk);
+  float acc = before;
+  const bool last_mass = before < 0.f;
+  int last_pos = -1;
+  for (int base = w0; base < w1; base += kRowThreads) {
+    const int v = base + threadIdx.x;
+    float val = 0.f;
+    if (v < w1) {
+      float p = __expf(to_f32<T>(lt[v]) * inv_temp - lset);
+      float q = __expf(lz[v] * inv_temp - lsez);
+      val = use_p ? p : fmaxf(0.f, p - q);
+    }
+    scan[threadIdx.x] = val;
+    __syncthreads();
+    for (int off = 1; off < kRowThreads; off <<= 1) {
+      float t = threadIdx.x >= off ? scan[threadIdx.x - off] : 0.f;
+      __syncthreads();
+      scan[threadIdx.x] += t;
+      __syncthreads();
+    }
+    if (!last_mass && found < 0 && val > 0.f && acc + scan[threadIdx.x] >= target)
+      atomicMin(reinterpret_cast<unsigned*>(&found), static_cast<unsigned>(v));
+    if (val > 0.f) last_pos = v;
+    __syncthreads();
+    acc += scan[kRowThreads - 1];
+    __syncthreads();
+    if (found >= 0) break;
+  }
+  if (last_mass) {
+    // no prefix reached the target through rounding: the last index with mass
+    __shared__ int lp;
+    if (threadIdx.x == 0) lp = -1;
+    __syncthreads();
+    if (last_pos >= 0) atomicMax(&lp, last_pos);
+    __syncthreads();
+    if (threadIdx.x == 0) out_tokens[r] = lp;
+  } else if (threadIdx.x == 0) {
+    out_tokens[r] = found;
+  }
+}
+
+}  // namespace dflash

@@ -1,0 +1,46 @@
+// Attention kernel instantiations (head_dim 64 / 128, 1-8 query warps) and fp32 path.
+#include "host.h"
+
+namespace dflash {
+
+template <int HD, int NW>
+static dflash_status one(dim3 grid, int smem, const AttnMaps& mp, const AttnArgs<bf16>& a,
+                         cudaStream_t st) {
+  static bool set = false;
+  if (!set) {
+    DFLASH_TRY(set_smem(k_attn_tc<HD, NW>, smem));
+    set = true;
+  }
+  return launch(k_attn_tc<HD, NW>, grid, dim3((NW + 1) * 32), smem, st, mp, a);
+}
+
+dflash_status launch_attn_tc(int hd, int nw, dim3 grid, int smem, const AttnMaps& mp,
+                             const AttnArgs<bf16>& a, cudaStream_t st) {
+  if (hd == 128) {
+    switch (nw) {
+      case 1: return one<128, 1>(grid, smem, mp, a, st);
+      case 2: return one<128, 2>(grid, smem, mp, a, st);
+      case 4: return one<128, 4>(grid, smem, mp, a, st);
+      case 8: return one<128, 8>(grid, smem, mp, a, st);
+    }
+  } else if (hd == 64) {
+    switch (nw) {
+      case 1: return one<64, 1>(grid, smem, mp, a, st);
+      case 2: return one<64, 2>(grid, smem, mp, a, st);
+      case 4: return one<64, 4>(grid, smem, mp, a, st);
+      case 8: return one<64, 8>(grid, smem, mp, a, st);
+    }
+  }
+  return fail(DFLASH_EUNSUPPORTED, "attention: head_dim %d with %d query rows", hd, nw * 16);
+}
+
+dflash_status launch_attn_f32(dim3 grid, int smem, const AttnArgs<float>& a, cudaStream_t st) {
+  static bool set = false;
+  if (!set) {
+    DFLASH_TRY(set_smem(k_attn_f32, 160 * 1024));
+    set = true;
+  }
+  return launch(k_attn_f32, grid, dim3(128), smem, st, a);
+}
+
+}  // namespace dflash

@@ -1,0 +1,180 @@
+"""One DFlash draft + verify step on a seeded synthetic workload, end to end on the GPU.
+
+StepRunner owns the device state of a workload: random-init weights of the named
+shape, the paged KV cache, the page table, the per-step inputs (the S newest target
+hidden features of every sequence and the target's verify logits) and the outputs.
+``step()`` enqueues the whole path as libdflash calls on the current stream:
+
+  dflash_inject_kv (fuse + inject the S new context rows of every sequence)
+  -> dflash_draft_block -> dflash_lm_head_argmax
+  -> dflash_verify_greedy, or dflash_verify_sample at temperature > 0.
+
+``capture()`` records that sequence into a CUDA graph.  Inputs come from the seeded
+counter-based generator, drawn directly on the device.
+"""
+from __future__ import annotations
+
+import torch
+
+from workload import inputs
+from workload.configs import Workload
+
+from . import BF16, F32, Drafter, KVCache, last_launch_count
+
+PREFILL_CHUNK = 4096
+
+
+def drafter_config(w: Workload) -> dict:
+    return dict(d_model=w.d_model, n_layers=w.n_layers, n_q_heads=w.n_q_heads,
+                n_kv_heads=w.n_kv_heads, head_dim=w.head_dim, ffn_dim=w.ffn_dim,
+                vocab=w.vocab, block_size=w.block_size, n_target_layers=w.n_target_layers,
+                target_width=w.target_width, page_size=w.page_size,
+                max_position=w.max_position, rope_theta=w.rope_theta, rms_eps=w.rms_eps,
+                dtype=BF16 if w.dtype == "bf16" else F32)
+
+
+class StepRunner:
+    def __init__(self, w: Workload, device="cuda", prefill=True, weights=None):
+        self.w = w
+        self.device = device
+        self.dt = inputs.torch_dtype(w)
+        S, B = w.block_size, w.batch
+        self.weights = weights if weights is not None else inputs.weights(w, device)
+        self.drafter = Drafter(drafter_config(w), self.weights)
+        self.lens = inputs.ctx_lens(w)
+        assert int(self.lens.min()) >= S, "each context must hold at least one block"
+        table, total = inputs.page_table(w, self.lens)
+        self.table_host = table
+        self.page_table = table.to(device)
+        self.cache = KVCache(w.n_layers, total, w.n_kv_heads, w.head_dim, self.dt, device)
+        self.ws = self.drafter.workspace(max(w.rows, PREFILL_CHUNK), B, w.max_pages, device)
+        # step inputs: the S newest context rows of every sequence
+        pos, slots = [], []
+        for b in range(B):
+            t = int(self.lens[b])
+            p = torch.arange(t - S, t)
+            pos.append(p)
+            slots.append(inputs.slots_for(w, table, b, p))
+        self.positions = torch.cat(pos).to(torch.int32).to(device)
+        self.slots = torch.cat(slots).to(torch.int32).to(device)
+        self.x_step = torch.cat([inputs.ctx_hidden(w, b, int(self.lens[b]) - S, int(self.lens[b]),
+                                                   device) for b in range(B)])
+        self.block_ids = inputs.block_ids(w).to(device)
+        self.ctx_lens = self.lens.to(torch.int32).to(device)
+        M, d = w.rows, w.d_model
+        self.fused = torch.empty(M, d, dtype=self.dt, device=device)
+        self.hidden = torch.empty(M, d, dtype=self.dt, device=device)
+        self.draft = torch.empty(B, S, dtype=torch.int32, device=device)
+        self.dmax = torch.empty(M, dtype=torch.float32, device=device)
+        self.dlse = torch.empty(M, dtype=torch.float32, device=device)
+        self.out_tokens = torch.empty(B, S, dtype=torch.int32, device=device)
+        self.n_acc = torch.empty(B, dtype=torch.int32, device=device)
+        self.n_emit = torch.empty(B, dtype=torch.int32, device=device)
+        self.logits = inputs.logits_noise(w, device=device)
+        self.uniforms = inputs.uniforms(w, device=device)
+        self.launches = 0
+        self.graph = None
+        if prefill:
+            self.prefill()
+
+    # ------------------------------------------------------------------ setup
+    def prefill(self):
+        """Injects context positions [0, T_b - S) of every sequence (untimed setup)."""
+        w = self.w
+        for b in range(w.batch):
+            t = int(self.lens[b]) - w.block_size
+            for p0 in range(0, t, PREFILL_CHUNK):
+                p1 = min(t, p0 + PREFILL_CHUNK)
+                x = inputs.ctx_hidden(w, b, p0, p1, self.device)
+                p = torch.arange(p0, p1)
+                s = inputs.slots_for(w, self.table_host, b, p)
+                self.drafter.inject_kv(p.to(torch.int32).to(self.device),
+                                       s.to(torch.int32).to(self.device), self.cache, self.ws,
+                                       x_cat=x)
+
+    def plant(self, drafts, mask=None):
+        """Regenerates the verify logits and plants agreement with `drafts` [B, S]."""
+        w = self.w
+        self.logits = inputs.logits_noise(w, device=self.device)
+        mask = inputs.plant_mask(w) if mask is None else mask
+        inputs.plant(w, self.logits, torch.as_tensor(drafts).cpu(), mask)
+
+    # ------------------------------------------------------------------ the step
+    def step(self):
+        w, d = self.w, self.drafter
+        n = 0
+        d.inject_kv(self.positions, self.slots, self.cache, self.ws, x_cat=self.x_step,
+                    fused_out=self.fused)
+        n += last_launch_count()
+        d.draft_block(self.block_ids, self.ctx_lens, self.page_table, self.cache, self.hidden,
+                      self.ws)
+        n += last_launch_count()
+        sample = w.temperature > 0
+        tau = w.temperature if sample else 1.0
+        d.lm_head_argmax(self.hidden, self.draft.view(-1), self.ws, self.dmax,
+                         self.dlse if sample else None, tau)
+        n += last_launch_count()
+        if sample:
+            d.verify_sample(self.draft, self.hidden, self.dmax, self.dlse, self.logits,
+                            self.uniforms, tau, self.out_tokens, self.n_acc, self.n_emit, self.ws)
+        else:
+            d.verify_greedy(self.draft, self.logits, self.out_tokens, self.n_acc, self.n_emit,
+                            self.ws)
+        n += last_launch_count()
+        self.launches = n
+
+    def capture(self):
+        """Records step() into a CUDA graph (after one eager warm-up step)."""
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.step()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step()
+        self.graph = g
+        return g
+
+    def replay(self):
+        self.graph.replay()
+
+
+# ---------------------------------------------------------------------- roofline model
+def weight_bytes(w: Workload) -> int:
+    """Bytes of every weight one step streams once (the embedding contributes only the
+    block's rows)."""
+    e = 2 if w.dtype == "bf16" else 4
+    d, F = w.d_model, w.ffn_dim
+    per_layer = (w.q_width * d + 2 * w.kv_width * d + d * w.q_width + 3 * F * d + 2 * d)
+    return e * (d * w.fuse_in + d + w.n_layers * per_layer + d + w.vocab * d
+                + w.rows * d)
+
+
+def step_bytes(w: Workload, lens=None) -> int:
+    """Algorithmic HBM bytes of one step: weights once, context K/V read once, the S
+    new K/V rows written, target hidden features and verify logits read, outputs."""
+    e = 2 if w.dtype == "bf16" else 4
+    lens = inputs.ctx_lens(w) if lens is None else lens
+    kv_row = w.n_layers * 2 * w.kv_width * e
+    ctx = int(lens.sum()) * kv_row
+    new = w.rows * kv_row
+    return (weight_bytes(w) + ctx + new + w.rows * w.fuse_in * e + w.rows * w.vocab * e
+            + w.rows * w.d_model * e + w.rows * 4 * 4)
+
+
+def step_flops(w: Workload, lens=None) -> int:
+    lens = inputs.ctx_lens(w) if lens is None else lens
+    d, F, R = w.d_model, w.ffn_dim, w.rows
+    lin = 2 * R * (d * w.fuse_in + w.n_layers * (2 * w.kv_width * d)
+                   + w.n_layers * (w.q_width * d + 2 * w.kv_width * d + d * w.q_width
+                                   + 3 * F * d) + w.vocab * d)
+    keys = int(lens.sum()) + w.batch * w.block_size
+    attn = w.n_layers * 4 * w.block_size * w.n_q_heads * w.head_dim * keys
+    return lin + attn
+
+
+def lm_head_bytes(w: Workload) -> int:
+    e = 2 if w.dtype == "bf16" else 4
+    return e * (w.vocab * w.d_model + w.rows * w.d_model) + w.rows * 12

@@ -1,0 +1,185 @@
+"""Per-entry-point GPU parity (LM head, fusion, verification) and device error paths,
+each on oracle-side inputs drawn from the shared generator."""
+import numpy as np
+import pytest
+import torch
+
+import block_diffusion_drafter_concat_gb300 as pkg
+from oracle import dflash_oracle as O
+from oracle import run as orun
+from workload import configs, inputs, synth
+
+from gpu_helpers import MARGIN, check_drafts, rel_err
+
+pytestmark = pytest.mark.gpu
+
+W_SMALL = configs.small_bf16()
+
+
+@pytest.fixture(scope="module")
+def small():
+    from block_diffusion_drafter_concat_gb300 import build
+    from block_diffusion_drafter_concat_gb300.runner import StepRunner
+    build.build()
+    return StepRunner(W_SMALL, prefill=False)
+
+
+def hidden_rows(w, rows, name="h_test"):
+    return synth.normal(w.seed, name, (rows, w.d_model), dtype=inputs.torch_dtype(w))
+
+
+@pytest.mark.parametrize("rows", [1, 16, 37, 130])
+def test_lm_head_argmax_stats(small, rows):
+    w = W_SMALL
+    h = hidden_rows(w, rows)
+    tok = torch.empty(rows, dtype=torch.int32, device="cuda")
+    mx = torch.empty(rows, dtype=torch.float32, device="cuda")
+    lse = torch.empty(rows, dtype=torch.float32, device="cuda")
+    small.drafter.lm_head_argmax(h.cuda(), tok, small.ws, mx, lse, temperature=0.7)
+    torch.cuda.synchronize()
+    W = orun.host_weights(w)
+    z = O.lm_head(orun.np64(h), W["lm_head"])
+    check_drafts(tok.cpu().numpy(), O.argmax_lowest(z), O.top2_margin(z))
+    assert rel_err(mx, z.max(axis=1)) < 1e-4
+    zt = z / 0.7
+    ref = zt.max(axis=1) + np.log(np.exp(zt - zt.max(axis=1, keepdims=True)).sum(axis=1))
+    np.testing.assert_allclose(lse.cpu().numpy(), ref, rtol=1e-4, atol=1e-4)
+
+
+@pytest.mark.parametrize("n", [1, 16, 45])
+def test_fuse_features(small, n):
+    w = W_SMALL
+    x = synth.normal(w.seed, "x_fuse_test", (n, w.fuse_in), dtype=torch.bfloat16)
+    out = torch.empty(n, w.d_model, dtype=torch.bfloat16, device="cuda")
+    small.drafter.fuse_features(x.cuda(), out, small.ws)
+    torch.cuda.synchronize()
+    W = orun.host_weights(w)
+    ref = O.fuse_features(orun.np64(x), W["w_fuse"], W["g_fuse"], w.rms_eps, True)
+    assert rel_err(out, ref) < 2e-2
+
+
+def test_verify_greedy_exact(small):
+    w = W_SMALL
+    B, S, V = 6, w.block_size, w.vocab
+    g = torch.Generator().manual_seed(5)
+    logits = (torch.randint(0, 6, (B, S, V), generator=g).float() - 3).to(torch.bfloat16)
+    tgt = logits.float().argmax(-1)                        # lowest index on ties
+    draft = tgt.clone()
+    draft[1, 0] = (draft[1, 0] + 1) % V                    # mismatch at slot 0
+    draft[2, 5] = (draft[2, 5] + 7) % V
+    draft[4] = torch.randint(0, V, (S,), generator=g)
+    draft = draft.to(torch.int32)
+    out = torch.empty(B, S, dtype=torch.int32, device="cuda")
+    na = torch.empty(B, dtype=torch.int32, device="cuda")
+    ne = torch.empty(B, dtype=torch.int32, device="cuda")
+    small.drafter.verify_greedy(draft.cuda(), logits.cuda(), out, na, ne, small.ws)
+    torch.cuda.synchronize()
+    for b in range(B):
+        o, n, e = O.verify_greedy(draft[b].numpy(), logits[b].float().numpy())
+        assert (int(na[b]), int(ne[b])) == (n, e)
+        assert out[b].cpu().tolist() == list(o)
+    assert int(ne[0]) == S and int(ne[1]) == 1 and int(na[2]) == 5
+
+
+def sample_ambiguous(draft, z, logits, u, tau, eps=1e-3):
+    """True when a fp32 evaluation could take a different branch than fp64: an
+    acceptance ratio or a residual CDF step within eps of the uniform."""
+    S = len(draft)
+    for i in range(S):
+        p = O.softmax(logits[i] / tau)
+        q = O.softmax(z[i] / tau)
+        d = int(draft[i])
+        if abs(u[i, 0] * q[d] - p[d]) <= eps * max(p[d], q[d]):
+            return True
+        if u[i, 0] < p[d] / q[d]:
+            continue
+        r = np.maximum(0, p - q)
+        if r.sum() == 0:
+            r = p
+        cdf = np.cumsum(r)
+        return bool(np.min(np.abs(cdf - u[i, 1] * r.sum())) <= eps * r.sum())
+    return False
+
+
+def test_verify_sample_matches_oracle(small):
+    w = W_SMALL.scaled(temperature=1.0)
+    B, S = 24, w.block_size
+    rows = B * S
+    h = hidden_rows(w, rows, "h_sample")
+    W = orun.host_weights(w)
+    z = O.lm_head(orun.np64(h), W["lm_head"])
+    draft_o = O.argmax_lowest(z).reshape(B, S)
+    margin = O.top2_margin(z).reshape(B, S)
+    logits = synth.normal(w.seed, "logits_sample", (B, S, w.vocab), std=2.0,
+                          dtype=torch.bfloat16)
+    # plant partial agreement so acceptance walks go past slot 0
+    mask = synth.uniform(w.seed, "plant_sample", (B, S)) < 0.6
+    inputs.plant(w, logits, torch.as_tensor(draft_o), mask)
+    u = synth.uniform(w.seed, "u_sample", (B, S, 2))
+    hc = h.cuda()
+    tok = torch.empty(rows, dtype=torch.int32, device="cuda")
+    mx = torch.empty(rows, dtype=torch.float32, device="cuda")
+    lse = torch.empty(rows, dtype=torch.float32, device="cuda")
+    small.drafter.lm_head_argmax(hc, tok, small.ws, mx, lse, temperature=1.0)
+    out = torch.empty(B, S, dtype=torch.int32, device="cuda")
+    na = torch.empty(B, dtype=torch.int32, device="cuda")
+    ne = torch.empty(B, dtype=torch.int32, device="cuda")
+    small.drafter.verify_sample(tok.view(B, S), hc, mx, lse, logits.cuda(), u.cuda(), 1.0, out,
+                                na, ne, small.ws)
+    torch.cuda.synchronize()
+    assert small.drafter.device_error() == 0
+    checked = 0
+    lg = logits.float().numpy()
+    zz = z.reshape(B, S, -1)
+    for b in range(B):
+        o, n, e = O.verify_sample(draft_o[b], zz[b], lg[b], u[b].numpy(), 1.0)
+        # drafts that may differ (low margin) or branches fp32 may take differently are
+        # excluded, up to the slot where the oracle's walk stopped
+        if (margin[b][: min(n, S - 1) + 1] < MARGIN).any() or \
+                sample_ambiguous(draft_o[b], zz[b], lg[b], u[b].numpy(), 1.0):
+            continue
+        assert (int(na[b]), int(ne[b])) == (n, e), b
+        assert out[b].cpu().tolist() == list(o), b
+        checked += 1
+    assert checked >= B // 2
+
+
+def test_device_errors_are_reported_not_trapped(small):
+    r = small
+    w = r.w
+    r.prefill()
+    d = r.drafter
+    # block token id out of range
+    bad_ids = r.block_ids.clone()
+    bad_ids[0, 0] = w.vocab + 3
+    d.draft_block(bad_ids, r.ctx_lens, r.page_table, r.cache, r.hidden, r.ws)
+    assert d.device_error() == 1
+    d.workspace_init(r.ws)
+    # context longer than the page table allows
+    bad_lens = r.ctx_lens.clone()
+    bad_lens[0] = w.max_pages * 16 + 1
+    d.draft_block(r.block_ids, bad_lens, r.page_table, r.cache, r.hidden, r.ws)
+    assert d.device_error() in (1, 2)
+    d.workspace_init(r.ws)
+    # a page id outside the pool
+    bad_table = r.page_table.clone()
+    bad_table[0, 0] = r.cache.num_pages + 5
+    d.draft_block(r.block_ids, r.ctx_lens, bad_table, r.cache, r.hidden, r.ws)
+    assert d.device_error() == 1
+    d.workspace_init(r.ws)
+    # the path still works afterwards
+    r.step()
+    torch.cuda.synchronize()
+    assert d.device_error() == 0
+
+
+def test_host_validation_statuses(small):
+    r = small
+    d = r.drafter
+    tiny_ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pkg.DFlashError) as e:
+        d.draft_block(r.block_ids, r.ctx_lens, r.page_table, r.cache, r.hidden, tiny_ws)
+    assert e.value.status == pkg.EWORKSPACE
+    with pytest.raises(pkg.DFlashError) as e:
+        d.lm_head_argmax(r.hidden[:, 1:], r.draft.view(-1), r.ws)   # misaligned rows
+    assert e.value.status == pkg.EINVAL
