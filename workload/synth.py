@@ -95,8 +95,9 @@ def normal_flat(seed, name, start, stop, std=1.0, mean=0.0, dtype=torch.float32,
     """Elements [start, stop) of the flat stream ``name``, 1-D."""
     n = stop - start
     out = torch.empty(n, dtype=dtype, device=device)
-    for c0 in range(0, n, CHUNK):
-        c1 = min(n, c0 + CHUNK)
+    chunk = CHUNK if torch.device(device).type == "cpu" else CHUNK << 6
+    for c0 in range(0, n, chunk):
+        c1 = min(n, c0 + chunk)
         idx = torch.arange(start + c0, start + c1, dtype=torch.int64, device=device)
         out[c0:c1] = _normal_from_hash(hash_at(seed, name, idx), std, mean, dtype)
     return out
