@@ -155,7 +155,9 @@ GemmShape plan_shape(const H* h, const WSet& w, int M, int K, bool tc, int* grid
   g.m_blocks = ceil_div(M, bn);
   g.ks = ceil_div(K, kBK);
   g.units = (long long)g.m_blocks * g.n_tiles * g.ks;
-  int grid = static_cast<int>(std::min<long long>(h->sms, (g.units + 3) / 4));
+  // at least 4 units per CTA, and few enough CTAs per tile for the reducer's table
+  const long long per = std::max<long long>(4, (g.ks + 509) / 510);
+  int grid = static_cast<int>(std::min<long long>(h->sms, (g.units + per - 1) / per));
   *grid_out = std::max(1, grid);
   return g;
 }
@@ -210,20 +212,12 @@ struct AttnPlan {
 };
 
 AttnPlan plan_attn(const H* h, int B, int max_pages) {
+  // enough (b, kv head, split) CTAs to cover the SMs, at least 8 pages per split
   const int kp = max_pages + 1;
   const int groups = B * h->c.n_kv_heads;
-  int want = std::max(1, ceil_div(h->sms, groups));
-  int pps = std::max(8, ceil_div(kp, want));
-  int ns = ceil_div(kp, pps);
-  const int QR = h->c.block_size * (h->c.n_q_heads / h->c.n_kv_heads);
-  // the combine weights (ns x QR floats) reuse the K/V ring of the bf16 kernel
-  const int ring = 4 * 2 * kPage * h->c.head_dim * 2;
-  const int cap = std::min(64, h->bf16 ? ring / (QR * 4) : h->c.head_dim);
-  if (ns > cap) {
-    pps = ceil_div(kp, cap);
-    ns = ceil_div(kp, pps);
-  }
-  return {pps, ns};
+  const int want = std::max(1, ceil_div(h->sms, groups));
+  const int pps = std::max(8, ceil_div(kp, want));
+  return {pps, ceil_div(kp, pps)};
 }
 
 // ------------------------------------------------------------------ workspace plans
@@ -424,7 +418,6 @@ static dflash_status draft_impl(H* h, const int32_t* block_ids, const int32_t* c
       a.nsplit = ap.nsplit;
       a.part_o = w.part_o;
       a.part_ml = w.part_ml;
-      a.counters = w.ctl;
       a.out = static_cast<T*>(w.o);
       a.err = h->d_err;
       dim3 grid(ap.nsplit, c.n_kv_heads, B);
@@ -436,12 +429,13 @@ static dflash_status draft_impl(H* h, const int32_t* block_ids, const int32_t* c
         const uint64_t blk_rows = (uint64_t)B * c.n_kv_heads * S;
         TRY(encode_bf16(&mp.kb, w.kb, blk_rows, c.head_dim, c.head_dim, kPage));
         TRY(encode_bf16(&mp.vb, w.vb, blk_rows, c.head_dim, c.head_dim, kPage));
-        const int smem = 1024 + 4 * 2 * kPage * c.head_dim * 2 + 2 * 4 * 8 + 16;
+        const int smem = 1024 + kAttnStages * (2 * kPage * c.head_dim * 2 + 16) + 16;
         TRY(launch_attn_tc(c.head_dim, QR / 16, grid, smem, mp, a, st));
       } else {
         const int smem = (2 * QR * c.head_dim + 2 * kPage * c.head_dim + QR * kPage + 3 * QR) * 4;
         TRY(launch_attn_f32(grid, smem, a, st));
       }
+      if (ap.nsplit > 1) TRY(launch_attn_combine(B, a, st));
     }
     {  // output projection + residual
       WSet ws_;

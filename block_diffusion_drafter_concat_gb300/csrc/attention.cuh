@@ -6,8 +6,8 @@
 // 16-token page at a time; the work of one (b, g) is split over CTAs by contiguous
 // ranges of pages (split-context, "flash-decoding"), each CTA keeps an online softmax
 // (running max in the log2 domain, running sum, unnormalised output) and publishes
-// it; the last CTA of the group combines them in split order and writes the bf16
-// attention output in [B*S, hq*hd] layout for the output projection.
+// it; a combine kernel merges the splits in split order and writes the attention output
+// in [B*S, hq*hd] layout for the output projection (a single split writes it directly).
 //
 // bf16 kernel: K and V pages arrive by TMA (two-dimensional view of the pool,
 // 16 x 64 boxes, 128-byte swizzle) in a ring of mbarrier-tracked stages; QK^T and PV
@@ -34,7 +34,6 @@ struct AttnArgs {
   int nsplit;
   float* part_o;     // [B][hkv][nsplit][QR][hd]
   float* part_ml;    // [B][hkv][nsplit][QR][2]
-  int* counters;     // [B*hkv]
   T* out;            // [B*S][hq*hd]
   int* err;
 };
@@ -43,40 +42,77 @@ struct AttnMaps {
   CUtensorMap k, v, kb, vb;
 };
 
-// Combine the published splits of group (b, g): out = sum_s w_s o_s / sum_s w_s l_s.
+// Combine of the published splits, grid (ceil(QR / 8), hkv, B), 8 rows x hd/4 threads:
+// out[r] = sum_s w_s o_s / sum_s w_s l_s with w_s = 2^(m_s - max m), splits in order.
 template <typename T>
-__device__ void attn_combine(const AttnArgs<T>& a, int b, int g, int ns, float* wsm,
-                             int tid, int nthr) {
-  const int QR = a.QR, hd = a.hd, G = a.hq / a.hkv;
+__global__ void __launch_bounds__(256) k_attn_combine(const AttnArgs<T> a) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int b = blockIdx.z, g = blockIdx.y;
+  const int hd4 = a.hd / 4;
+  const int r = blockIdx.x * 8 + threadIdx.x / hd4, d4 = threadIdx.x % hd4;
+  if (r >= a.QR) return;
+  const int ctx = a.ctx_lens[b];
+  if (ctx < 0 || ctx > a.max_pages * kPage) return;   // reported by the attention kernel
+  const int kp = (ctx + kPage - 1) / kPage + 1;
+  const int ns = (kp + a.pps - 1) / a.pps;
   const long long grp = (long long)b * a.hkv + g;
-  const float* ml = a.part_ml + grp * a.nsplit * QR * 2;
-  for (int r = tid; r < QR; r += nthr) {
-    float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(ml + ((long long)s * QR + r) * 2));
-    float L = 0.f;
-    for (int s = 0; s < ns; ++s) {
-      float w = exp2f(__ldcg(ml + ((long long)s * QR + r) * 2) - M);
-      wsm[s * QR + r] = w;
-      L += w * __ldcg(ml + ((long long)s * QR + r) * 2 + 1);
-    }
-    float inv = 1.f / L;
-    for (int s = 0; s < ns; ++s) wsm[s * QR + r] *= inv;
+  const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + grp * a.nsplit * a.QR;
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[(long long)s * a.QR + r].x);
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4* po = reinterpret_cast<const float4*>(a.part_o + grp * a.nsplit * a.QR * a.hd);
+  for (int s0 = 0; s0 < ns; s0 += 8) {
+    float4 v[8];
+    float2 q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (s0 + j < ns) {
+        q[j] = ml[(long long)(s0 + j) * a.QR + r];
+        v[j] = po[((long long)(s0 + j) * a.QR + r) * hd4 + d4];
+      }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (s0 + j < ns) {
+        const float w = exp2f(q[j].x - M);
+        L += w * q[j].y;
+        acc.x += w * v[j].x; acc.y += w * v[j].y; acc.z += w * v[j].z; acc.w += w * v[j].w;
+      }
   }
-  __syncthreads();
-  const float* po = a.part_o + grp * a.nsplit * QR * hd;
-  for (int x = tid; x < QR * hd; x += nthr) {
-    int r = x / hd, d = x % hd;
-    float acc = 0.f;
-    for (int s = 0; s < ns; ++s) acc += wsm[s * QR + r] * __ldcg(po + (long long)s * QR * hd + x);
-    int i = r / G, hh = r % G;
-    a.out[((long long)b * a.S + i) * (a.hq * hd) + (g * G + hh) * hd + d] = from_f32<T>(acc);
+  const float inv = 1.f / L;
+  const int G = a.hq / a.hkv, i = r / G, hh = r % G;
+  T* dst = a.out + ((long long)b * a.S + i) * (a.hq * a.hd) + (g * G + hh) * a.hd + d4 * 4;
+  dst[0] = from_f32<T>(acc.x * inv);
+  dst[1] = from_f32<T>(acc.y * inv);
+  dst[2] = from_f32<T>(acc.z * inv);
+  dst[3] = from_f32<T>(acc.w * inv);
+}
+
+// A split's online-softmax state: with one split the output is final and written
+// directly, otherwise (o unnormalised, m, l) go to the partial buffers.
+template <typename T>
+__device__ __forceinline__ void attn_emit(const AttnArgs<T>& a, int b, int g, int split, int r,
+                                          int d, float o0, float o1, float l) {
+  const long long grp = (long long)b * a.hkv + g;
+  if (a.nsplit == 1) {
+    const float inv = 1.f / l;
+    const int G = a.hq / a.hkv, i = r / G, hh = r % G;
+    T* out = a.out + ((long long)b * a.S + i) * (a.hq * a.hd) + (g * G + hh) * a.hd + d;
+    out[0] = from_f32<T>(o0 * inv);
+    out[1] = from_f32<T>(o1 * inv);
+  } else {
+    float* po = a.part_o + ((grp * a.nsplit + split) * a.QR + r) * a.hd + d;
+    *reinterpret_cast<float2*>(po) = make_float2(o0, o1);
   }
 }
 
 // ------------------------------------------------------------------ bf16 tensor core
+constexpr int kAttnStages = 8;
+
 template <int HD>
 struct AttnCfg {
-  static constexpr int NS = 4;
+  static constexpr int NS = kAttnStages;
   static constexpr int TILE = kPage * HD * 2;   // one K (or V) page of one head
   static constexpr int STAGE = 2 * TILE;
   static constexpr int MAXSPLIT = 64;
@@ -91,8 +127,6 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::NS * C::STAGE);
   uint64_t* empty = full + C::NS;
-  int* flag = reinterpret_cast<int*>(empty + C::NS);
-  float* wsm = reinterpret_cast<float*>(smem);  // combine weights reuse the ring
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -248,15 +282,14 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const long long grp = (long long)b * a.hkv + g;
-    float* po = a.part_o + ((grp * a.nsplit + split) * a.QR + qr0) * HD;
 #pragma unroll
     for (int j = 0; j < HD / 8; ++j) {
-      int d = j * 8 + 2 * t4;
-      *reinterpret_cast<float2*>(po + g8 * HD + d) = make_float2(o[j][0], o[j][1]);
-      *reinterpret_cast<float2*>(po + (g8 + 8) * HD + d) = make_float2(o[j][2], o[j][3]);
+      const int d = j * 8 + 2 * t4;
+      attn_emit<bf16>(a, b, g, split, qr0 + g8, d, o[j][0], o[j][1], l0);
+      attn_emit<bf16>(a, b, g, split, qr0 + g8 + 8, d, o[j][2], o[j][3], l1);
     }
-    if (t4 == 0) {
+    if (t4 == 0 && a.nsplit > 1) {
+      const long long grp = (long long)b * a.hkv + g;
       float* pm = a.part_ml + ((grp * a.nsplit + split) * a.QR + qr0) * 2;
       pm[g8 * 2] = m0;
       pm[g8 * 2 + 1] = l0;
@@ -264,8 +297,6 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       pm[(g8 + 8) * 2 + 1] = l1;
     }
   }
-  if (elect_last(&a.counters[(long long)b * a.hkv + g], ns, flag))
-    attn_combine<bf16>(a, b, g, ns, wsm, tid, (NW + 1) * 32);
 }
 
 // ---------------------------------------------------------------------- fp32 path
@@ -281,7 +312,6 @@ static __global__ void __launch_bounds__(128) k_attn_f32(const AttnArgs<float> a
   float* mrow = Ss + QR * kPage;     // [QR]
   float* lrow = mrow + QR;
   float* arow = lrow + QR;
-  __shared__ int flag;
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
   pdl_launch_dependents();
   pdl_wait();
@@ -354,11 +384,19 @@ static __global__ void __launch_bounds__(128) k_attn_f32(const AttnArgs<float> a
     }
     __syncthreads();
   }
-  float* po = a.part_o + (grp * a.nsplit + split) * QR * hd;
-  for (int x = tid; x < QR * hd; x += 128) po[x] = Os[x];
-  float* pm = a.part_ml + (grp * a.nsplit + split) * QR * 2;
-  for (int r = tid; r < QR; r += 128) { pm[2 * r] = mrow[r]; pm[2 * r + 1] = lrow[r]; }
-  if (elect_last(&a.counters[grp], ns, &flag)) attn_combine<float>(a, b, g, ns, Qs, tid, 128);
+  for (int x = tid; x < QR * hd; x += 128) {
+    const int r = x / hd;
+    if (a.nsplit == 1) {
+      const int G = a.hq / a.hkv, i = r / G, hh = r % G, d = x % hd;
+      a.out[((long long)b * a.S + i) * (a.hq * hd) + (g * G + hh) * hd + d] = Os[x] / lrow[r];
+    } else {
+      a.part_o[(grp * a.nsplit + split) * QR * hd + x] = Os[x];
+    }
+  }
+  if (a.nsplit > 1) {
+    float* pm = a.part_ml + (grp * a.nsplit + split) * QR * 2;
+    for (int r = tid; r < QR; r += 128) { pm[2 * r] = mrow[r]; pm[2 * r + 1] = lrow[r]; }
+  }
 }
 
 }  // namespace dflash

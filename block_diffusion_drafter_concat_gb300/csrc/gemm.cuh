@@ -88,14 +88,31 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
 
   if constexpr (EPI == EPI_F32 || EPI == EPI_RESID) {
     const int nc = min(kBM, e.N - nt * kBM);
-    for (int i = tid; i < mr * kBM; i += nthr) {
-      int r = i / kBM, c = i % kBM;
-      if (c >= nc) continue;
-      float v = Cs[r * pitch + c];
-      float* dst = e.y + (long long)(m0 + r) * e.ldy + nt * kBM + c;
-      if constexpr (EPI == EPI_RESID) *dst += v; else *dst = v;
+    if (nc == kBM && (e.ldy & 3) == 0 && (pitch & 3) == 0) {
+      // full tile: float4 accesses, four in flight per thread
+#pragma unroll 4
+      for (int i = tid; i < mr * (kBM / 4); i += nthr) {
+        const int r = i / (kBM / 4), c4 = i % (kBM / 4);
+        float4 v = *reinterpret_cast<const float4*>(Cs + r * pitch + c4 * 4);
+        float4* dst = reinterpret_cast<float4*>(e.y + (long long)(m0 + r) * e.ldy + nt * kBM) + c4;
+        if constexpr (EPI == EPI_RESID) {
+          float4 o = *dst;
+          v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+        }
+        *dst = v;
+      }
+    } else {
+#pragma unroll 4
+      for (int i = tid; i < mr * kBM; i += nthr) {
+        int r = i / kBM, c = i % kBM;
+        if (c >= nc) continue;
+        float v = Cs[r * pitch + c];
+        float* dst = e.y + (long long)(m0 + r) * e.ldy + nt * kBM + c;
+        if constexpr (EPI == EPI_RESID) *dst += v; else *dst = v;
+      }
     }
   } else if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll 4
     for (int i = tid; i < mr * 64; i += nthr) {
       int r = i / 64, c = i % 64;
       int f = r0 + c;
@@ -112,6 +129,7 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
     else { layer = seg >> 1; kind = 1 + (seg & 1); }
     const int G = e.hq / e.hkv;
     if (kind == 2) {
+#pragma unroll 4
       for (int i = tid; i < mr * kBM; i += nthr) {
         int r = i / kBM, c = i % kBM;
         int f = r0 + c, m = m0 + r;
@@ -130,6 +148,7 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
       }
     } else {
       // rotary pairs (j, j + hd/2) of one head lie in the same 128-column tile
+#pragma unroll 4
       for (int i = tid; i < mr * (kBM / 2); i += nthr) {
         int r = i / (kBM / 2), cc = i % (kBM / 2);
         int hl = cc / half, j = cc % half;
@@ -203,7 +222,9 @@ struct TcCfg {
   static constexpr int STAGE = W_BYTES + A_BYTES;
   static constexpr int PITCH = kBM + 4;
   static constexpr int CS_BYTES = BN * PITCH * 4;
-  static constexpr int SMEM = 1024 /*align slack*/ + NS * STAGE + CS_BYTES + 2 * NS * 8 + 16;
+  static constexpr int MAXC = 512;  // contributors of one tile (units per CTA >= 4)
+  static constexpr int SMEM = 1024 /*align slack*/ + NS * STAGE + CS_BYTES + 2 * NS * 8 + 16 +
+                              MAXC * 4;
   static constexpr int THREADS = 160;  // 4 consumer warps + 1 TMA producer warp
 };
 
@@ -230,6 +251,7 @@ __global__ void __launch_bounds__(160, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::NS * C::STAGE + C::CS_BYTES);
   uint64_t* empty = full + C::NS;
   int* flag = reinterpret_cast<int*>(empty + C::NS);
+  int* cslot = flag + 4;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grid = gridDim.x, cta = blockIdx.x;
@@ -380,7 +402,10 @@ __global__ void __launch_bounds__(160, 1)
       // publish this piece, then let the last contributor of the tile finish it
       const int slot = (u == u0) ? 0 : 1;
       float* dst = g.part + ((long long)cta * 2 + slot) * BN * kBM;
-      for (int x = tid; x < BN * kBM; x += 128) dst[x] = Cs[(x / kBM) * C::PITCH + x % kBM];
+      for (int x = tid; x < BN * kBM / 4; x += 128) {
+        const int r = x / (kBM / 4), c4 = x % (kBM / 4);
+        reinterpret_cast<float4*>(dst)[x] = *reinterpret_cast<const float4*>(Cs + r * C::PITCH + c4 * 4);
+      }
       // contributors: the CTAs whose unit ranges intersect [ts, tile_end)
       const long long ts = static_cast<long long>(t) * g.ks;
       int clo = static_cast<int>((ts * grid) / g.units);
@@ -398,15 +423,32 @@ __global__ void __launch_bounds__(160, 1)
       consumer_sync();
       mine = *flag != 0;
       if (mine) {
-        for (int x = tid; x < BN * kBM; x += 128) {
-          float v = 0.f;
-          for (int c = clo; c <= chi; ++c) {
-            long long cu0 = g.units * c / grid;
-            int sl = (cu0 / g.ks == t) ? 0 : 1;
-            if (c == cta) sl = slot;
-            v += __ldcg(g.part + ((long long)c * 2 + sl) * BN * kBM + x);
+        // partial slots of the contributors, in contributor order
+        const int nc = chi - clo + 1;
+        for (int c = tid; c < nc; c += 128) {
+          const int cc = clo + c;
+          const long long cu0 = g.units * cc / grid;
+          cslot[c] = cc * 2 + ((cu0 / g.ks == t) ? 0 : 1);
+        }
+        consumer_sync();
+        // sum the published partials in contributor order; loads of up to four
+        // contributors are in flight together
+        for (int x = tid; x < BN * kBM / 4; x += 128) {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int c0 = 0; c0 < nc; c0 += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (c0 + j < nc)
+                v[j] = __ldcg(reinterpret_cast<const float4*>(g.part + (long long)cslot[c0 + j] * BN * kBM) + x);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (c0 + j < nc) {
+                acc.x += v[j].x; acc.y += v[j].y; acc.z += v[j].z; acc.w += v[j].w;
+              }
           }
-          Cs[(x / kBM) * C::PITCH + x % kBM] = v;
+          const int r = x / (kBM / 4), c4 = x % (kBM / 4);
+          *reinterpret_cast<float4*>(Cs + r * C::PITCH + c4 * 4) = acc;
         }
         consumer_sync();
       }
@@ -436,7 +478,7 @@ __global__ void __launch_bounds__(256)
                const EpiArgs<float> e) {
   __shared__ float As[kF32BN][kF32BK + 1];
   __shared__ float Ws[kBM][kF32BK + 1];
-  __shared__ float Cs[kF32BN * (kBM + 4)];
+  __shared__ __align__(16) float Cs[kF32BN * (kBM + 4)];
   pdl_launch_dependents();
   pdl_wait();
   const int t = blockIdx.x;

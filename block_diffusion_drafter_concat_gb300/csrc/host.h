@@ -73,5 +73,7 @@ dflash_status launch_gemm_f32(int epi, dim3 grid, const float* A, int lda, const
 dflash_status launch_attn_tc(int hd, int nw, dim3 grid, int smem, const AttnMaps& mp,
                              const AttnArgs<bf16>& a, cudaStream_t st);
 dflash_status launch_attn_f32(dim3 grid, int smem, const AttnArgs<float>& a, cudaStream_t st);
+dflash_status launch_attn_combine(int B, const AttnArgs<bf16>& a, cudaStream_t st);
+dflash_status launch_attn_combine(int B, const AttnArgs<float>& a, cudaStream_t st);
 
 }  // namespace dflash

@@ -60,6 +60,34 @@ __global__ void __launch_bounds__(kRowThreads)
       y[(long long)m * d + c] = from_f32<T>(to_f32<T>(e[c]) * rs * to_f32<T>(gain[c]));
     return;
   }
+  if constexpr (sizeof(Tin) == 4) {
+    if ((d & 3) == 0 && d <= kRowThreads * 4 * 8) {
+      // the row stays in registers: up to 8 float4 per thread, all loads in flight
+      float4 v[8];
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int c = (k * kRowThreads + threadIdx.x) * 4;
+        if (c < d) {
+          v[k] = *reinterpret_cast<const float4*>(src + c);
+          ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+        }
+      }
+      const float rs = 1.0f / sqrtf(block_sum(ss, red) / d + eps);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int c = (k * kRowThreads + threadIdx.x) * 4;
+        if (c < d) {
+          T* o = y + (long long)m * d + c;
+          o[0] = from_f32<T>(v[k].x * rs * to_f32<T>(gain[c]));
+          o[1] = from_f32<T>(v[k].y * rs * to_f32<T>(gain[c + 1]));
+          o[2] = from_f32<T>(v[k].z * rs * to_f32<T>(gain[c + 2]));
+          o[3] = from_f32<T>(v[k].w * rs * to_f32<T>(gain[c + 3]));
+        }
+      }
+      return;
+    }
+  }
   float ss = 0.f;
   for (int c = threadIdx.x; c < d; c += kRowThreads) {
     float v = to_f32<Tin>(src[c]);

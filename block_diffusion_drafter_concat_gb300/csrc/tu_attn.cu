@@ -43,4 +43,16 @@ dflash_status launch_attn_f32(dim3 grid, int smem, const AttnArgs<float>& a, cud
   return launch(k_attn_f32, grid, dim3(128), smem, st, a);
 }
 
+template <typename T>
+static dflash_status combine(int B, const AttnArgs<T>& a, cudaStream_t st) {
+  dim3 grid((a.QR + 7) / 8, a.hkv, B);
+  return launch(k_attn_combine<T>, grid, dim3(8 * a.hd / 4), 0, st, a);
+}
+dflash_status launch_attn_combine(int B, const AttnArgs<bf16>& a, cudaStream_t st) {
+  return combine(B, a, st);
+}
+dflash_status launch_attn_combine(int B, const AttnArgs<float>& a, cudaStream_t st) {
+  return combine(B, a, st);
+}
+
 }  // namespace dflash

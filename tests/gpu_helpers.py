@@ -46,3 +46,23 @@ def check_greedy(gpu_out, gpu_nacc, gpu_nemit, draft_o, logits_row, low):
     assert int(gpu_nacc) == n and int(gpu_nemit) == ne, (int(gpu_nacc), n, int(gpu_nemit), ne)
     assert list(np.asarray(gpu_out)) == list(out)
     return True
+
+
+def sample_ambiguous(draft, z, logits, u, tau, eps=1e-3):
+    """True when a fp32 evaluation could take a different branch than fp64: an
+    acceptance ratio or a residual CDF step within eps of the uniform."""
+    S = len(draft)
+    for i in range(S):
+        p = O.softmax(logits[i] / tau)
+        q = O.softmax(z[i] / tau)
+        d = int(draft[i])
+        if abs(u[i, 0] * q[d] - p[d]) <= eps * max(p[d], q[d]):
+            return True
+        if u[i, 0] < p[d] / q[d]:
+            continue
+        r = np.maximum(0, p - q)
+        if r.sum() == 0:
+            r = p
+        cdf = np.cumsum(r)
+        return bool(np.min(np.abs(cdf - u[i, 1] * r.sum())) <= eps * r.sum())
+    return False

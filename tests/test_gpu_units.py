@@ -9,7 +9,7 @@ from oracle import dflash_oracle as O
 from oracle import run as orun
 from workload import configs, inputs, synth
 
-from gpu_helpers import MARGIN, check_drafts, rel_err
+from gpu_helpers import MARGIN, check_drafts, rel_err, sample_ambiguous
 
 pytestmark = pytest.mark.gpu
 
@@ -79,26 +79,6 @@ def test_verify_greedy_exact(small):
         assert (int(na[b]), int(ne[b])) == (n, e)
         assert out[b].cpu().tolist() == list(o)
     assert int(ne[0]) == S and int(ne[1]) == 1 and int(na[2]) == 5
-
-
-def sample_ambiguous(draft, z, logits, u, tau, eps=1e-3):
-    """True when a fp32 evaluation could take a different branch than fp64: an
-    acceptance ratio or a residual CDF step within eps of the uniform."""
-    S = len(draft)
-    for i in range(S):
-        p = O.softmax(logits[i] / tau)
-        q = O.softmax(z[i] / tau)
-        d = int(draft[i])
-        if abs(u[i, 0] * q[d] - p[d]) <= eps * max(p[d], q[d]):
-            return True
-        if u[i, 0] < p[d] / q[d]:
-            continue
-        r = np.maximum(0, p - q)
-        if r.sum() == 0:
-            r = p
-        cdf = np.cumsum(r)
-        return bool(np.min(np.abs(cdf - u[i, 1] * r.sum())) <= eps * r.sum())
-    return False
 
 
 def test_verify_sample_matches_oracle(small):
