@@ -11,7 +11,8 @@
 //
 // bf16 kernel: K and V pages arrive by TMA (two-dimensional view of the pool,
 // 16 x 64 boxes, 128-byte swizzle) in a ring of mbarrier-tracked stages; QK^T and PV
-// run on mma.sync.m16n8k16 with the probabilities re-used from the score registers.
+// run on mma.sync.m16n8k16 with the probabilities re-used from the score registers
+// (as a bf16 hi/lo pair).
 #pragma once
 
 #include "common.cuh"
@@ -261,11 +262,14 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         o[j][0] *= al0; o[j][1] *= al0;
         o[j][2] *= al1; o[j][3] *= al1;
       }
-      uint32_t pa[4];
-      pa[0] = pack_bf16x2(p[0][0], p[0][1]);
-      pa[1] = pack_bf16x2(p[0][2], p[0][3]);
-      pa[2] = pack_bf16x2(p[1][0], p[1][1]);
-      pa[3] = pack_bf16x2(p[1][2], p[1][3]);
+      // P as a bf16 pair hi + lo: a single bf16 P would put a 2^-9 relative error on
+      // the output (a sum of zero-mean terms, so it does not average out); the pair
+      // keeps it near 2^-17 for a second MMA per tile.
+      uint32_t pa[4], pl[4];
+      split_bf16x2(p[0][0], p[0][1], pa[0], pl[0]);
+      split_bf16x2(p[0][2], p[0][3], pa[1], pl[1]);
+      split_bf16x2(p[1][0], p[1][1], pa[2], pl[2]);
+      split_bf16x2(p[1][2], p[1][3], pa[3], pl[3]);
 #pragma unroll
       for (int dj = 0; dj < HD / 16; ++dj) {
         uint32_t vf[4];
@@ -274,6 +278,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         ldsm_x4_trans(vf, vbase + (ch >> 3) * 2048 + swz128(key, ch & 7));
         mma_bf16(o[2 * dj], pa, vf[0], vf[1]);
         mma_bf16(o[2 * dj + 1], pa, vf[2], vf[3]);
+        mma_bf16(o[2 * dj], pl, vf[0], vf[1]);
+        mma_bf16(o[2 * dj + 1], pl, vf[2], vf[3]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);

@@ -136,6 +136,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+// (a, b) as bf16 pairs hi = bf16(a, b) and lo = bf16((a, b) - hi).
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  float2 hf = __bfloat1622float2(h);
+  hi = *reinterpret_cast<uint32_t*>(&h);
+  lo = pack_bf16x2(a - hf.x, b - hf.y);
+}
 
 // ------------------------------------------------------------------ PDL
 // Programmatic dependent launch: the next kernel on the stream may be scheduled once
