@@ -23,6 +23,7 @@ DEV_ERRORS = {0: "ok", 1: "index out of range", 2: "position out of range", 3: "
 API = ["dflash_create", "dflash_destroy", "dflash_workspace_size", "dflash_workspace_init",
        "dflash_fuse_features", "dflash_inject_kv", "dflash_draft_block",
        "dflash_lm_head_argmax", "dflash_verify_greedy", "dflash_verify_sample",
+       "dflash_verify_greedy_static",
        "dflash_get_device_error", "dflash_last_error", "dflash_last_launch_count"]
 
 
@@ -74,6 +75,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "dflash_lm_head_argmax": [P, P, i32, ctypes.c_float, P, P, P, P, sz, P],
         "dflash_verify_greedy": [P, P, P, i32, P, P, P, P, sz, P],
         "dflash_verify_sample": [P, P, P, P, P, P, P, ctypes.c_float, i32, P, P, P, P, sz, P],
+        "dflash_verify_greedy_static": [P, P, P, i32, P, P, P, P],
         "dflash_get_device_error": [P, ctypes.POINTER(i32), i32],
         "dflash_last_error": [],
         "dflash_last_launch_count": [],

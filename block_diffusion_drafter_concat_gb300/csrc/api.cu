@@ -876,3 +876,82 @@ dflash_status dflash_get_device_error(dflash_handle h, int32_t* code, int32_t cl
 }
 
 }  // extern "C"
+
+// ------------------------------------------------- greedy verification, no allocation
+// Some callers cannot allocate device memory where they verify a block: a host runtime
+// that hands out only buffers it already owns, code running under a frozen memory
+// budget where cudaMalloc is forbidden, or a plain C caller with no allocator at all.
+// dflash_verify_greedy_static serves them with the same kernel and the same results as
+// dflash_verify_greedy; its scratch (per-chunk partial argmaxes and per-sequence
+// counters) lives in one fixed device array of this library.
+namespace {
+constexpr size_t kStaticScratchBytes = 256 * 1024;  // per device, held until exit
+constexpr int kStaticMaxRows = 16384;               // batch * block_size
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+std::mutex g_static_mu;
+void* g_static_ptr[256] = {};  // device address of g_static_scratch, per device
+
+// In host code the array's name only stands in for it; its device address is looked
+// up once per device, with that device current, on the first call there.
+dflash_status static_scratch(void** out) {
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 256) return fail(DFLASH_EUNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(DFLASH_ECUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return DFLASH_OK;
+}
+}  // namespace
+
+extern "C" dflash_status dflash_verify_greedy_static(dflash_handle h, const int32_t* draft,
+                                                     const void* target_logits, int32_t batch,
+                                                     int32_t* out_tokens, int32_t* n_accepted,
+                                                     int32_t* n_emitted, void* stream) {
+  g_launches = 0;
+  if (!h) return fail(DFLASH_EINVAL, "null handle");
+  if (batch < 0) return fail(DFLASH_EINVAL, "batch < 0");
+  if (batch == 0) return DFLASH_OK;
+  NEED(draft, "draft");
+  NEED(target_logits, "target_logits");
+  NEED(out_tokens, "out_tokens");
+  NEED(n_accepted, "n_accepted");
+  NEED(n_emitted, "n_emitted");
+  const int S = h->c.block_size, V = h->c.vocab;
+  if (S > 64) return fail(DFLASH_EUNSUPPORTED, "block_size > 64");
+  if ((long long)batch * S > kStaticMaxRows)
+    return fail(DFLASH_EUNSUPPORTED,
+                "batch*block_size = %lld exceeds the static scratch limit of %d rows",
+                (long long)batch * S, kStaticMaxRows);
+  const int rows = batch * S;
+  const int nch = verify_chunks(h, rows), chunk = chunk_of(h, nch);
+  // layout: counters [batch], partial values [rows*nch], partial indices [rows*nch]
+  const size_t off_v = ((size_t)batch * 4 + 255) & ~size_t(255);
+  const size_t off_i = (off_v + (size_t)rows * nch * 4 + 255) & ~size_t(255);
+  const size_t need = off_i + (size_t)rows * nch * 4;
+  if (need > kStaticScratchBytes)
+    return fail(DFLASH_EUNSUPPORTED, "static scratch too small: %zu > %zu bytes", need,
+                kStaticScratchBytes);
+  void* base = nullptr;
+  TRY(static_scratch(&base));
+  char* b = static_cast<char*>(base);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the counters must start at zero whatever an earlier call left in the array
+  CUDA_TRY(cudaMemsetAsync(b, 0, (size_t)batch * 4, st));
+  int* ctr = reinterpret_cast<int*>(b);
+  float* pv = reinterpret_cast<float*>(b + off_v);
+  int* pi = reinterpret_cast<int*>(b + off_i);
+  if (h->bf16)
+    return launch(k_verify_greedy<bf16>, dim3(nch, rows), dim3(kRowThreads), 0, st,
+                  static_cast<const bf16*>(target_logits), draft, S, V, chunk, pv, pi, ctr,
+                  out_tokens, n_accepted, n_emitted, h->d_err);
+  return launch(k_verify_greedy<float>, dim3(nch, rows), dim3(kRowThreads), 0, st,
+                static_cast<const float*>(target_logits), draft, S, V, chunk, pv, pi, ctr,
+                out_tokens, n_accepted, n_emitted, h->d_err);
+}

@@ -203,6 +203,22 @@ DFLASH_API dflash_status dflash_verify_sample(dflash_handle h, const int32_t* dr
                                    int32_t* n_emitted, void* ws, size_t ws_bytes,
                                    void* stream);
 
+/* Greedy verification that allocates nothing and takes no workspace.  The paper has no
+ * counterpart: this exists for callers that cannot call cudaMalloc where they verify a
+ * block (a host runtime that owns only fixed buffers, a memory budget frozen at that
+ * point, a plain C caller without an allocator).  Same inputs, outputs and results as
+ * dflash_verify_greedy; its scratch is one fixed 256 KiB device array of the library
+ * (held by every GPU that loads the library until exit), so batch * block_size must
+ * not exceed 16384 (larger requests return DFLASH_EUNSUPPORTED with a message).  The
+ * first call on a device looks up that array's device address (cudaGetSymbolAddress,
+ * with the device current); make that first call before any stream capture.  Each call
+ * clears the array's counters on `stream` before use.  All calls share the one array:
+ * calls whose work overlaps on the GPU (other streams, other threads) race. */
+DFLASH_API dflash_status dflash_verify_greedy_static(dflash_handle h, const int32_t* draft,
+                                                     const void* target_logits, int32_t batch,
+                                                     int32_t* out_tokens, int32_t* n_accepted,
+                                                     int32_t* n_emitted, void* stream);
+
 /* Synchronizes the device, returns the handle's error word in *code (DFLASH_DEV_*)
  * and zeroes it when clear != 0. */
 DFLASH_API dflash_status dflash_get_device_error(dflash_handle h, int32_t* code, int32_t clear);
