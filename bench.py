@@ -29,7 +29,7 @@ sys.path.insert(0, ROOT)
 METRIC = "draft+verify steps/sec and tokens/sec; achieved HBM GB/s vs ~8 TB/s (1 GB300)"
 DEFAULT_CONFIG = "qwen3-8b-shaped-b1"
 # ncu summary of the LM-head kernel on this workload: DRAM bytes per launch, or None
-LM_HEAD_TRAFFIC = None
+LM_HEAD_TRAFFIC = 1251274432  # dram read + write bytes of one launch (ncu)
 
 
 def parse():
