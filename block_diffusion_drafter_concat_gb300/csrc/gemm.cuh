@@ -239,6 +239,24 @@ __device__ __forceinline__ void cta_range(long long units, int c, int grid, long
   u1 = units * (c + 1) / grid;
 }
 
+// Contributors of tile t (units [t*ks, (t+1)*ks)): the CTAs whose non-empty unit range
+// intersects it, in CTA order.  Writes each one's partial slot (cta*2 + 0 when its range
+// starts inside the tile, + 1 when the tile is the last piece of its range) to `slots`
+// when given, and returns how many there are.
+__device__ __forceinline__ int tile_contributors(long long units, int grid, int ks, int t,
+                                                 int* slots) {
+  const long long ts = static_cast<long long>(t) * ks, te = ts + ks;
+  int n = 0;
+  for (int c = static_cast<int>((ts * grid) / units); c < grid; ++c) {
+    const long long s0 = units * c / grid, s1 = units * (c + 1) / grid;
+    if (s0 >= te) break;
+    if (s1 <= ts || s0 == s1) continue;
+    if (slots) slots[n] = c * 2 + ((s0 / ks == t) ? 0 : 1);
+    ++n;
+  }
+  return n;
+}
+
 template <int BN, int EPI>
 __global__ void __launch_bounds__(160, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ WMaps wm,
@@ -406,17 +424,12 @@ __global__ void __launch_bounds__(160, 1)
         const int r = x / (kBM / 4), c4 = x % (kBM / 4);
         reinterpret_cast<float4*>(dst)[x] = *reinterpret_cast<const float4*>(Cs + r * C::PITCH + c4 * 4);
       }
-      // contributors: the CTAs whose unit ranges intersect [ts, tile_end)
-      const long long ts = static_cast<long long>(t) * g.ks;
-      int clo = static_cast<int>((ts * grid) / g.units);
-      while ((g.units * (clo + 1)) / grid <= ts) ++clo;
-      int chi = clo;
-      while (chi + 1 < grid && (g.units * (chi + 1)) / grid < tile_end) ++chi;
+      const int nc = tile_contributors(g.units, grid, g.ks, t, nullptr);
       __threadfence();
       consumer_sync();
       if (tid == 0) {
         int prev = atomicAdd(&g.counters[t], 1);
-        int last = (prev == chi - clo);
+        int last = (prev == nc - 1);
         if (last) { atomicExch(&g.counters[t], 0); __threadfence(); }
         *flag = last;
       }
@@ -424,12 +437,7 @@ __global__ void __launch_bounds__(160, 1)
       mine = *flag != 0;
       if (mine) {
         // partial slots of the contributors, in contributor order
-        const int nc = chi - clo + 1;
-        for (int c = tid; c < nc; c += 128) {
-          const int cc = clo + c;
-          const long long cu0 = g.units * cc / grid;
-          cslot[c] = cc * 2 + ((cu0 / g.ks == t) ? 0 : 1);
-        }
+        if (tid == 0) tile_contributors(g.units, grid, g.ks, t, cslot);
         consumer_sync();
         // sum the published partials in contributor order; loads of up to four
         // contributors are in flight together
