@@ -9,7 +9,6 @@
 #include <cstdio>
 #include <type_traits>
 #include <cstring>
-#include <initializer_list>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -363,116 +362,6 @@ static dflash_status fuse_impl(H* h, const void* x_cat, int n, void* fused, floa
   return rmsnorm<float, float>(h, u, h->g_fuse, static_cast<float*>(fused), n, st);
 }
 
-// The whole layer stack as one persistent kernel when the block is small: batch x block
-// <= 16 rows, head_dim 128 with 64 query rows per kv head (the batch-1 shapes).
-static bool persist_eligible(const H* h, int B) {
-  const auto& c = h->c;
-  return h->bf16 && B * c.block_size <= 16 && c.head_dim == kPHD &&
-         c.block_size * (c.n_q_heads / c.n_kv_heads) == kPQR && c.n_layers <= kPMaxLayers &&
-         c.d_model % 4 == 0 && persist_max_grid(h->sms) > 0;
-}
-
-static dflash_status draft_persist(H* h, const int32_t* ctx_lens, const int32_t* page_table,
-                                   int32_t max_pages, int32_t B, int32_t num_pages,
-                                   void* const* k_pool, void* const* v_pool, void* final_hidden,
-                                   const DraftWs& w, cudaStream_t st) {
-  const auto& c = h->c;
-  const int S = c.block_size, M = B * S, d = c.d_model;
-  const int qw = c.n_q_heads * c.head_dim, kvw = c.n_kv_heads * c.head_dim, F = c.ffn_dim;
-  const int grid = persist_max_grid(h->sms);
-  const AttnPlan ap = plan_attn(h, B, max_pages);
-  thread_local PersistMaps maps;  // large: built on the host, passed by value at launch
-  thread_local PersistArgs a;
-  memset(&a, 0, sizeof a);
-  const uint64_t pool_rows = (uint64_t)num_pages * c.n_kv_heads * kPage;
-  for (int l = 0; l < c.n_layers; ++l) {
-    maps.m[9 * l + 0] = h->m_q[l];
-    maps.m[9 * l + 1] = h->m_k[l];
-    maps.m[9 * l + 2] = h->m_v[l];
-    maps.m[9 * l + 3] = h->m_o[l];
-    maps.m[9 * l + 4] = h->m_gate[l];
-    maps.m[9 * l + 5] = h->m_up[l];
-    maps.m[9 * l + 6] = h->m_down[l];
-    TRY(encode_bf16(&maps.m[9 * l + 7], k_pool[l], pool_rows, c.head_dim, c.head_dim, kPage));
-    TRY(encode_bf16(&maps.m[9 * l + 8], v_pool[l], pool_rows, c.head_dim, c.head_dim, kPage));
-    a.g_attn[l] = static_cast<const bf16*>(h->g_attn[l]);
-    a.g_mlp[l] = static_cast<const bf16*>(h->g_mlp[l]);
-  }
-  TRY(encode_bf16(&maps.m[kMapN], w.n, M, d, d, 16));
-  TRY(encode_bf16(&maps.m[kMapO], w.o, M, qw, qw, 16));
-  TRY(encode_bf16(&maps.m[kMapAct], w.act, M, F, F, 16));
-  const uint64_t blk_rows = (uint64_t)B * c.n_kv_heads * S;
-  TRY(encode_bf16(&maps.m[kMapKb], w.kb, blk_rows, c.head_dim, c.head_dim, kPage));
-  TRY(encode_bf16(&maps.m[kMapVb], w.vb, blk_rows, c.head_dim, c.head_dim, kPage));
-
-  auto gemm_phase = [&](int layer, int epi, int K, std::initializer_list<int> maps_,
-                        std::initializer_list<int> rows, bool paired, int amap) {
-    PPhase& p = a.ph[a.n_phases++];
-    p.type = PH_GEMM;
-    p.epi = epi;
-    p.layer = layer;
-    p.K = K;
-    p.ks = ceil_div(K, kBK);
-    p.paired = paired;
-    p.amap = amap;
-    int t = 0, sidx = 0;
-    auto r = rows.begin();
-    for (int m : maps_) {
-      p.wmap[sidx] = m;
-      p.seg_tile0[sidx] = t;
-      p.seg_rows[sidx] = *r;
-      t += paired ? (sidx == 0 ? ceil_div(*r, kBM / 2) : 0) : ceil_div(*r, kBM);
-      ++sidx;
-      ++r;
-    }
-    p.nseg = sidx;
-    for (int q = sidx; q < 4; ++q) p.seg_tile0[q] = t;
-    if (paired) p.seg_tile0[1] = t;
-    p.n_tiles = t;
-    p.units = (long long)t * p.ks;
-  };
-  auto simple_phase = [&](int type, int layer, int epi, int final_norm) {
-    PPhase& p = a.ph[a.n_phases++];
-    p.type = type;
-    p.layer = layer;
-    p.epi = epi;
-    p.final_norm = final_norm;
-  };
-  for (int l = 0; l < c.n_layers; ++l) {
-    gemm_phase(l, EPI_QKV, d, {9 * l + 0, 9 * l + 1, 9 * l + 2}, {qw, kvw, kvw}, false, kMapN);
-    simple_phase(PH_ATTN, l, 0, 0);
-    if (ap.nsplit > 1) simple_phase(PH_COMBINE, l, 0, 0);
-    gemm_phase(l, EPI_RESID, qw, {9 * l + 3}, {d}, false, kMapO);
-    simple_phase(PH_NORM, l, 0, 0);
-    gemm_phase(l, EPI_SWIGLU, d, {9 * l + 4, 9 * l + 5}, {F, F}, true, kMapN);
-    gemm_phase(l, EPI_RESID, F, {9 * l + 6}, {d}, false, kMapAct);
-    if (l + 1 < c.n_layers) simple_phase(PH_NORM, l + 1, 1, 0);
-    else simple_phase(PH_NORM, l, 0, 1);
-  }
-  for (int p = 0; p < a.n_phases; ++p)
-    if (a.ph[p].type == PH_GEMM) {
-      const PPhase& q = a.ph[p];
-      if (q.n_tiles > kCtlWords - 2 || (long long)q.ks * grid / std::max<long long>(1, q.units) + 2 > kPMaxC)
-        return fail(DFLASH_EUNSUPPORTED, "persistent phase %d too fragmented", p);
-    }
-  a.n_layers = c.n_layers;
-  a.d = d; a.qw = qw; a.kvw = kvw; a.F = F;
-  a.hq = c.n_q_heads; a.hkv = c.n_kv_heads; a.S = S; a.B = B; a.M = M;
-  a.ctx_lens = ctx_lens; a.page_table = page_table;
-  a.max_pages = max_pages; a.num_pages = num_pages; a.pps = ap.pps; a.nsplit = ap.nsplit;
-  a.part_o = w.part_o; a.part_ml = w.part_ml;
-  a.x = w.x; a.n = static_cast<bf16*>(w.n); a.q = static_cast<bf16*>(w.q);
-  a.kb = static_cast<bf16*>(w.kb); a.vb = static_cast<bf16*>(w.vb);
-  a.o = static_cast<bf16*>(w.o); a.act = static_cast<bf16*>(w.act);
-  a.final_hidden = static_cast<bf16*>(final_hidden);
-  a.pos = w.pos; a.rope = h->d_rope; a.max_pos = c.max_position;
-  a.g_final = static_cast<const bf16*>(h->g_final);
-  a.eps = c.rms_eps;
-  a.part = w.gpart; a.counters = w.ctl; a.bar = w.ctl + kCtlWords - 2;
-  a.err = h->d_err;
-  return launch_persist(grid, maps, a, st);
-}
-
 template <typename T>
 static dflash_status draft_impl(H* h, const int32_t* block_ids, const int32_t* ctx_lens,
                                 const int32_t* page_table, int32_t max_pages, int32_t B,
@@ -488,11 +377,6 @@ static dflash_status draft_impl(H* h, const int32_t* block_ids, const int32_t* c
              static_cast<const float*>(nullptr), w.x, static_cast<const T*>(h->g_attn[0]), n, d,
              c.rms_eps, block_ids, static_cast<const T*>(h->embed), c.vocab, ctx_lens, S,
              c.max_position, w.pos, h->d_err));
-  if constexpr (std::is_same<T, bf16>::value) {
-    if (persist_eligible(h, B))
-      return draft_persist(h, ctx_lens, page_table, max_pages, B, num_pages, k_pool, v_pool,
-                           final_hidden, w, st);
-  }
   const AttnPlan ap = plan_attn(h, B, max_pages);
   for (int l = 0; l < c.n_layers; ++l) {
     {  // Q, K, V with RoPE

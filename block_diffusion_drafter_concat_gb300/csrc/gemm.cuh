@@ -147,8 +147,9 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
         }
       }
     } else {
-      // rotary pairs (j, j + hd/2) of one head lie in the same 128-column tile
-#pragma unroll 4
+      // rotary pairs (j, j + hd/2) of one head lie in the same 128-column tile; the
+      // loop is unrolled so that the position and table loads of several pairs overlap
+#pragma unroll 8
       for (int i = tid; i < mr * (kBM / 2); i += nthr) {
         int r = i / (kBM / 2), cc = i % (kBM / 2);
         int hl = cc / half, j = cc % half;
@@ -257,6 +258,30 @@ __device__ __forceinline__ int tile_contributors(long long units, int grid, int 
   return n;
 }
 
+// Incremental walk over (m-block, n-tile, k-stage) units for the TMA producer:
+// coordinates of the weight box (segment, row, k) and the activation box (m-block).
+struct UnitWalk {
+  int ks, nt, mb, seg, row;
+  __device__ __forceinline__ void locate(const GemmShape& g) {
+    seg = 0;
+    while (seg + 1 < g.nseg && nt >= g.seg_tile0[seg + 1]) ++seg;
+    row = g.paired ? nt * (kBM / 2) : (nt - g.seg_tile0[seg]) * kBM;
+  }
+  __device__ __forceinline__ void start(const GemmShape& g, long long u) {
+    const int t = static_cast<int>(u / g.ks);
+    ks = static_cast<int>(u - static_cast<long long>(t) * g.ks);
+    mb = t / g.n_tiles;
+    nt = t - mb * g.n_tiles;
+    locate(g);
+  }
+  __device__ __forceinline__ void next(const GemmShape& g) {
+    if (++ks < g.ks) return;
+    ks = 0;
+    if (++nt == g.n_tiles) { nt = 0; ++mb; }
+    locate(g);
+  }
+};
+
 template <int BN, int EPI>
 __global__ void __launch_bounds__(160, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ WMaps wm,
@@ -290,52 +315,51 @@ __global__ void __launch_bounds__(160, 1)
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      // The single issuing thread must keep up with HBM (one 16 KB weight box every
+      // ~0.3 us per SM), so the unit walk is incremental: no division per unit.
       tma_prefetch_desc(&tmA);
       const uint64_t pol = policy_evict_first();
-      auto unit_coords = [&](long long u, int& t, int& ks, int& mb, int& nt) {
-        t = static_cast<int>(u / g.ks);
-        ks = static_cast<int>(u % g.ks);
-        mb = t / g.n_tiles;
-        nt = t % g.n_tiles;
-      };
-      auto issue_w = [&](int i, long long u) {
-        int t, ks, mb, nt;
-        unit_coords(u, t, ks, mb, nt);
-        uint8_t* st = stages + (i % C::NS) * C::STAGE;
-        int seg = 0;
-        while (seg + 1 < g.nseg && nt >= g.seg_tile0[seg + 1]) ++seg;
+      UnitWalk wc, ac;
+      wc.start(g, u0);
+      ac = wc;
+      auto issue_w = [&](int s, const UnitWalk& w) {
+        uint8_t* st = stages + s * C::STAGE;
         if (g.paired) {
-          int row = (nt - g.seg_tile0[seg]) * (kBM / 2);
-          tma_load_2d_hint(st, &wm.m[0], &full[i % C::NS], ks * kBK, row, pol);
-          tma_load_2d_hint(st + C::W_BYTES / 2, &wm.m[1], &full[i % C::NS], ks * kBK, row, pol);
+          tma_load_2d_hint(st, &wm.m[0], &full[s], w.ks * kBK, w.row, pol);
+          tma_load_2d_hint(st + C::W_BYTES / 2, &wm.m[1], &full[s], w.ks * kBK, w.row, pol);
         } else {
-          int row = (nt - g.seg_tile0[seg]) * kBM;
-          tma_load_2d_hint(st, &wm.m[seg], &full[i % C::NS], ks * kBK, row, pol);
+          tma_load_2d_hint(st, &wm.m[w.seg], &full[s], w.ks * kBK, w.row, pol);
         }
       };
-      auto issue_a = [&](int i, long long u) {
-        int t, ks, mb, nt;
-        unit_coords(u, t, ks, mb, nt);
-        uint8_t* st = stages + (i % C::NS) * C::STAGE + C::W_BYTES;
-        tma_load_2d(st, &tmA, &full[i % C::NS], ks * kBK, mb * BN);
+      auto issue_a = [&](int s, const UnitWalk& w) {
+        tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmA, &full[s], w.ks * kBK, w.mb * BN);
       };
       const int pre = min(C::NS, n_my);
       for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(&full[i], C::STAGE);
-        issue_w(i, u0 + i);
+        issue_w(i, wc);
+        wc.next(g);
       }
       pdl_wait();  // activations are written by the previous kernel
-      for (int i = 0; i < pre; ++i) issue_a(i, u0 + i);
+      for (int i = 0; i < pre; ++i) {
+        issue_a(i, ac);
+        ac.next(g);
+      }
       int issued = pre;
+      int s = pre % C::NS;
+      uint32_t par = (pre / C::NS) & 1;  // parity of this stage's current use
       for (int i = pre; i < n_my; ++i) {
-        if (!mbar_wait(&empty[i % C::NS], ((i / C::NS) - 1) & 1)) {
+        if (!mbar_wait(&empty[s], par ^ 1)) {
           raise_error(e.err, DFLASH_DEV_TIMEOUT);
           break;
         }
-        mbar_arrive_expect_tx(&full[i % C::NS], C::STAGE);
-        issue_w(i, u0 + i);
-        issue_a(i, u0 + i);
+        mbar_arrive_expect_tx(&full[s], C::STAGE);
+        issue_w(s, wc);
+        issue_a(s, ac);
+        wc.next(g);
+        ac.next(g);
         issued = i + 1;
+        if (++s == C::NS) { s = 0; par ^= 1; }
       }
       // never leave with copies in flight
       for (int i = max(0, issued - C::NS); i < issued; ++i) mbar_wait(&full[i % C::NS], (i / C::NS) & 1);

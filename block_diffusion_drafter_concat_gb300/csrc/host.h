@@ -8,7 +8,6 @@
 
 #include "attention.cuh"
 #include "gemm.cuh"
-#include "persist.cuh"
 
 namespace dflash {
 
@@ -75,10 +74,6 @@ dflash_status launch_attn_tc(int hd, int nw, dim3 grid, int smem, const AttnMaps
                              const AttnArgs<bf16>& a, cudaStream_t st);
 dflash_status launch_attn_f32(dim3 grid, int smem, const AttnArgs<float>& a, cudaStream_t st);
 dflash_status launch_attn_combine(int B, const AttnArgs<bf16>& a, cudaStream_t st);
-// tu_persist.cu: the persistent layer stack (grid 0 when it cannot be resident)
-int persist_max_grid(int sms);
-dflash_status launch_persist(int grid, const PersistMaps& maps, const PersistArgs& a,
-                             cudaStream_t st);
 dflash_status launch_attn_combine(int B, const AttnArgs<float>& a, cudaStream_t st);
 
 }  // namespace dflash

@@ -19,11 +19,11 @@ SMALL = {
     "small-bf16-hd64-g8": configs.small_bf16(
         name="small-bf16-hd64-g8", d_model=384, n_q_heads=16, n_kv_heads=2, head_dim=64,
         ffn_dim=384, vocab=2176, batch=3, ctx_range=(16, 120), seed=12),
-    # batch 1 x block 16 rows: the persistent layer-stack kernel (two and one splits)
-    "small-bf16-b1-persist": configs.small_bf16(
-        name="small-bf16-b1-persist", batch=1, ctx_range=(150, 200), seed=14),
-    "small-bf16-b1-persist-1split": configs.small_bf16(
-        name="small-bf16-b1-persist-1split", batch=1, ctx_range=(40, 100), seed=15),
+    # batch 1 x block 16 rows (the 16-row projection tiles), two and one context splits
+    "small-bf16-b1": configs.small_bf16(
+        name="small-bf16-b1", batch=1, ctx_range=(150, 200), seed=14),
+    "small-bf16-b1-1split": configs.small_bf16(
+        name="small-bf16-b1-1split", batch=1, ctx_range=(40, 100), seed=15),
     "small-bf16-b5-s8": configs.small_bf16(
         name="small-bf16-b5-s8", block_size=8, batch=5, n_q_heads=4, n_kv_heads=2,
         ctx_range=(8, 70), vocab=1000, seed=13),
@@ -69,7 +69,7 @@ def test_step_matches_oracle(built, name):
     assert checked >= 1
 
 
-@pytest.mark.parametrize("name", ["small-bf16-hd128", "small-bf16-b1-persist"])
+@pytest.mark.parametrize("name", ["small-bf16-hd128", "small-bf16-b1"])
 def test_step_is_deterministic_and_graph_replay_matches(built, name):
     from block_diffusion_drafter_concat_gb300.runner import StepRunner
     w = SMALL[name]
