@@ -59,11 +59,10 @@ __global__ void __launch_bounds__(256) k_attn_combine(const AttnArgs<T> a) {
   const int ns = (kp + a.pps - 1) / a.pps;
   const long long grp = (long long)b * a.hkv + g;
   const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + grp * a.nsplit * a.QR;
-  float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[(long long)s * a.QR + r].x);
-  float L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4* po = reinterpret_cast<const float4*>(a.part_o + grp * a.nsplit * a.QR * a.hd);
+  // one pass in split order with a running maximum (loads of 8 splits in flight)
+  float M = -INFINITY, L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s0 = 0; s0 < ns; s0 += 8) {
     float4 v[8];
     float2 q[8];
@@ -76,9 +75,14 @@ __global__ void __launch_bounds__(256) k_attn_combine(const AttnArgs<T> a) {
 #pragma unroll
     for (int j = 0; j < 8; ++j)
       if (s0 + j < ns) {
-        const float w = exp2f(q[j].x - M);
-        L += w * q[j].y;
-        acc.x += w * v[j].x; acc.y += w * v[j].y; acc.z += w * v[j].z; acc.w += w * v[j].w;
+        const float nm = fmaxf(M, q[j].x);
+        const float al = exp2f(M - nm), w = exp2f(q[j].x - nm);
+        M = nm;
+        L = L * al + w * q[j].y;
+        acc.x = acc.x * al + w * v[j].x;
+        acc.y = acc.y * al + w * v[j].y;
+        acc.z = acc.z * al + w * v[j].z;
+        acc.w = acc.w * al + w * v[j].w;
       }
   }
   const float inv = 1.f / L;
@@ -156,41 +160,55 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   __syncthreads();
 
   if (warp == NW) {
-    if (lane == 0) {
-      int issued = 0;
-      for (int i = 0; i < nmy; ++i) {
-        const int s = i % C::NS;
-        if (i >= C::NS && !mbar_wait(&empty[s], ((i / C::NS) - 1) & 1)) {
-          raise_error(a.err, DFLASH_DEV_TIMEOUT);
-          break;
-        }
-        mbar_arrive_expect_tx(&full[s], C::STAGE);
-        uint8_t* kd = stages + s * C::STAGE;
-        uint8_t* vd = kd + C::TILE;
-        const int pg = p0 + i;
-        const CUtensorMap *mk, *mv;
-        int row;
-        if (pg < np) {
-          int page = a.page_table[(long long)b * a.max_pages + pg];
-          if (page < 0 || page >= a.num_pages) {
-            raise_error(a.err, DFLASH_DEV_BAD_INDEX);
-            page = 0;
-          }
-          mk = &maps.k; mv = &maps.v;
-          row = (page * a.hkv + g) * kPage;
-        } else {
-          mk = &maps.kb; mv = &maps.vb;
-          row = (b * a.hkv + g) * a.S;
-        }
+    // The page ids of this split are read 32 at a time by the whole warp (one round
+    // trip) and handed to lane 0, which issues the TMA copies.
+    int issued = 0;
+    bool ok = true;
+    for (int base = 0; base < nmy && ok; base += 32) {
+      int my_page = 0;
+      const int pgl = p0 + base + lane;
+      if (base + lane < nmy && pgl < np) my_page = a.page_table[(long long)b * a.max_pages + pgl];
+      const int cnt = min(32, nmy - base);
+      for (int j = 0; j < cnt; ++j) {
+        const int page_j = __shfl_sync(0xffffffffu, my_page, j);
+        if (lane == 0 && ok) {
+          const int i = base + j;
+          const int s = i % C::NS;
+          if (i >= C::NS && !mbar_wait(&empty[s], ((i / C::NS) - 1) & 1)) {
+            raise_error(a.err, DFLASH_DEV_TIMEOUT);
+            ok = false;
+          } else {
+            mbar_arrive_expect_tx(&full[s], C::STAGE);
+            uint8_t* kd = stages + s * C::STAGE;
+            uint8_t* vd = kd + C::TILE;
+            const int pg = p0 + i;
+            const CUtensorMap *mk, *mv;
+            int row;
+            if (pg < np) {
+              int page = page_j;
+              if (page < 0 || page >= a.num_pages) {
+                raise_error(a.err, DFLASH_DEV_BAD_INDEX);
+                page = 0;
+              }
+              mk = &maps.k; mv = &maps.v;
+              row = (page * a.hkv + g) * kPage;
+            } else {
+              mk = &maps.kb; mv = &maps.vb;
+              row = (b * a.hkv + g) * a.S;
+            }
 #pragma unroll
-        for (int bx = 0; bx < HD / 64; ++bx) {
-          tma_load_2d(kd + bx * 2048, mk, &full[s], bx * 64, row);
-          tma_load_2d(vd + bx * 2048, mv, &full[s], bx * 64, row);
+            for (int bx = 0; bx < HD / 64; ++bx) {
+              tma_load_2d(kd + bx * 2048, mk, &full[s], bx * 64, row);
+              tma_load_2d(vd + bx * 2048, mv, &full[s], bx * 64, row);
+            }
+            issued = i + 1;
+          }
         }
-        issued = i + 1;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
-      for (int i = max(0, issued - C::NS); i < issued; ++i) mbar_wait(&full[i % C::NS], (i / C::NS) & 1);
     }
+    if (lane == 0)
+      for (int i = max(0, issued - C::NS); i < issued; ++i) mbar_wait(&full[i % C::NS], (i / C::NS) & 1);
   } else {
     // ------------------------------------------------------------------ consumers
     const int g8 = lane >> 2, t4 = lane & 3, mi = lane >> 3, r8 = lane & 7;

@@ -243,14 +243,26 @@ __device__ __forceinline__ void cta_range(long long units, int c, int grid, long
 // Contributors of tile t (units [t*ks, (t+1)*ks)): the CTAs whose non-empty unit range
 // intersects it, in CTA order.  Writes each one's partial slot (cta*2 + 0 when its range
 // starts inside the tile, + 1 when the tile is the last piece of its range) to `slots`
-// when given, and returns how many there are.
+// when given, and returns how many there are.  With at least one unit per CTA the
+// contributors are the consecutive CTAs [c_lo, c_hi] found with two divisions (this
+// runs on the tail of every split tile, so it must stay cheap).
 __device__ __forceinline__ int tile_contributors(long long units, int grid, int ks, int t,
                                                  int* slots) {
   const long long ts = static_cast<long long>(t) * ks, te = ts + ks;
-  int n = 0;
-  for (int c = static_cast<int>((ts * grid) / units); c < grid; ++c) {
+  // CTA c owns [units*c/grid, units*(c+1)/grid): c_lo is the last CTA starting at or
+  // before ts, c_hi the last starting before te
+  const int c_lo = static_cast<int>(((ts + 1) * grid + units - 1) / units) - 1;
+  const int c_hi = static_cast<int>((te * grid + units - 1) / units) - 1;
+  if (units >= grid) {
+    if (slots) {
+      slots[0] = c_lo * 2 + ((units * c_lo / grid == ts) ? 0 : 1);
+      for (int c = c_lo + 1; c <= c_hi; ++c) slots[c - c_lo] = c * 2;
+    }
+    return c_hi - c_lo + 1;
+  }
+  int n = 0;  // fewer units than CTAs: skip the CTAs with empty ranges
+  for (int c = c_lo; c <= c_hi; ++c) {
     const long long s0 = units * c / grid, s1 = units * (c + 1) / grid;
-    if (s0 >= te) break;
     if (s1 <= ts || s0 == s1) continue;
     if (slots) slots[n] = c * 2 + ((s0 / ks == t) ? 0 : 1);
     ++n;
@@ -448,10 +460,10 @@ __global__ void __launch_bounds__(160, 1)
         const int r = x / (kBM / 4), c4 = x % (kBM / 4);
         reinterpret_cast<float4*>(dst)[x] = *reinterpret_cast<const float4*>(Cs + r * C::PITCH + c4 * 4);
       }
-      const int nc = tile_contributors(g.units, grid, g.ks, t, nullptr);
       __threadfence();
       consumer_sync();
       if (tid == 0) {
+        const int nc = tile_contributors(g.units, grid, g.ks, t, nullptr);
         int prev = atomicAdd(&g.counters[t], 1);
         int last = (prev == nc - 1);
         if (last) { atomicExch(&g.counters[t], 0); __threadfence(); }
@@ -461,8 +473,9 @@ __global__ void __launch_bounds__(160, 1)
       mine = *flag != 0;
       if (mine) {
         // partial slots of the contributors, in contributor order
-        if (tid == 0) tile_contributors(g.units, grid, g.ks, t, cslot);
+        if (tid == 0) flag[1] = tile_contributors(g.units, grid, g.ks, t, cslot);
         consumer_sync();
+        const int nc = flag[1];
         // sum the published partials in contributor order; loads of up to four
         // contributors are in flight together
         for (int x = tid; x < BN * kBM / 4; x += 128) {

@@ -32,6 +32,17 @@ __global__ void __launch_bounds__(kRowThreads)
               int max_position, int* __restrict__ pos, int* err) {
   __shared__ float red[kRowThreads / 32];
   pdl_launch_dependents();
+  // the gains are weights (never written on the device): fetch them before the wait
+  float gv[32];
+  const bool regs = (sizeof(Tin) == 4) && (d & 3) == 0 && d <= kRowThreads * 4 * 8 && !ids;
+  if (regs) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int c = (k * kRowThreads + threadIdx.x) * 4;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) gv[k * 4 + q] = c + q < d ? to_f32<T>(gain[c + q]) : 0.f;
+    }
+  }
   pdl_wait();
   const int m = blockIdx.x;
   const Tin* src = xin + (long long)m * d;
@@ -61,7 +72,7 @@ __global__ void __launch_bounds__(kRowThreads)
     return;
   }
   if constexpr (sizeof(Tin) == 4) {
-    if ((d & 3) == 0 && d <= kRowThreads * 4 * 8) {
+    if (regs) {
       // the row stays in registers: up to 8 float4 per thread, all loads in flight
       float4 v[8];
       float ss = 0.f;
@@ -79,10 +90,10 @@ __global__ void __launch_bounds__(kRowThreads)
         const int c = (k * kRowThreads + threadIdx.x) * 4;
         if (c < d) {
           T* o = y + (long long)m * d + c;
-          o[0] = from_f32<T>(v[k].x * rs * to_f32<T>(gain[c]));
-          o[1] = from_f32<T>(v[k].y * rs * to_f32<T>(gain[c + 1]));
-          o[2] = from_f32<T>(v[k].z * rs * to_f32<T>(gain[c + 2]));
-          o[3] = from_f32<T>(v[k].w * rs * to_f32<T>(gain[c + 3]));
+          o[0] = from_f32<T>(v[k].x * rs * gv[k * 4]);
+          o[1] = from_f32<T>(v[k].y * rs * gv[k * 4 + 1]);
+          o[2] = from_f32<T>(v[k].z * rs * gv[k * 4 + 2]);
+          o[3] = from_f32<T>(v[k].w * rs * gv[k * 4 + 3]);
         }
       }
       return;
