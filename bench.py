@@ -297,7 +297,9 @@ def run_ours(args):
                           "frac": t_roof / (ms / 1e3), "peak_gbs": hbm, "peak_src": src},
         "roofline": {"kernel": "k_gemm_tc<16,EPI_ARGMAX> + k_argmax_finalize (LM head)",
                      "bound": "hbm", "achieved": lm_gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": lm_gbs / hbm, "traffic": LM_HEAD_TRAFFIC, "peak_src": src,
+                     "frac": lm_gbs / hbm,
+                     "traffic": LM_HEAD_TRAFFIC if w.name == DEFAULT_CONFIG else None,
+                     "peak_src": src,
                      "us_per_launch": t_lm * 1e6},
         "e2e": {"value": world * k_e2e / te, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
