@@ -28,8 +28,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "draft+verify steps/sec and tokens/sec; achieved HBM GB/s vs ~8 TB/s (1 GB300)"
 DEFAULT_CONFIG = "qwen3-8b-shaped-b1"
-# ncu summary of the LM-head kernel on this workload: DRAM bytes per launch, or None
-LM_HEAD_TRAFFIC = 1251274432  # dram read + write bytes of one launch (ncu)
+# DRAM read + write bytes of one LM-head launch on this workload, from an ncu capture of
+# the current kernel (None until the kernel has been captured since its last change)
+LM_HEAD_TRAFFIC = None
 
 
 def parse():
@@ -169,32 +170,27 @@ def run_ours(args):
     import torch.distributed as dist
 
     from block_diffusion_drafter_concat_gb300 import build
+    from block_diffusion_drafter_concat_gb300 import replicas
     from workload.configs import BY_NAME
 
     build.build()
     from block_diffusion_drafter_concat_gb300.runner import (StepRunner, lm_head_bytes,
                                                             step_bytes, step_flops)
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rep = replicas.from_env()
+    world, rank, local = rep.world, rep.rank, rep.local
     torch.cuda.set_device(local)
-    if world > 1:
+    if rep.distributed:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     def barrier():
-        if world > 1:
-            dist.barrier()
+        replicas.barrier(rep)
 
     def max_over_ranks(t):
-        if world == 1:
-            return t
-        tt = torch.tensor([t], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        return float(tt)
+        return replicas.max_over_ranks(rep, t, device="cuda")
 
     w = BY_NAME[args.config]
-    r = StepRunner(w)
+    r = StepRunner(replicas.shard(w, rank))
     # one eager step, then plant the verify logits' agreement with this step's drafts
     r.step()
     torch.cuda.synchronize()
@@ -228,7 +224,7 @@ def run_ours(args):
     barrier()
     t = max_over_ranks(ev[0].elapsed_time(ev[1]) / 1e3)
     mean_emit = float(r.n_emit.float().mean())
-    value = world * args.steps / t
+    value = replicas.aggregate(args.steps, rep, t)
     ms = t / args.steps * 1e3
 
     # ---- end to end through the public API: pinned host inputs in, results out
@@ -301,7 +297,7 @@ def run_ours(args):
                      "traffic": LM_HEAD_TRAFFIC if w.name == DEFAULT_CONFIG else None,
                      "peak_src": src,
                      "us_per_launch": t_lm * 1e6},
-        "e2e": {"value": world * k_e2e / te, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": replicas.aggregate(k_e2e, rep, te), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": r.launches * args.steps,
         "launches_per_step": r.launches,
@@ -316,7 +312,7 @@ def run_ours(args):
                       "prepared untimed; scaled to whole steps"}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if world > 1:
+    if rep.distributed:
         dist.destroy_process_group()
 
 
