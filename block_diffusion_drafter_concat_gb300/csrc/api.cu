@@ -134,7 +134,10 @@ struct WSet {
   }
 };
 
-int pick_bn(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
+// Activation rows per tile: up to 64 rows the projections stream weights past an
+// mma.sync tile; beyond that they are dense contractions for the tcgen05 kernel.
+int pick_bn(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256; }
+bool umma_bn(int bn) { return bn >= 128; }
 
 GemmShape plan_shape(const H* h, const WSet& w, int M, int K, bool tc, int* grid_out) {
   GemmShape g = {};
@@ -151,18 +154,61 @@ GemmShape plan_shape(const H* h, const WSet& w, int M, int K, bool tc, int* grid
   g.seg_tile0[w.nseg] = t;
   if (w.paired) g.seg_tile0[1] = t;  // both halves of every tile come from segment 0's range
   g.n_tiles = t;
-  const int bn = tc ? pick_bn(M) : kF32BN;
-  g.m_blocks = ceil_div(M, bn);
   g.ks = ceil_div(K, kBK);
-  g.units = (long long)g.m_blocks * g.n_tiles * g.ks;
-  // at least 4 units per CTA, and few enough CTAs per tile for the reducer's table
+  // stream-K: at least 4 units per CTA, and few enough CTAs per tile for the table of
+  // the tile's finisher
   const long long per = std::max<long long>(4, (g.ks + 509) / 510);
-  int grid = static_cast<int>(std::min<long long>(h->sms, (g.units + per - 1) / per));
+  auto streamk_grid = [&](long long units) {
+    return static_cast<int>(std::min<long long>(h->sms, (units + per - 1) / per));
+  };
+  int bn = tc ? pick_bn(M) : kF32BN;
+  int grid = 0;
+  if (tc && umma_bn(bn)) {
+    // tcgen05 tiles of 128 or 256 rows, as whole tiles per CTA (waves of tiles) or as
+    // stream-K ranges (every SM busy, split tiles finished by their last contributor):
+    // the cheaper by a model of times measured on GB300: a k-stage of a 256-row tile
+    // ~0.46 us, of a 128-row tile ~0.53 us (both bound by operand delivery, not the
+    // MMA), and ~40 us to finish split tiles through the partial buffers.
+    constexpr double kStage128 = 0.53, kStage256 = 0.46, kFinish = 40.0;
+    double best = 1e30;
+    for (int cand : {128, 256}) {
+      if (cand == 256 && M <= 128) continue;
+      const long long tiles = (long long)ceil_div(M, cand) * g.n_tiles;
+      // with many tiles per CTA, stream-K balances to the unit and finishes only a
+      // handful of split tiles off the critical path
+      const bool many = tiles >= 4LL * h->sms;
+      const double st = cand == 256 ? kStage256 : kStage128;
+      const long long waves = (tiles + h->sms - 1) / h->sms;
+      const double t_tile = (double)waves * g.ks * st;
+      const int gs = streamk_grid(tiles * g.ks);
+      const bool splits = (tiles * g.ks) % gs != 0 || (tiles * g.ks / gs) % g.ks != 0;
+      const double t_sk = (double)((tiles * g.ks + gs - 1) / gs) * st + (splits ? kFinish : 0.0);
+      if (!many && t_tile <= best) {
+        best = t_tile;
+        bn = cand;
+        g.tile_mode = 1;
+        grid = static_cast<int>((tiles + waves - 1) / waves);
+      }
+      if (t_sk < best) {
+        best = t_sk;
+        bn = cand;
+        g.tile_mode = 0;
+        grid = gs;
+      }
+    }
+  }
+  g.bn = bn;
+  g.m_blocks = ceil_div(M, bn);
+  g.units = (long long)g.m_blocks * g.n_tiles * g.ks;
+  if (grid == 0) grid = streamk_grid(g.units);
   *grid_out = std::max(1, grid);
   return g;
 }
 
-size_t gemm_part_floats(const H* h) { return (size_t)h->sms * 2 * 128 * kBM; }
+// split-tile partials: two slots per CTA of tiles with up to max_rows activation rows
+size_t gemm_part_floats(const H* h, int max_rows) {
+  return (size_t)h->sms * 2 * pick_bn(std::max(1, max_rows)) * kBM;
+}
 
 // Runs one projection: y = A W^T over the weight segments of `w`, epilogue EPI.
 template <int EPI, typename T>
@@ -176,15 +222,18 @@ dflash_status gemm(const H* h, const void* A, int M, int K, const WSet& w, EpiAr
   g.counters = ctr;
   e.M = M;
   if (EPI == EPI_F32 || EPI == EPI_RESID || EPI == EPI_ARGMAX) e.N = w.rows[0];
-  if (g.m_blocks * g.n_tiles > kCtlWords)
+  // one control word per tile (two on the tcgen05 path: arrivals and publications)
+  const int ctl_per_tile = (tc && umma_bn(g.bn)) ? 2 : 1;
+  if (g.m_blocks * g.n_tiles * ctl_per_tile > kCtlWords)
     return fail(DFLASH_EUNSUPPORTED, "GEMM with %d tiles exceeds the control words",
                 g.m_blocks * g.n_tiles);
   if constexpr (std::is_same<T, bf16>::value) {
     CUtensorMap tmA;
-    const int bn = pick_bn(M);
+    const int bn = g.bn;
     TRY(encode_bf16(&tmA, A, M, K, K, bn));
     WMaps wm;
     for (int s = 0; s < w.nseg; ++s) wm.m[s] = *w.maps[s];
+    if (umma_bn(bn)) return launch_gemm_umma(bn, EPI, tmA, wm, g, grid, e, st);
     if (bn <= 32) return launch_gemm_tc_lo(bn, EPI, tmA, wm, g, grid, e, st);
     return launch_gemm_tc_hi(bn, EPI, tmA, wm, g, grid, e, st);
   } else {
@@ -249,7 +298,7 @@ DraftWs carve_draft(const H* h, Carve& cv, int B, int max_pages) {
   w.act = cv.take<char>(M * c.ffn_dim * elt(h));
   w.part_o = cv.take<float>((size_t)B * c.n_kv_heads * ap.nsplit * QR * c.head_dim);
   w.part_ml = cv.take<float>((size_t)B * c.n_kv_heads * ap.nsplit * QR * 2);
-  w.gpart = cv.take<float>(gemm_part_floats(h));
+  w.gpart = cv.take<float>(gemm_part_floats(h, static_cast<int>(M)));
   return w;
 }
 
@@ -265,7 +314,7 @@ InjectWs carve_inject(const H* h, Carve& cv, int n) {
   w.ctl = cv.take<int>(kCtlWords);
   w.u = cv.take<float>((size_t)n * h->c.d_model);
   w.fused = cv.take<char>((size_t)n * h->c.d_model * elt(h));
-  w.gpart = cv.take<float>(gemm_part_floats(h));
+  w.gpart = cv.take<float>(gemm_part_floats(h, n));
   return w;
 }
 
@@ -283,7 +332,7 @@ HeadWs carve_head(const H* h, Carve& cv, int rows) {
   w.am_max = cv.take<float>(t);
   w.am_sum = cv.take<float>(t);
   w.am_idx = cv.take<int>(t);
-  w.gpart = cv.take<float>(gemm_part_floats(h));
+  w.gpart = cv.take<float>(gemm_part_floats(h, rows));
   return w;
 }
 
@@ -320,7 +369,7 @@ VerifyWs carve_verify(const H* h, Carve& cv, int B, bool sample) {
     w.rej = cv.take<int>(B);
     w.hrow = cv.take<char>((size_t)B * h->c.d_model * elt(h));
     w.zr = cv.take<float>((size_t)B * h->c.vocab);
-    w.gpart = cv.take<float>(gemm_part_floats(h));
+    w.gpart = cv.take<float>(gemm_part_floats(h, B));
   }
   return w;
 }
@@ -544,6 +593,8 @@ dflash_status dflash_create(const dflash_config* cfg, const dflash_weights* w,
   if (c.page_size != kPage) return fail(DFLASH_EUNSUPPORTED, "page_size must be 16");
   if (c.n_q_heads % c.n_kv_heads) return fail(DFLASH_EINVAL, "n_q_heads %% n_kv_heads != 0");
   if (c.head_dim % 2) return fail(DFLASH_EINVAL, "head_dim must be even");
+  // the rotary pairs of a head are finished inside one 128-column projection tile
+  if (kBM % c.head_dim) return fail(DFLASH_EUNSUPPORTED, "head_dim must divide 128");
   if (!(c.rope_theta > 0.f) || !(c.rms_eps >= 0.f)) return fail(DFLASH_EINVAL, "bad theta/eps");
   if (c.dtype != DFLASH_BF16 && c.dtype != DFLASH_F32) return fail(DFLASH_EINVAL, "bad dtype");
   const int QR = c.block_size * (c.n_q_heads / c.n_kv_heads);

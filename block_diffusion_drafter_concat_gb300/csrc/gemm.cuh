@@ -67,16 +67,31 @@ struct EpiArgs {
 
 struct GemmShape {
   int M, K, n_tiles, ks, m_blocks, paired, nseg;
+  int bn;          // activation rows per tile
+  int tile_mode;   // 1: CTAs take whole tiles (no split); 0: stream-K unit ranges
   long long units;
   int seg_tile0[kMaxSeg + 1];
   int seg_rows[kMaxSeg];  // rows of each weight matrix
-  float* part;      // [grid][2][BN][kBM] partial tiles
+  float* part;      // [grid][2][BN * kBM] partial tiles (split pieces)
   int* counters;    // one per output tile
 };
 
 // ---------------------------------------------------------------------------- epilogue
 // Cs: the finished fp32 tile, Cs[r * pitch + c] for activation row m0 + r and output
-// column c of n-tile nt.  Runs on `nthr` threads (thread index `tid`).
+// column c of n-tile nt.  Runs on `nthr` threads (thread index `tid`, whole warps).
+// Each warp takes whole rows (r = warp, warp + nw, ...) and its lanes the columns, so
+// the integer work of a row (sequence, slot, position) is done once per row, every
+// global access of a warp is contiguous, and the loads of four rows are issued before
+// the first of their stores.
+template <typename T>
+__device__ __forceinline__ void store_pair(T* p, float a, float b) {
+  if constexpr (sizeof(T) == 2) {
+    *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
+  } else {
+    *reinterpret_cast<float2*>(p) = make_float2(a, b);
+  }
+}
+
 template <typename T, int EPI>
 __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt,
                               const GemmShape& g, const EpiArgs<T>& e, int tid, int nthr) {
@@ -85,41 +100,59 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
   const int rows_per_tile = g.paired ? kBM / 2 : kBM;
   const int r0 = (nt - g.seg_tile0[seg]) * rows_per_tile;  // first row within the segment
   const int mr = min(BN, e.M - m0);
+  const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
+  constexpr int RB = 4;  // rows per batch of a warp
 
   if constexpr (EPI == EPI_F32 || EPI == EPI_RESID) {
     const int nc = min(kBM, e.N - nt * kBM);
     if (nc == kBM && (e.ldy & 3) == 0 && (pitch & 3) == 0) {
-      // full tile: float4 accesses, four in flight per thread
-#pragma unroll 4
-      for (int i = tid; i < mr * (kBM / 4); i += nthr) {
-        const int r = i / (kBM / 4), c4 = i % (kBM / 4);
-        float4 v = *reinterpret_cast<const float4*>(Cs + r * pitch + c4 * 4);
-        float4* dst = reinterpret_cast<float4*>(e.y + (long long)(m0 + r) * e.ldy + nt * kBM) + c4;
+      // lane -> columns 4*lane .. 4*lane+3
+      for (int rb = warp; rb < mr; rb += nw * RB) {
+        float4 o[RB];
         if constexpr (EPI == EPI_RESID) {
-          float4 o = *dst;
-          v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+#pragma unroll
+          for (int k = 0; k < RB; ++k) {
+            const int r = rb + k * nw;
+            if (r < mr)
+              o[k] = reinterpret_cast<const float4*>(e.y + (long long)(m0 + r) * e.ldy + nt * kBM)[lane];
+          }
         }
-        *dst = v;
+#pragma unroll
+        for (int k = 0; k < RB; ++k) {
+          const int r = rb + k * nw;
+          if (r >= mr) continue;
+          float4 v = *reinterpret_cast<const float4*>(Cs + r * pitch + lane * 4);
+          if constexpr (EPI == EPI_RESID) {
+            v.x += o[k].x; v.y += o[k].y; v.z += o[k].z; v.w += o[k].w;
+          }
+          reinterpret_cast<float4*>(e.y + (long long)(m0 + r) * e.ldy + nt * kBM)[lane] = v;
+        }
       }
     } else {
-#pragma unroll 4
-      for (int i = tid; i < mr * kBM; i += nthr) {
-        int r = i / kBM, c = i % kBM;
-        if (c >= nc) continue;
-        float v = Cs[r * pitch + c];
-        float* dst = e.y + (long long)(m0 + r) * e.ldy + nt * kBM + c;
-        if constexpr (EPI == EPI_RESID) *dst += v; else *dst = v;
+      for (int r = warp; r < mr; r += nw) {
+        float* yr = e.y + (long long)(m0 + r) * e.ldy + nt * kBM;
+        for (int c = lane; c < nc; c += 32) {
+          const float v = Cs[r * pitch + c];
+          if constexpr (EPI == EPI_RESID) yr[c] += v; else yr[c] = v;
+        }
       }
     }
   } else if constexpr (EPI == EPI_SWIGLU) {
-#pragma unroll 4
-    for (int i = tid; i < mr * 64; i += nthr) {
-      int r = i / 64, c = i % 64;
-      int f = r0 + c;
-      if (f >= e.F) continue;
-      float gt = Cs[r * pitch + c], up = Cs[r * pitch + 64 + c];
-      float s = gt / (1.0f + __expf(-gt));
-      e.act[(long long)(m0 + r) * e.F + f] = from_f32<T>(s * up);
+    // 64 gate columns and the 64 matching up columns; lane -> columns 2*lane, 2*lane+1
+    const int f = r0 + 2 * lane;
+    const bool pair_ok = ((e.F & 1) == 0) && f + 1 < e.F;
+    for (int r = warp; r < mr; r += nw) {
+      T* ar = e.act + (long long)(m0 + r) * e.F;
+      const float2 gt = *reinterpret_cast<const float2*>(Cs + r * pitch + 2 * lane);
+      const float2 up = *reinterpret_cast<const float2*>(Cs + r * pitch + 64 + 2 * lane);
+      const float a0 = gt.x / (1.0f + __expf(-gt.x)) * up.x;
+      const float a1 = gt.y / (1.0f + __expf(-gt.y)) * up.y;
+      if (pair_ok) {
+        store_pair<T>(ar + f, a0, a1);
+      } else {
+        if (f < e.F) ar[f] = from_f32<T>(a0);
+        if (f + 1 < e.F) ar[f + 1] = from_f32<T>(a1);
+      }
     }
   } else if constexpr (EPI == EPI_QKV || EPI == EPI_KV) {
     const int hd = e.hd, half = hd >> 1;
@@ -128,68 +161,134 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
     if constexpr (EPI == EPI_QKV) kind = seg;
     else { layer = seg >> 1; kind = 1 + (seg & 1); }
     const int G = e.hq / e.hkv;
+    const int nheads = (kind == 0) ? e.hq : e.hkv;
     if (kind == 2) {
-#pragma unroll 4
-      for (int i = tid; i < mr * kBM; i += nthr) {
-        int r = i / kBM, c = i % kBM;
-        int f = r0 + c, m = m0 + r;
-        int head = f / hd, j = f % hd;
-        if (head >= e.hkv) continue;
-        T v = from_f32<T>(Cs[r * pitch + c]);
-        if constexpr (EPI == EPI_QKV) {
-          int b = m / e.S, ii = m % e.S;
-          e.vb[(((long long)b * e.hkv + head) * e.S + ii) * hd + j] = v;
-        } else {
-          int slot = e.slots[m];
-          if (slot < 0 || slot >= e.num_slots) { raise_error(e.err, DFLASH_DEV_BAD_INDEX); continue; }
-          long long page = slot / kPage, off = slot % kPage;
-          e.vpool[layer][((page * e.hkv + head) * kPage + off) * hd + j] = v;
+      // lane -> columns 2*lane + 64*k (k = 0, 1): head and offset fixed per lane
+      int hv[2], jv[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int f = r0 + 2 * lane + 64 * k;
+        hv[k] = f / hd;
+        jv[k] = f - hv[k] * hd;
+      }
+      for (int rb = warp; rb < mr; rb += nw * RB) {
+        long long rbase[RB];
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+          const int r = rb + q * nw;
+          rbase[q] = -1;
+          if (r >= mr) continue;
+          const int m = m0 + r;
+          if constexpr (EPI == EPI_QKV) {
+            const int b = m / e.S, ii = m - (m / e.S) * e.S;
+            rbase[q] = ((long long)b * e.hkv * e.S + ii) * hd;   // + head * S * hd
+          } else {
+            const int slot = e.slots[m];
+            if (slot < 0 || slot >= e.num_slots) { raise_error(e.err, DFLASH_DEV_BAD_INDEX); continue; }
+            rbase[q] = ((long long)(slot / kPage) * e.hkv * kPage + slot % kPage) * hd;  // + head*16*hd
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+          const int r = rb + q * nw;
+          if (r >= mr || rbase[q] < 0) continue;
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            if (hv[k] >= e.hkv) continue;
+            const float2 v = *reinterpret_cast<const float2*>(Cs + r * pitch + 2 * lane + 64 * k);
+            if constexpr (EPI == EPI_QKV) {
+              store_pair<T>(e.vb + rbase[q] + (long long)hv[k] * e.S * hd + jv[k], v.x, v.y);
+            } else {
+              store_pair<T>(e.vpool[layer] + rbase[q] + (long long)hv[k] * kPage * hd + jv[k], v.x, v.y);
+            }
+          }
         }
       }
     } else {
-      // rotary pairs (j, j + hd/2) of one head lie in the same 128-column tile; the
-      // loop is unrolled so that the position and table loads of several pairs overlap
-#pragma unroll 8
-      for (int i = tid; i < mr * (kBM / 2); i += nthr) {
-        int r = i / (kBM / 2), cc = i % (kBM / 2);
-        int hl = cc / half, j = cc % half;
-        int c = hl * hd + j;
-        int f = r0 + c, m = m0 + r;
-        int head = f / hd;
-        int nheads = (kind == 0) ? e.hq : e.hkv;
-        if (head >= nheads) continue;
-        int p = e.pos[m];
-        if (p < 0 || p >= e.max_pos) { raise_error(e.err, DFLASH_DEV_BAD_POSITION); continue; }
-        float2 cs = e.rope[(long long)p * half + j];
-        float x0 = Cs[r * pitch + c], x1 = Cs[r * pitch + c + half];
-        T y0 = from_f32<T>(x0 * cs.x - x1 * cs.y);
-        T y1 = from_f32<T>(x1 * cs.x + x0 * cs.y);
-        long long base;
-        if constexpr (EPI == EPI_QKV) {
-          int b = m / e.S, ii = m % e.S;
-          if (kind == 0) {
-            int gk = head / G, hh = head % G;
-            base = ((((long long)b * e.hkv + gk) * e.S + ii) * G + hh) * hd;
-            e.q[base + j] = y0;
-            e.q[base + j + half] = y1;
-          } else {
-            base = (((long long)b * e.hkv + head) * e.S + ii) * hd;
-            e.kb[base + j] = y0;
-            e.kb[base + j + half] = y1;
+      // rotary pairs (j, j + hd/2) of one head lie in the same 128-column tile; lane ->
+      // pair indices lane and lane + 32 of the tile's 64 pairs
+      int cv[2], hv[2], jv[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int cc = lane + 32 * k;
+        const int hl = cc / half;
+        jv[k] = cc - hl * half;
+        cv[k] = hl * hd + jv[k];
+        hv[k] = (r0 + cv[k]) / hd;
+      }
+      // rows in batches of 8 per warp: lane q < 8 fetches row q's position (and cache
+      // slot), shuffles broadcast them, then the 16 rotary-table loads of the batch go
+      // out together: two dependent round trips per 8 rows
+      constexpr int RR = 8;
+      for (int rb = warp; rb < mr; rb += nw * RR) {
+        int my_p = -1;
+        long long my_base = 0;
+        if (lane < RR) {
+          const int r = rb + lane * nw;
+          if (r < mr) {
+            const int m = m0 + r;
+            const int p = e.pos[m];
+            bool ok = p >= 0 && p < e.max_pos;
+            if (!ok) raise_error(e.err, DFLASH_DEV_BAD_POSITION);
+            if constexpr (EPI == EPI_QKV) {
+              const int b = m / e.S, ii = m - (m / e.S) * e.S;
+              my_base = kind == 0 ? (((long long)b * e.hkv * e.S + ii) * G) * hd   // + (gk*S*G + hh)*hd
+                                  : ((long long)b * e.hkv * e.S + ii) * hd;        // + head*S*hd
+            } else {
+              const int slot = e.slots[m];
+              if (slot < 0 || slot >= e.num_slots) {
+                raise_error(e.err, DFLASH_DEV_BAD_INDEX);
+                ok = false;
+              } else {
+                my_base = ((long long)(slot / kPage) * e.hkv * kPage + slot % kPage) * hd;
+              }
+            }
+            if (ok) my_p = p;
           }
-        } else {
-          int slot = e.slots[m];
-          if (slot < 0 || slot >= e.num_slots) { raise_error(e.err, DFLASH_DEV_BAD_INDEX); continue; }
-          long long page = slot / kPage, off = slot % kPage;
-          base = ((page * e.hkv + head) * kPage + off) * hd;
-          e.kpool[layer][base + j] = y0;
-          e.kpool[layer][base + j + half] = y1;
+        }
+        int pv[RR];
+        long long rbase[RR];
+#pragma unroll
+        for (int q = 0; q < RR; ++q) {
+          pv[q] = __shfl_sync(0xffffffffu, my_p, q);
+          rbase[q] = __shfl_sync(0xffffffffu, my_base, q);
+        }
+        float2 cs[RR][2];
+#pragma unroll
+        for (int q = 0; q < RR; ++q)
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            cs[q][k] = pv[q] >= 0 ? e.rope[(long long)pv[q] * half + jv[k]] : make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < RR; ++q) {
+          const int r = rb + q * nw;
+          if (pv[q] < 0) continue;   // past the chunk, or reported above
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int head = hv[k];
+            if (head >= nheads) continue;
+            const float x0 = Cs[r * pitch + cv[k]], x1 = Cs[r * pitch + cv[k] + half];
+            const T y0 = from_f32<T>(x0 * cs[q][k].x - x1 * cs[q][k].y);
+            const T y1 = from_f32<T>(x1 * cs[q][k].x + x0 * cs[q][k].y);
+            T* dst;
+            if constexpr (EPI == EPI_QKV) {
+              if (kind == 0) {
+                const int gk = head / G, hh = head - gk * G;
+                dst = e.q + rbase[q] + ((long long)gk * e.S * G + hh) * hd;
+              } else {
+                dst = e.kb + rbase[q] + (long long)head * e.S * hd;
+              }
+            } else {
+              dst = e.kpool[layer] + rbase[q] + (long long)head * kPage * hd;
+            }
+            dst[jv[k]] = y0;
+            dst[jv[k] + half] = y1;
+          }
         }
       }
     }
   } else if constexpr (EPI == EPI_ARGMAX) {
     // one warp per row: lanes cover the 128 columns, then a (max, idx) shuffle reduce
-    const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
     const int nc = min(kBM, e.N - nt * kBM);
     for (int r = warp; r < mr; r += nw) {
       float best = -INFINITY;

@@ -60,7 +60,7 @@ dflash_status launch_tc(const CUtensorMap& tmA, const WMaps& wm, const GemmShape
                 tmA, wm, g, e);
 }
 
-// tu_gemm_a.cu: BN 16 and 32; tu_gemm_b.cu: BN 64 and 128 and the fp32 kernels;
+// tu_gemm_a.cu: BN 16 and 32; tu_gemm_b.cu: BN 64 and the fp32 kernels;
 // tu_attn.cu: attention.
 dflash_status launch_gemm_tc_lo(int bn, int epi, const CUtensorMap& tmA, const WMaps& wm,
                                 const GemmShape& g, int grid, const EpiArgs<bf16>& e,
@@ -68,6 +68,10 @@ dflash_status launch_gemm_tc_lo(int bn, int epi, const CUtensorMap& tmA, const W
 dflash_status launch_gemm_tc_hi(int bn, int epi, const CUtensorMap& tmA, const WMaps& wm,
                                 const GemmShape& g, int grid, const EpiArgs<bf16>& e,
                                 cudaStream_t st);
+// tu_gemm_c.cu: the tcgen05 kernel, 128 and 256 activation rows per tile
+dflash_status launch_gemm_umma(int bn, int epi, const CUtensorMap& tmA, const WMaps& wm,
+                               const GemmShape& g, int grid, const EpiArgs<bf16>& e,
+                               cudaStream_t st);
 dflash_status launch_gemm_f32(int epi, dim3 grid, const float* A, int lda, const WPtrs& w,
                               const GemmShape& g, const EpiArgs<float>& e, cudaStream_t st);
 dflash_status launch_attn_tc(int hd, int nw, dim3 grid, int smem, const AttnMaps& mp,

@@ -1,5 +1,5 @@
-// GEMM kernel instantiations with 64 and 128 activation rows per tile, and the
-// fp32 SIMT kernels.
+// mma.sync GEMM kernel instantiations with 64 activation rows per tile, and the fp32
+// SIMT kernels.
 #include "host.h"
 
 namespace dflash {
@@ -22,7 +22,7 @@ dflash_status launch_gemm_tc_hi(int bn, int epi, const CUtensorMap& tmA, const W
                                 const GemmShape& g, int grid, const EpiArgs<bf16>& e,
                                 cudaStream_t st) {
   if (bn == 64) return by_epi<64>(epi, tmA, wm, g, grid, e, st);
-  return by_epi<128>(epi, tmA, wm, g, grid, e, st);
+  return fail(DFLASH_EUNSUPPORTED, "mma.sync tile with %d rows", bn);
 }
 
 dflash_status launch_gemm_f32(int epi, dim3 grid, const float* A, int lda, const WPtrs& w,

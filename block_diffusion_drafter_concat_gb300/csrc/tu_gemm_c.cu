@@ -1,0 +1,42 @@
+// tcgen05 (TMEM-accumulator) projection kernel instantiations: 128 and 256 activation
+// rows per tile, every epilogue.
+#include "host.h"
+#include "umma.cuh"
+
+namespace dflash {
+
+template <int BN, int EPI>
+static dflash_status launch_um(const CUtensorMap& tmA, const WMaps& wm, const GemmShape& g,
+                               int grid, const EpiArgs<bf16>& e, cudaStream_t st) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    DFLASH_TRY(set_smem(k_gemm_umma<BN, EPI>, UmCfg<BN>::SMEM));
+    attr_set = true;
+  }
+  return launch(k_gemm_umma<BN, EPI>, dim3(grid), dim3(UmCfg<BN>::THREADS), UmCfg<BN>::SMEM, st,
+                tmA, wm, g, e);
+}
+
+template <int BN>
+static dflash_status by_epi(int epi, const CUtensorMap& tmA, const WMaps& wm, const GemmShape& g,
+                            int grid, const EpiArgs<bf16>& e, cudaStream_t st) {
+  switch (epi) {
+    case EPI_F32: return launch_um<BN, EPI_F32>(tmA, wm, g, grid, e, st);
+    case EPI_QKV: return launch_um<BN, EPI_QKV>(tmA, wm, g, grid, e, st);
+    case EPI_KV: return launch_um<BN, EPI_KV>(tmA, wm, g, grid, e, st);
+    case EPI_RESID: return launch_um<BN, EPI_RESID>(tmA, wm, g, grid, e, st);
+    case EPI_SWIGLU: return launch_um<BN, EPI_SWIGLU>(tmA, wm, g, grid, e, st);
+    case EPI_ARGMAX: return launch_um<BN, EPI_ARGMAX>(tmA, wm, g, grid, e, st);
+  }
+  return fail(DFLASH_EUNSUPPORTED, "unknown epilogue %d", epi);
+}
+
+dflash_status launch_gemm_umma(int bn, int epi, const CUtensorMap& tmA, const WMaps& wm,
+                               const GemmShape& g, int grid, const EpiArgs<bf16>& e,
+                               cudaStream_t st) {
+  if (bn == 128) return by_epi<128>(epi, tmA, wm, g, grid, e, st);
+  if (bn == 256) return by_epi<256>(epi, tmA, wm, g, grid, e, st);
+  return fail(DFLASH_EUNSUPPORTED, "tcgen05 tile with %d rows", bn);
+}
+
+}  // namespace dflash

@@ -1,0 +1,445 @@
+// Fifth-generation tensor-core (tcgen05) projection kernel for blocks of many rows.
+//
+// With a batch of sequences the block holds 128 to thousands of rows and every
+// projection turns from a weight stream into a dense contraction: mma.sync cannot keep
+// up there, so this kernel issues tcgen05.mma from one thread with its operands in
+// shared memory and its fp32 accumulator in tensor memory (TMEM).  The tile is the same
+// as the weight-streaming kernel's (swap-AB: 128 weight rows on the MMA's M side, BN =
+// 128 or 256 activation rows on its N side), fed by the same TMA ring and cut into the
+// same stream-K unit ranges, so the epilogues and the workspace layout are shared.  A
+// tile split between CTAs is finished by the contributor that arrives last, from its
+// own TMEM accumulator plus the others' published partials (two control words per
+// tile: arrivals and publications).
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer (one thread): weight box + activation box per k-stage
+//   warp 1      allocates TMEM (two accumulators of BN columns); one thread issues
+//               4 x tcgen05.mma (K = 16 each) per stage and commits the stage back to
+//               the producer, and each finished tile piece to the epilogue
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator 32 activation rows at a time
+//               (warp w reads TMEM lanes 32*(w%4)..+31, i.e. those weight rows), fp32
+//               tile chunk in shared memory, then the fused epilogue of the projection.
+// Two TMEM accumulators let the MMA of the next tile piece run under the epilogue of
+// the previous one.  Every mbarrier wait is bounded; a wait that gives up raises the
+// device error word and its role stops waiting, so the CTA always reaches the final
+// barrier and frees its TMEM.
+#pragma once
+
+#include "gemm.cuh"
+
+namespace dflash {
+
+// ---------------------------------------------------------------- tcgen05 wrappers
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand written by TMA with the 128-byte
+// swizzle: rows of 128 bytes (64 bf16 of K), 8-row swizzle atoms 1024 bytes apart
+// (stride byte offset), leading byte offset unused for this layout, descriptor version
+// 1, swizzle mode 2 (128 B).  `saddr` may be advanced by 32 bytes per K = 16 step inside
+// an atom; the atom base itself is 1024-byte aligned, so the base-offset field is 0.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both K-major,
+// M x N tile.
+template <int M, int N>
+__host__ __device__ constexpr uint32_t umma_idesc_bf16() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far is done.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 32 consecutive 32-bit TMEM columns of this warp's 32 lanes (lane i of the warp reads
+// TMEM lane (taddr >> 16) + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+        "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+        "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+        "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ configuration
+template <int BN>
+struct UmCfg {
+  static_assert(BN == 128 || BN == 256, "tcgen05 tiles take 128 or 256 activation rows");
+  static constexpr int NS = BN == 256 ? 4 : 6;       // pipeline stages
+  static constexpr int W_BYTES = kBM * kBK * 2;      // 16 KB weight box(es)
+  static constexpr int A_BYTES = BN * kBK * 2;       // activation box
+  static constexpr int STAGE = W_BYTES + A_BYTES;
+  static constexpr int CH = 32;                      // activation rows per epilogue chunk
+  static constexpr int PITCH = kBM + 4;
+  static constexpr int CS_BYTES = CH * PITCH * 4;
+  static constexpr int TMEM_COLS = 2 * BN;           // two fp32 accumulators
+  static constexpr int MAXC = 512;                   // contributors of one split tile
+  static constexpr int NBAR = 2 * NS + 5;            // full, empty, tfull[2], tempty[2], done
+  static constexpr int SMEM = 1024 + NS * STAGE + CS_BYTES + NBAR * 8 + 32 + MAXC * 4;
+  static constexpr int THREADS = 192;
+  static constexpr uint32_t IDESC = umma_idesc_bf16<kBM, BN>();
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(STAGE % 1024 == 0 && W_BYTES % 1024 == 0, "swizzle atoms stay 1024-aligned");
+};
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(192, 1)
+    k_gemm_umma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ WMaps wm,
+                const GemmShape g, const EpiArgs<bf16> e) {
+  using C = UmCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  float* Cs = reinterpret_cast<float*>(smem + C::NS * C::STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::NS * C::STAGE + C::CS_BYTES);
+  uint64_t* empty = full + C::NS;
+  uint64_t* tfull = empty + C::NS;   // [2] accumulator ready for the epilogue
+  uint64_t* tempty = tfull + 2;      // [2] accumulator drained by the epilogue
+  uint64_t* done = tempty + 2;       // every MMA of this CTA finished
+  uint32_t* tbase = reinterpret_cast<uint32_t*>(done + 1);
+  int* flag = reinterpret_cast<int*>(tbase + 4);
+  int* cslot = flag + 4;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int grid = gridDim.x, cta = blockIdx.x;
+  long long u0, u1;
+  if (g.tile_mode) {
+    // whole tiles: CTA c takes tiles [T*c/grid, T*(c+1)/grid)
+    const long long T = g.units / g.ks;
+    u0 = T * cta / grid * g.ks;
+    u1 = T * (cta + 1) / grid * g.ks;
+  } else {
+    cta_range(g.units, cta, grid, u0, u1);
+  }
+  const int n_my = static_cast<int>(u1 - u0);
+
+  if (tid == 0) {
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(done, 1);
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tbase, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tbase;
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && n_my > 0) {
+      tma_prefetch_desc(&tmA);
+      const uint64_t pol = policy_evict_first();
+      UnitWalk wc, ac;
+      wc.start(g, u0);
+      ac = wc;
+      auto issue_w = [&](int s, const UnitWalk& w) {
+        uint8_t* st = stages + s * C::STAGE;
+        if (g.paired) {
+          tma_load_2d_hint(st, &wm.m[0], &full[s], w.ks * kBK, w.row, pol);
+          tma_load_2d_hint(st + C::W_BYTES / 2, &wm.m[1], &full[s], w.ks * kBK, w.row, pol);
+        } else {
+          tma_load_2d_hint(st, &wm.m[w.seg], &full[s], w.ks * kBK, w.row, pol);
+        }
+      };
+      auto issue_a = [&](int s, const UnitWalk& w) {
+        tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmA, &full[s], w.ks * kBK, w.mb * BN);
+      };
+      const int pre = min(C::NS, n_my);
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], C::STAGE);
+        issue_w(i, wc);
+        wc.next(g);
+      }
+      pdl_wait();  // activations are written by the previous kernel
+      for (int i = 0; i < pre; ++i) {
+        issue_a(i, ac);
+        ac.next(g);
+      }
+      int issued = pre;
+      int s = pre % C::NS;
+      uint32_t par = (pre / C::NS) & 1;
+      for (int i = pre; i < n_my; ++i) {
+        if (!mbar_wait(&empty[s], par ^ 1)) {
+          raise_error(e.err, DFLASH_DEV_TIMEOUT);
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], C::STAGE);
+        issue_w(s, wc);
+        issue_a(s, ac);
+        wc.next(g);
+        ac.next(g);
+        issued = i + 1;
+        if (++s == C::NS) { s = 0; par ^= 1; }
+      }
+      // never leave with copies in flight
+      for (int i = max(0, issued - C::NS); i < issued; ++i)
+        mbar_wait(&full[i % C::NS], (i / C::NS) & 1);
+    }
+    __syncwarp();  // the warp reaches the final barrier converged
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      long long u = u0;
+      int i = 0, piece = 0;
+      while (u < u1) {
+        const int t = static_cast<int>(u / g.ks);
+        const long long seg_end = min(static_cast<long long>(t + 1) * g.ks, u1);
+        const int nk = static_cast<int>(seg_end - u);
+        const int ab = piece & 1, use = piece >> 1;
+        // the epilogue must have drained this accumulator's previous tile piece
+        if (ok && use > 0 && !mbar_wait(&tempty[ab], (use - 1) & 1)) {
+          raise_error(e.err, DFLASH_DEV_TIMEOUT);
+          ok = false;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(ab * BN);
+        for (int k = 0; k < nk; ++k, ++i) {
+          const int s = i % C::NS;
+          if (ok && !mbar_wait(&full[s], (i / C::NS) & 1)) {
+            raise_error(e.err, DFLASH_DEV_TIMEOUT);
+            ok = false;
+          }
+          if (ok) {
+            tc_fence_after();
+            const uint32_t wb = smem_u32(stages + s * C::STAGE);
+            const uint32_t ab_ = wb + C::W_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              umma_bf16(d, umma_desc_sw128(wb + kk * 32), umma_desc_sw128(ab_ + kk * 32), C::IDESC,
+                        (k | kk) != 0);
+          }
+          umma_commit(&empty[s]);  // frees the stage once these MMAs have read it
+        }
+        umma_commit(&tfull[ab]);   // the tile piece is complete in TMEM
+        u = seg_end;
+        ++piece;
+      }
+      umma_commit(done);
+      mbar_wait(done, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue warps
+    const int et = tid - 64;          // 0..127
+    const int q = warp & 3;           // TMEM lane quarter this warp may read
+    const int feat = q * 32 + lane;   // weight row (output column) of the tile this thread holds
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    bool ok = true;
+    pdl_wait();
+    long long u = u0;
+    int piece = 0;
+    while (u < u1) {
+      const int t = static_cast<int>(u / g.ks);
+      const int ks0 = static_cast<int>(u % g.ks);
+      const long long tile_end = static_cast<long long>(t + 1) * g.ks;
+      const long long seg_end = min(tile_end, u1);
+      const int ab = piece & 1, use = piece >> 1;
+      if (ok && !__all_sync(0xffffffffu, mbar_wait(&tfull[ab], use & 1))) {
+        if (lane == 0) raise_error(e.err, DFLASH_DEV_TIMEOUT);
+        ok = false;
+      }
+      tc_fence_after();
+      const uint32_t tacc = tmem + lane_base + static_cast<uint32_t>(ab * BN);
+      const int mb = t / g.n_tiles, nt = t - mb * g.n_tiles;
+      const int m_first = mb * BN;
+      const int rows = min(BN, g.M - m_first);            // valid activation rows
+      const int nch = (rows + C::CH - 1) / C::CH;         // chunks holding them
+      const bool whole = (ks0 == 0) && (seg_end == tile_end);
+
+      // Reads chunk c of the accumulator into v; after the last chunk the accumulator is
+      // handed back to the MMA issuer.
+      auto read_chunk = [&](int c, uint32_t (&v)[32]) {
+        if (ok) {
+          tmem_ld32(tacc + c * C::CH, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0u;
+        }
+        if (c == nch - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[ab]);
+        }
+      };
+
+      if (whole) {
+        for (int c = 0; c < nch; ++c) {
+          uint32_t v[32];
+          read_chunk(c, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) Cs[j * C::PITCH + feat] = __uint_as_float(v[j]);
+          epi_sync();
+          tile_epilogue<bf16, EPI>(Cs, C::PITCH, C::CH, m_first + c * C::CH, nt, g, e, et, 128);
+          epi_sync();
+        }
+      } else {
+        // A piece of a tile split between CTAs.  The order of arrival picks the CTA that
+        // finishes the tile: the others publish their partial tile ([BN][kBM] fp32 in
+        // their slot) and count themselves published; the finisher waits for them (they
+        // are already running and wait on nothing), keeps its own partial in TMEM and
+        // sums all contributions in contributor order, so the result does not depend on
+        // who arrived last.
+        const int slot = (u == u0) ? 0 : 1;
+        int* arrived = g.counters + t;
+        int* published = g.counters + kCtlWords / 2 + t;
+        if (et == 0) {
+          const int ncontrib = tile_contributors(g.units, grid, g.ks, t, nullptr);
+          flag[0] = (atomicAdd(arrived, 1) == ncontrib - 1);
+          flag[1] = ncontrib;
+        }
+        epi_sync();
+        const bool finisher = flag[0] != 0;
+        const int ncontrib = flag[1];
+        if (!finisher) {
+          // partial slot layout [activation row][weight row]: for each row the 32 lanes
+          // of a warp write (and the finisher reads) one whole 128-byte line
+          float* dst = g.part + (static_cast<long long>(cta) * 2 + slot) * BN * kBM;
+          for (int c = 0; c < nch; ++c) {
+            uint32_t v[32];
+            read_chunk(c, v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dst[(c * C::CH + j) * kBM + feat] = __uint_as_float(v[j]);
+          }
+          __threadfence();
+          epi_sync();
+          if (et == 0) atomicAdd(published, 1);
+        } else {
+          if (et == 0) {
+            tile_contributors(g.units, grid, g.ks, t, cslot);
+            const unsigned long long t0 = global_ns();
+            while (ld_acquire_gpu(published) < ncontrib - 1) {
+              if (global_ns() - t0 > kWaitNs) {
+                raise_error(e.err, DFLASH_DEV_TIMEOUT);
+                break;
+              }
+            }
+            *arrived = 0;
+            *published = 0;
+            __threadfence();
+          }
+          epi_sync();
+          for (int c = 0; c < nch; ++c) {
+            uint32_t own[32];
+            read_chunk(c, own);
+            float acc[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+            // contributors two at a time: 64 coalesced loads in flight per thread
+            for (int c0 = 0; c0 < ncontrib; c0 += 2) {
+              float pv[2][32];
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const int ci = c0 + k;
+                if (ci < ncontrib && (cslot[ci] >> 1) != cta) {
+                  const float* src = g.part + static_cast<long long>(cslot[ci]) * BN * kBM +
+                                     (c * C::CH) * kBM + feat;
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) pv[k][j] = __ldcg(src + j * kBM);
+                }
+              }
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const int ci = c0 + k;
+                if (ci >= ncontrib) continue;
+                if ((cslot[ci] >> 1) == cta) {
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) acc[j] += __uint_as_float(own[j]);
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) acc[j] += pv[k][j];
+                }
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) Cs[j * C::PITCH + feat] = acc[j];
+            epi_sync();
+            tile_epilogue<bf16, EPI>(Cs, C::PITCH, C::CH, m_first + c * C::CH, nt, g, e, et,
+                                     128);
+            epi_sync();
+          }
+        }
+      }
+      u = seg_end;
+      ++piece;
+    }
+  }
+
+  // ---- teardown: every role is here, every MMA has completed; free TMEM
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace dflash

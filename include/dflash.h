@@ -78,7 +78,8 @@ enum {
 
 /* Drafter shape.  d_model = d, fused input width = n_target_layers * target_width
  * (target layer l in columns [l*target_width, (l+1)*target_width)), q width =
- * n_q_heads * head_dim, kv width = n_kv_heads * head_dim.  page_size must be 16.
+ * n_q_heads * head_dim, kv width = n_kv_heads * head_dim.  page_size must be 16;
+ * head_dim must be even and divide 128 (64 or 128 for bf16).
  * max_position bounds every RoPE position (context and block).  rope_theta: base of
  * the rotary frequencies theta^(-2j/head_dim); rms_eps: epsilon of every RMSNorm. */
 typedef struct dflash_config {

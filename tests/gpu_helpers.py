@@ -26,25 +26,65 @@ def gather_kv(pool, table_host, b, positions):
     return pool[pages, :, off, :].float().cpu().numpy().astype(np.float64)
 
 
-def check_drafts(gpu_draft, oracle_draft, margin):
-    """Bit-exact where the oracle's margin is >= MARGIN.  Returns the low-margin mask."""
+def check_drafts(gpu_draft, oracle_draft, margin, slack=None):
+    """Bit-exact where the oracle's top-2 margin is >= MARGIN and, per row, >= `slack`
+    when given.  Returns the mask of rows left out."""
     gpu_draft = np.asarray(gpu_draft)
     low = np.asarray(margin) < MARGIN
+    if slack is not None:
+        low |= np.asarray(margin) < np.asarray(slack)
     bad = (~low) & (gpu_draft != np.asarray(oracle_draft))
     assert not bad.any(), (np.nonzero(bad), gpu_draft[bad], np.asarray(oracle_draft)[bad],
                            np.asarray(margin)[bad])
     return low
 
 
-def check_greedy(gpu_out, gpu_nacc, gpu_nemit, draft_o, logits_row, low):
-    """Greedy verify outputs of one sequence against the oracle on the oracle's drafts;
-    skipped (returns False) when a low-margin draft lies at or before the oracle's
-    first mismatch, since the two sides may then legitimately verify different drafts."""
-    out, n, ne = O.verify_greedy(draft_o, logits_row)
-    if low[: min(n, len(draft_o) - 1) + 1].any():
-        return False
+def check_greedy(gpu_out, gpu_nacc, gpu_nemit, gpu_draft, logits_row):
+    """Greedy verify outputs of one sequence, bit-exact against the oracle's verification
+    of the same drafts (the GPU's, which the draft checks tie to the oracle's) with the
+    same target logits."""
+    out, n, ne = O.verify_greedy(np.asarray(gpu_draft), logits_row)
     assert int(gpu_nacc) == n and int(gpu_nemit) == ne, (int(gpu_nacc), n, int(gpu_nemit), ne)
     assert list(np.asarray(gpu_out)) == list(out)
+    return True
+
+
+def check_sample(gpu_out, gpu_nacc, gpu_nemit, draft, z, logits, u, tau, eps=1e-3,
+                 cdf_tol=1e-4):
+    """Temperature-tau verify outputs of one sequence against the oracle's walk over the
+    same drafts, drafter logits z, target logits and uniforms.
+
+    The acceptance decisions are compared exactly; a walk that meets a ratio within eps
+    of its uniform is left unchecked (returns False).  At a rejection the residual token
+    is drawn by inverse CDF over the whole vocabulary: with 10^5 entries the CDF steps
+    are far finer than what an fp32 sum resolves, so the unique part is compared (the
+    rejection slot, the accepted prefix) and the drawn token must be a valid draw: its
+    CDF interval must contain u * sum(r) to within cdf_tol * sum(r)."""
+    gpu_out = np.asarray(gpu_out)
+    draft = np.asarray(draft)
+    S = len(draft)
+    for i in range(S):
+        p = O.softmax(np.asarray(logits[i], dtype=np.float64) / tau)
+        q = O.softmax(np.asarray(z[i], dtype=np.float64) / tau)
+        d = int(draft[i])
+        if abs(u[i, 0] * q[d] - p[d]) <= eps * max(p[d], q[d]):
+            return False
+        if u[i, 0] < p[d] / q[d]:
+            continue
+        assert (int(gpu_nacc), int(gpu_nemit)) == (i, i + 1), (int(gpu_nacc), int(gpu_nemit), i)
+        assert list(gpu_out[:i]) == list(draft[:i])
+        r = np.maximum(0.0, p - q)
+        if r.sum() == 0.0:
+            r = p
+        Z = r.sum()
+        cdf = np.cumsum(r)
+        t = int(gpu_out[i])
+        assert 0 <= t < len(r) and r[t] > 0, t
+        lo = cdf[t - 1] if t > 0 else 0.0
+        assert lo - cdf_tol * Z <= u[i, 1] * Z <= cdf[t] + cdf_tol * Z, (t, lo, cdf[t], u[i, 1] * Z)
+        return True
+    assert (int(gpu_nacc), int(gpu_nemit)) == (S, S)
+    assert list(gpu_out) == list(draft)
     return True
 
 
@@ -66,3 +106,22 @@ def sample_ambiguous(draft, z, logits, u, tau, eps=1e-3):
         cdf = np.cumsum(r)
         return bool(np.min(np.abs(cdf - u[i, 1] * r.sum())) <= eps * r.sum())
     return False
+
+
+def head_parity(gpu_draft, h_gpu, w_lm, z_oracle):
+    """The LM head + argmax on identical input, then the slack of the end-to-end draft
+    comparison.
+
+    The oracle's LM head applied to the GPU's own final hidden state must pick the
+    GPU's draft wherever that margin is >= MARGIN (the head adds no error of its own).
+    The GPU's hidden state differs from the oracle's by bf16 rounding decisions taken
+    the other way at the contract points (fp32 vs fp64 sums just either side of a
+    rounding boundary); over a long context these flips reach the logits.  The
+    returned per-row slack, twice the largest logit change that hidden-state
+    difference causes, is the margin below which the two drafts may legitimately
+    differ.  Also returns the oracle's logits of the GPU's hidden state."""
+    hg = np.asarray(h_gpu.detach().float().cpu().numpy() if torch.is_tensor(h_gpu) else h_gpu,
+                    dtype=np.float64)
+    zg = O.lm_head(hg, w_lm)
+    check_drafts(gpu_draft, O.argmax_lowest(zg), O.top2_margin(zg))
+    return 2.0 * np.abs(zg - np.asarray(z_oracle)).max(axis=1), zg

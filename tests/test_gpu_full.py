@@ -10,7 +10,8 @@ from oracle import dflash_oracle as O
 from oracle import run as orun
 from workload import configs, inputs
 
-from gpu_helpers import check_drafts, check_greedy, gather_kv, rel_err, sample_ambiguous, tol
+from gpu_helpers import (check_drafts, check_greedy, check_sample, gather_kv, head_parity,
+                         rel_err, tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -59,20 +60,20 @@ def test_full_size_sampled_parity(built, name):
             errs[f"v{l}"] = rel_err(gather_kv(r.cache.v[l], r.table_host, b, pos), s["V"][l][pos])
         print(name, b, {k: f"{v:.2e}" for k, v in errs.items()})
         assert max(errs.values()) < t, errs
-        low = check_drafts(r.draft[b].cpu().numpy(), s["draft"], s["margin"])
+        d_gpu = r.draft[b].cpu().numpy()
+        slack, zg = head_parity(d_gpu, hid[b], W["lm_head"], s["z"])
+        low = check_drafts(d_gpu, s["draft"], s["margin"], slack)
+        print(name, b, "logit slack", f"{slack.max():.3e}", "rows left out", int(low.sum()))
         lg = r.logits[b].float().cpu().numpy()
         if w.temperature > 0:
+            # verification of the GPU's drafts, whose drafter distribution is the oracle's
+            # LM head on the GPU's hidden state
             u = r.uniforms[b].cpu().numpy()
-            o, n, e = O.verify_sample(s["draft"], s["z"], lg, u, w.temperature)
-            if low[: min(n, S - 1) + 1].any() or sample_ambiguous(s["draft"], s["z"], lg, u,
-                                                                  w.temperature):
-                continue
-            assert (int(r.n_acc[b]), int(r.n_emit[b])) == (n, e)
-            assert r.out_tokens[b].cpu().tolist() == list(o)
-            checked += 1
+            checked += check_sample(r.out_tokens[b].cpu().numpy(), r.n_acc[b], r.n_emit[b],
+                                    d_gpu, zg, lg, u, w.temperature)
         else:
             checked += check_greedy(r.out_tokens[b].cpu().numpy(), r.n_acc[b].cpu(),
-                                    r.n_emit[b].cpu(), s["draft"], lg, low)
-    assert checked >= 1 or w.temperature > 0
+                                    r.n_emit[b].cpu(), d_gpu, lg)
+    assert checked >= 1
     del r
     torch.cuda.empty_cache()
