@@ -222,8 +222,8 @@ dflash_status gemm(const H* h, const void* A, int M, int K, const WSet& w, EpiAr
   g.counters = ctr;
   e.M = M;
   if (EPI == EPI_F32 || EPI == EPI_RESID || EPI == EPI_ARGMAX) e.N = w.rows[0];
-  // one control word per tile (two on the tcgen05 path: arrivals and publications)
-  const int ctl_per_tile = (tc && umma_bn(g.bn)) ? 2 : 1;
+  // two control words per tile: arrivals and publications of split pieces
+  const int ctl_per_tile = 2;
   if (g.m_blocks * g.n_tiles * ctl_per_tile > kCtlWords)
     return fail(DFLASH_EUNSUPPORTED, "GEMM with %d tiles exceeds the control words",
                 g.m_blocks * g.n_tiles);

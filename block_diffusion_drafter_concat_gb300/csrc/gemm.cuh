@@ -328,6 +328,12 @@ struct TcCfg {
   static constexpr int THREADS = 160;  // 4 consumer warps + 1 TMA producer warp
 };
 
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }
@@ -552,47 +558,85 @@ __global__ void __launch_bounds__(160, 1)
     const bool whole = (ks0 == 0) && (seg_end == tile_end);
     bool mine = true;
     if (!whole) {
-      // publish this piece, then let the last contributor of the tile finish it
-      const int slot = (u == u0) ? 0 : 1;
-      float* dst = g.part + ((long long)cta * 2 + slot) * BN * kBM;
-      for (int x = tid; x < BN * kBM / 4; x += 128) {
-        const int r = x / (kBM / 4), c4 = x % (kBM / 4);
-        reinterpret_cast<float4*>(dst)[x] = *reinterpret_cast<const float4*>(Cs + r * C::PITCH + c4 * 4);
-      }
-      __threadfence();
-      consumer_sync();
+      // A tile split between CTAs: the last to arrive finishes it.  The others publish
+      // their piece and count themselves published; the finisher waits for them (they
+      // are running and wait on nothing), then sums every piece in contributor order,
+      // its own straight from shared memory.
+      int* arrived = g.counters + t;
+      int* published = g.counters + kCtlWords / 2 + t;
       if (tid == 0) {
         const int nc = tile_contributors(g.units, grid, g.ks, t, nullptr);
-        int prev = atomicAdd(&g.counters[t], 1);
-        int last = (prev == nc - 1);
-        if (last) { atomicExch(&g.counters[t], 0); __threadfence(); }
-        *flag = last;
+        flag[0] = (atomicAdd(arrived, 1) == nc - 1);
+        flag[1] = nc;
       }
       consumer_sync();
-      mine = *flag != 0;
-      if (mine) {
-        // partial slots of the contributors, in contributor order
-        if (tid == 0) flag[1] = tile_contributors(g.units, grid, g.ks, t, cslot);
-        consumer_sync();
-        const int nc = flag[1];
-        // sum the published partials in contributor order; loads of up to four
-        // contributors are in flight together
+      mine = flag[0] != 0;
+      const int nc = flag[1];
+      if (!mine) {
+        const int slot = (u == u0) ? 0 : 1;
+        float* dst = g.part + ((long long)cta * 2 + slot) * BN * kBM;
         for (int x = tid; x < BN * kBM / 4; x += 128) {
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int c0 = 0; c0 < nc; c0 += 4) {
-            float4 v[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (c0 + j < nc)
-                v[j] = __ldcg(reinterpret_cast<const float4*>(g.part + (long long)cslot[c0 + j] * BN * kBM) + x);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (c0 + j < nc) {
-                acc.x += v[j].x; acc.y += v[j].y; acc.z += v[j].z; acc.w += v[j].w;
-              }
-          }
           const int r = x / (kBM / 4), c4 = x % (kBM / 4);
-          *reinterpret_cast<float4*>(Cs + r * C::PITCH + c4 * 4) = acc;
+          reinterpret_cast<float4*>(dst)[x] = *reinterpret_cast<const float4*>(Cs + r * C::PITCH + c4 * 4);
+        }
+        __threadfence();
+        consumer_sync();
+        if (tid == 0) atomicAdd(published, 1);
+      } else {
+        if (tid == 0) {
+          tile_contributors(g.units, grid, g.ks, t, cslot);
+          const unsigned long long t0 = global_ns();
+          while (ld_acquire_gpu(published) < nc - 1) {
+            if (global_ns() - t0 > kWaitNs) {
+              raise_error(e.err, DFLASH_DEV_TIMEOUT);
+              break;
+            }
+          }
+          *arrived = 0;
+          *published = 0;
+          __threadfence();
+        }
+        consumer_sync();
+        // every thread sums XN float4 positions; the loads of CR contributors for all of
+        // them (16 float4) are in flight together
+        constexpr int XN = BN * kBM / 4 / 128;
+        constexpr int CR = XN >= 16 ? 1 : 16 / XN;
+        float4 acc[XN];
+#pragma unroll
+        for (int q = 0; q < XN; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c0 = 0; c0 < nc; c0 += CR) {
+          float4 v[CR][XN];
+#pragma unroll
+          for (int j = 0; j < CR; ++j) {
+            if (c0 + j >= nc) continue;
+            const int cs = cslot[c0 + j];
+#pragma unroll
+            for (int q = 0; q < XN; ++q) {
+              const int x = tid + q * 128;
+              if ((cs >> 1) == cta) {
+                const int r = x / (kBM / 4), c4 = x % (kBM / 4);
+                v[j][q] = *reinterpret_cast<const float4*>(Cs + r * C::PITCH + c4 * 4);
+              } else {
+                v[j][q] = __ldcg(reinterpret_cast<const float4*>(g.part + (long long)cs * BN * kBM) + x);
+              }
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < CR; ++j) {
+            if (c0 + j >= nc) continue;
+#pragma unroll
+            for (int q = 0; q < XN; ++q) {
+              acc[q].x += v[j][q].x; acc[q].y += v[j][q].y;
+              acc[q].z += v[j][q].z; acc[q].w += v[j][q].w;
+            }
+          }
+        }
+        consumer_sync();   // every own value read before Cs is overwritten
+#pragma unroll
+        for (int q = 0; q < XN; ++q) {
+          const int x = tid + q * 128;
+          const int r = x / (kBM / 4), c4 = x % (kBM / 4);
+          *reinterpret_cast<float4*>(Cs + r * C::PITCH + c4 * 4) = acc[q];
         }
         consumer_sync();
       }
