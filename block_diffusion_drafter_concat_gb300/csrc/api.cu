@@ -765,7 +765,7 @@ dflash_status dflash_inject_kv(dflash_handle h, const void* x_cat, const void* f
     TRY(fuse_impl(h, x_cat, n, dst, w.u, w.gpart, w.ctl, st));
     f = dst;
   }
-  // one GEMM per group of up to 4 layers: segments k_l | v_l
+  // one GEMM per group of up to 8 layers: segments k_l | v_l
   for (int l0 = 0; l0 < c.n_layers; l0 += kMaxSeg / 2) {
     const int nl = std::min(kMaxSeg / 2, c.n_layers - l0);
     WSet ws_;

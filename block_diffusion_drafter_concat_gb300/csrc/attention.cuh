@@ -47,8 +47,8 @@ struct AttnMaps {
 // out[r] = sum_s w_s o_s / sum_s w_s l_s with w_s = 2^(m_s - max m), splits in order.
 template <typename T>
 __global__ void __launch_bounds__(256) k_attn_combine(const AttnArgs<T> a) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int b = blockIdx.z, g = blockIdx.y;
   const int hd4 = a.hd / 4;
   const int r = blockIdx.x * 8 + threadIdx.x / hd4, d4 = threadIdx.x % hd4;
@@ -60,20 +60,21 @@ __global__ void __launch_bounds__(256) k_attn_combine(const AttnArgs<T> a) {
   const long long grp = (long long)b * a.hkv + g;
   const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + grp * a.nsplit * a.QR;
   const float4* po = reinterpret_cast<const float4*>(a.part_o + grp * a.nsplit * a.QR * a.hd);
-  // one pass in split order with a running maximum (loads of 8 splits in flight)
+  // one pass in split order with a running maximum (loads of 16 splits in flight)
+  constexpr int SF = 16;
   float M = -INFINITY, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < ns; s0 += 8) {
-    float4 v[8];
-    float2 q[8];
+  for (int s0 = 0; s0 < ns; s0 += SF) {
+    float4 v[SF];
+    float2 q[SF];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < SF; ++j)
       if (s0 + j < ns) {
         q[j] = ml[(long long)(s0 + j) * a.QR + r];
         v[j] = po[((long long)(s0 + j) * a.QR + r) * hd4 + d4];
       }
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < SF; ++j)
       if (s0 + j < ns) {
         const float nm = fmaxf(M, q[j].x);
         const float al = exp2f(M - nm), w = exp2f(q[j].x - nm);
@@ -135,9 +136,9 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  pdl_launch_dependents();
-  pdl_wait();
-
+  // Context lengths, the page table and the context pages were written before the
+  // previous kernel started: they are read, and the context pages fetched, before the
+  // wait.  Only q and the block's own K/V come from the previous kernel.
   const int T = a.ctx_lens[b];
   if (T < 0 || T > a.max_pages * kPage) {
     if (tid == 0) raise_error(a.err, DFLASH_DEV_BAD_INDEX);
@@ -171,8 +172,10 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       const int cnt = min(32, nmy - base);
       for (int j = 0; j < cnt; ++j) {
         const int page_j = __shfl_sync(0xffffffffu, my_page, j);
+        const int i = base + j;
+        // the block's own keys, and stages beyond the first ring, follow the wait
+        if (i == min(C::NS, np - p0)) pdl_wait();
         if (lane == 0 && ok) {
-          const int i = base + j;
           const int s = i % C::NS;
           if (i >= C::NS && !mbar_wait(&empty[s], ((i / C::NS) - 1) & 1)) {
             raise_error(a.err, DFLASH_DEV_TIMEOUT);
@@ -211,6 +214,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       for (int i = max(0, issued - C::NS); i < issued; ++i) mbar_wait(&full[i % C::NS], (i / C::NS) & 1);
   } else {
     // ------------------------------------------------------------------ consumers
+    pdl_wait();   // q is written by the previous kernel
+    pdl_launch_dependents();
     const int g8 = lane >> 2, t4 = lane & 3, mi = lane >> 3, r8 = lane & 7;
     const int qr0 = warp * 16;
     const bf16* qb = a.q + (((long long)b * a.hkv + g) * a.QR + qr0) * HD;
@@ -337,8 +342,8 @@ static __global__ void __launch_bounds__(128) k_attn_f32(const AttnArgs<float> a
   float* lrow = mrow + QR;
   float* arow = lrow + QR;
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int T = a.ctx_lens[b];
   if (T < 0 || T > a.max_pages * kPage) {
     if (tid == 0) raise_error(a.err, DFLASH_DEV_BAD_INDEX);

@@ -147,7 +147,11 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
 // ------------------------------------------------------------------ PDL
 // Programmatic dependent launch: the next kernel on the stream may be scheduled once
 // every CTA of this one has called launch_dependents; it must call wait before it
-// touches anything this kernel writes.  Both are no-ops without the launch attribute.
+// touches anything this kernel writes.  Every kernel here calls launch_dependents only
+// after its own wait, so when a kernel starts, every kernel before its predecessor has
+// completed and its writes are visible: reads of such data (weights, the page table,
+// context lengths, cache pages written by an earlier call) may precede the wait.  Both
+// are no-ops without the launch attribute.
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

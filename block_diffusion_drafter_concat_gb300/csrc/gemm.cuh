@@ -20,7 +20,7 @@
 
 namespace dflash {
 
-constexpr int kMaxSeg = 8;
+constexpr int kMaxSeg = 16;  // weight segments of one projection launch (K/V of up to 8 layers)
 
 enum Epi : int {
   EPI_F32 = 0,    // y[m, n] = v (fp32)
@@ -427,7 +427,6 @@ __global__ void __launch_bounds__(160, 1)
     mbar_fence_init();
   }
   __syncthreads();
-  pdl_launch_dependents();
 
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
@@ -486,6 +485,7 @@ __global__ void __launch_bounds__(160, 1)
 
   // -------------------------------------------------------------------- consumers
   pdl_wait();
+  pdl_launch_dependents();
   constexpr int NB = BN / 8;  // n8 tiles of activation rows
   float acc[2][NB][4];
   const int g8 = lane >> 2, t4 = lane & 3, mi = lane >> 3, r8 = lane & 7;
@@ -667,8 +667,8 @@ __global__ void __launch_bounds__(256)
   __shared__ float As[kF32BN][kF32BK + 1];
   __shared__ float Ws[kBM][kF32BK + 1];
   __shared__ __align__(16) float Cs[kF32BN * (kBM + 4)];
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int t = blockIdx.x;
   const int mb = t / g.n_tiles, nt = t % g.n_tiles;
   int seg = 0;

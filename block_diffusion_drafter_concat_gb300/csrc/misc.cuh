@@ -31,7 +31,6 @@ __global__ void __launch_bounds__(kRowThreads)
               const T* __restrict__ embed, int vocab, const int* __restrict__ ctx_lens, int S,
               int max_position, int* __restrict__ pos, int* err) {
   __shared__ float red[kRowThreads / 32];
-  pdl_launch_dependents();
   // the gains are weights (never written on the device): fetch them before the wait
   float gv[32];
   const bool regs = (sizeof(Tin) == 4) && (d & 3) == 0 && d <= kRowThreads * 4 * 8 && !ids;
@@ -44,6 +43,7 @@ __global__ void __launch_bounds__(kRowThreads)
     }
   }
   pdl_wait();
+  pdl_launch_dependents();
   const int m = blockIdx.x;
   const Tin* src = xin + (long long)m * d;
   if (ids) {
@@ -116,8 +116,8 @@ static __global__ void __launch_bounds__(kRowThreads)
                       const float* __restrict__ am_sum, int n_tiles, int M, float inv_temp,
                       int* __restrict__ tokens, float* __restrict__ max_logit,
                       float* __restrict__ lse) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = blockIdx.x * (kRowThreads / 32) + warp;
   if (m >= M) return;
@@ -155,8 +155,8 @@ __global__ void __launch_bounds__(kRowThreads)
   __shared__ int si[kRowThreads / 32];
   __shared__ int flag;
   __shared__ int tok[64];
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int c = blockIdx.x, row = blockIdx.y, nch = gridDim.x;
   const int b = row / S;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -247,8 +247,8 @@ __global__ void __launch_bounds__(kRowThreads)
   __shared__ float redm[kRowThreads / 32];
   __shared__ int flag;
   __shared__ int nrej;
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int c = blockIdx.x, row = blockIdx.y, nch = gridDim.x;
   const int b = row / S;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -323,8 +323,8 @@ __global__ void __launch_bounds__(kRowThreads)
   __shared__ int flag;
   __shared__ float scan[kRowThreads];
   __shared__ int found;
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int c = blockIdx.x, b = blockIdx.y, nch = gridDim.x;
   const int n = rej[b];
   if (n >= S) return;  // everything accepted: nothing to sample (counter unused)

@@ -184,7 +184,6 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tbase;
-  pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -289,6 +288,7 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     bool ok = true;
     pdl_wait();
+    pdl_launch_dependents();
     long long u = u0;
     int piece = 0;
     while (u < u1) {
