@@ -261,11 +261,14 @@ struct AttnPlan {
 };
 
 AttnPlan plan_attn(const H* h, int B, int max_pages) {
-  // enough (b, kv head, split) CTAs to cover the SMs, at least 8 pages per split
+  // About eight (b, kv head, split) CTAs per SM at the longest context, so that ragged
+  // lengths and the last wave of CTAs balance; at least 8 pages and at most 64 splits.
   const int kp = max_pages + 1;
-  const int groups = B * h->c.n_kv_heads;
-  const int want = std::max(1, ceil_div(h->sms, groups));
-  const int pps = std::max(8, ceil_div(kp, want));
+  const long long groups = (long long)B * h->c.n_kv_heads;
+  const long long want = std::max<long long>(1, (8LL * h->sms + groups - 1) / groups);
+  const long long cap = std::min(64, ceil_div(kp, 8));
+  const int ns = static_cast<int>(std::min(want, cap));
+  const int pps = std::max(8, ceil_div(kp, ns));
   return {pps, ceil_div(kp, pps)};
 }
 

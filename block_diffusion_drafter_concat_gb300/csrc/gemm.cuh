@@ -328,6 +328,12 @@ struct TcCfg {
   static constexpr int THREADS = 160;  // 4 consumer warps + 1 TMA producer warp
 };
 
+// Publication of a CTA's partial tile: after a CTA barrier one thread's release-add
+// makes every thread's earlier writes visible at GPU scope to an acquiring reader.
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -579,9 +585,8 @@ __global__ void __launch_bounds__(160, 1)
           const int r = x / (kBM / 4), c4 = x % (kBM / 4);
           reinterpret_cast<float4*>(dst)[x] = *reinterpret_cast<const float4*>(Cs + r * C::PITCH + c4 * 4);
         }
-        __threadfence();
         consumer_sync();
-        if (tid == 0) atomicAdd(published, 1);
+        if (tid == 0) red_release_add(published, 1);
       } else {
         if (tid == 0) {
           tile_contributors(g.units, grid, g.ks, t, cslot);

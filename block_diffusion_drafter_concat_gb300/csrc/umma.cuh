@@ -364,9 +364,8 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) dst[(c * C::CH + j) * kBM + feat] = __uint_as_float(v[j]);
           }
-          __threadfence();
           epi_sync();
-          if (et == 0) atomicAdd(published, 1);
+          if (et == 0) red_release_add(published, 1);
         } else {
           if (et == 0) {
             tile_contributors(g.units, grid, g.ks, t, cslot);
