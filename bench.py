@@ -30,7 +30,7 @@ METRIC = "draft+verify steps/sec and tokens/sec; achieved HBM GB/s vs ~8 TB/s (1
 DEFAULT_CONFIG = "qwen3-8b-shaped-b1"
 # DRAM read + write bytes of one LM-head launch on this workload, from an ncu capture of
 # the current kernel (None until the kernel has been captured since its last change)
-LM_HEAD_TRAFFIC = None
+LM_HEAD_TRAFFIC = 1250015696
 
 
 def parse():
