@@ -256,6 +256,13 @@ dflash_status rmsnorm(const H* h, const Tin* x, const void* gain, T* y, int rows
 }
 
 // ------------------------------------------------------------------ attention plan
+// Blocks of many rows (a batch of sequences) with head_dim 64 run attention on the
+// tcgen05 kernel; the rest on the mma.sync kernel.
+bool use_attn_umma(const dflash_config& c, int M) {
+  const int QR = c.block_size * (c.n_q_heads / c.n_kv_heads);
+  return c.dtype == DFLASH_BF16 && c.head_dim == 64 && M > 64 && QR <= 128;
+}
+
 struct AttnPlan {
   int pps, nsplit;
 };
@@ -481,8 +488,19 @@ static dflash_status draft_impl(H* h, const int32_t* block_ids, const int32_t* c
         const uint64_t blk_rows = (uint64_t)B * c.n_kv_heads * S;
         TRY(encode_bf16(&mp.kb, w.kb, blk_rows, c.head_dim, c.head_dim, kPage));
         TRY(encode_bf16(&mp.vb, w.vb, blk_rows, c.head_dim, c.head_dim, kPage));
-        const int smem = 1024 + kAttnStages * (2 * kPage * c.head_dim * 2 + 16) + 16;
-        TRY(launch_attn_tc(c.head_dim, QR / 16, grid, smem, mp, a, st));
+        if (use_attn_umma(c, M)) {
+          AuMaps am;
+          am.k = mp.k;
+          am.v = mp.v;
+          am.kb = mp.kb;
+          am.vb = mp.vb;
+          TRY(encode_bf16(&am.q, w.q, (uint64_t)B * c.n_kv_heads * QR, c.head_dim, c.head_dim,
+                          128));
+          TRY(launch_attn_umma(c.head_dim, grid, am, a, st));
+        } else {
+          const int smem = 1024 + kAttnStages * (2 * kPage * c.head_dim * 2 + 16) + 16;
+          TRY(launch_attn_tc(c.head_dim, QR / 16, grid, smem, mp, a, st));
+        }
       } else {
         const int smem = (2 * QR * c.head_dim + 2 * kPage * c.head_dim + QR * kPage + 3 * QR) * 4;
         TRY(launch_attn_f32(grid, smem, a, st));

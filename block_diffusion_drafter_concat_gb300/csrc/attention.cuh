@@ -39,6 +39,12 @@ struct AttnArgs {
   int* err;
 };
 
+// Tensor maps of the tcgen05 attention kernel: q as [B*hkv*QR, hd] with 128-row boxes,
+// the pools and the block K/V with 16-row boxes.
+struct AuMaps {
+  CUtensorMap q, k, v, kb, vb;
+};
+
 struct AttnMaps {
   CUtensorMap k, v, kb, vb;
 };

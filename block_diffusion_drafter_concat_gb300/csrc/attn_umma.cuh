@@ -1,0 +1,362 @@
+// Split-context attention on the 5th-generation tensor cores, for batches of blocks.
+//
+// One CTA takes one (sequence, kv head, page range) like the mma.sync kernel and
+// produces the same online-softmax state, but both contractions run as tcgen05.mma
+// with M = 128 query rows (the block's S*G rows of the kv head, padded to 128):
+//   S = Q K^T     N = 64 keys (four 16-key pages), K = head_dim;   fp32 in TMEM
+//   O_j = P V     N = head_dim, K = 64 keys, P as a bf16 pair hi + lo (two MMAs)
+// Q and the K/V pages arrive by TMA with the 128-byte swizzle (K pages are K-major
+// operands, V pages MN-major ones, exactly as they sit in the cache); P is written to
+// shared memory by the softmax warps in the K-major swizzled layout.
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: Q once, then four pages of K and V per ring stage
+//   warp 1      allocates TMEM (S double buffer 2 x 64 columns + O_j, head_dim columns)
+//               and issues the MMAs from one thread: S of step j+1 is computed while
+//               the softmax warps work on step j
+//   warps 2..5  one query row per thread (TMEM lane): read S, mask, running max and
+//               sum in the log2 domain, write P, then fold O_j into registers:
+//               O = O * 2^(m_old - m_new) + O_j
+// Every wait is bounded; a role whose wait gives up raises the error word and stops.
+#pragma once
+
+#include "attention.cuh"
+#include "umma.cuh"
+
+namespace dflash {
+
+// Shared-memory descriptor with explicit leading/stride byte offsets, 128-byte swizzle.
+__device__ __forceinline__ uint64_t umma_desc_sw128_lbo(uint32_t saddr, uint32_t lbo,
+                                                        uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <int HD>
+struct AuCfg {
+  static constexpr int KT = 64;                    // keys per step
+  static constexpr int PG = KT / kPage;            // pages per step
+  static constexpr int KB = HD / 64;               // 64-column blocks of a head
+  static constexpr int NS = HD == 64 ? 4 : 2;      // ring stages
+  static constexpr int Q_BYTES = 128 * HD * 2;
+  static constexpr int KV_BLOCK = KT * 128;        // one 64-column block of K or V
+  static constexpr int KV_BYTES = KB * KV_BLOCK;
+  static constexpr int STAGE = 2 * KV_BYTES;       // K then V
+  static constexpr int PAGE_BYTES = kPage * HD * 2;  // one page of K (or V)
+  static constexpr int P_BYTES = 128 * KT * 2;     // one bf16 P tile
+  static constexpr int NBAR = 2 * NS + 8;
+  static constexpr int SMEM = 1024 + Q_BYTES + NS * STAGE + 2 * P_BYTES + NBAR * 8 + 16;
+  static constexpr int TMEM_COLS = 256;
+  static constexpr int O_COL = 2 * KT;             // O_j columns [128, 128 + HD)
+  static constexpr int THREADS = 192;
+  static constexpr uint32_t IDESC_S = umma_idesc_bf16<128, KT>();
+  static constexpr uint32_t IDESC_O = umma_idesc_bf16<128, HD>() | (1u << 16);  // B MN-major
+  static_assert(O_COL + HD <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+template <int HD>
+__global__ void __launch_bounds__(192, 1)
+    k_attn_umma(const __grid_constant__ AuMaps maps, const AttnArgs<bf16> a) {
+  using C = AuCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sq = smem;                                   // Q: KB blocks of [128][64]
+  uint8_t* stages = sq + C::Q_BYTES;                    // K blocks, then V blocks
+  uint8_t* sp = stages + C::NS * C::STAGE;              // P hi, P lo: [128][64 keys]
+  uint64_t* kvfull = reinterpret_cast<uint64_t*>(sp + 2 * C::P_BYTES);
+  uint64_t* kvempty = kvfull + C::NS;
+  uint64_t* qfull = kvempty + C::NS;
+  uint64_t* sfull = qfull + 1;    // [2]
+  uint64_t* sfree = sfull + 2;    // [2]
+  uint64_t* pready = sfree + 2;
+  uint64_t* ofull = pready + 1;
+  uint64_t* done = ofull + 1;
+  uint32_t* tbase = reinterpret_cast<uint32_t*>(done + 1);
+
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // context lengths and the page table predate the previous kernel (read before the wait)
+  const int T = a.ctx_lens[b];
+  if (T < 0 || T > a.max_pages * kPage) {
+    if (tid == 0) raise_error(a.err, DFLASH_DEV_BAD_INDEX);
+    return;
+  }
+  const int np = (T + kPage - 1) / kPage;   // context pages
+  const int kp = np + 1;                    // + the block's own keys
+  const int ns = (kp + a.pps - 1) / a.pps;
+  if (split >= ns) return;
+  const int p0 = split * a.pps, p1 = min(kp, p0 + a.pps);
+  const int npg = p1 - p0;
+  const int nsteps = (npg + C::PG - 1) / C::PG;
+
+  if (tid == 0) {
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&kvfull[s], 1);
+      mbar_init(&kvempty[s], 1);
+    }
+    mbar_init(qfull, 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&sfull[k], 1);
+      mbar_init(&sfree[k], 4);
+    }
+    mbar_init(pready, 4);
+    mbar_init(ofull, 1);
+    mbar_init(done, 1);
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tbase, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tbase;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    // Context pages are fetched before the wait; Q, the block's own keys and any stage
+    // that reuses the ring (its consumers need Q) come after it.
+    bool ok = true, waited = false;
+    int issued = 0;
+    auto wait_then_q = [&]() {
+      if (waited) return;
+      pdl_wait();
+      waited = true;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(qfull, C::Q_BYTES);
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_2d(sq + kb * (128 * 128), &maps.q, qfull, kb * 64, (b * a.hkv + g) * a.QR);
+      }
+    };
+    for (int j = 0; j < nsteps && ok; ++j) {
+      const int s = j % C::NS;
+      const int pa = j * C::PG;                       // first page of the step in the split
+      const int cnt = min(C::PG, npg - pa);
+      if (j >= C::NS || p0 + pa + cnt > np) wait_then_q();
+      int my_page = 0;
+      if (lane < cnt && p0 + pa + lane < np)
+        my_page = a.page_table[(long long)b * a.max_pages + p0 + pa + lane];
+      if (lane == 0 && j >= C::NS && !mbar_wait(&kvempty[s], ((j / C::NS) - 1) & 1)) {
+        raise_error(a.err, DFLASH_DEV_TIMEOUT);
+        ok = false;
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (lane == 0) mbar_arrive_expect_tx(&kvfull[s], cnt * 2 * C::PAGE_BYTES);
+      for (int q = 0; q < cnt; ++q) {
+        const int page_q = __shfl_sync(0xffffffffu, my_page, q);
+        if (lane == 0) {
+          const int pg = p0 + pa + q;
+          const CUtensorMap *mk, *mv;
+          int row;
+          if (pg < np) {
+            int page = page_q;
+            if (page < 0 || page >= a.num_pages) {
+              raise_error(a.err, DFLASH_DEV_BAD_INDEX);
+              page = 0;
+            }
+            mk = &maps.k;
+            mv = &maps.v;
+            row = (page * a.hkv + g) * kPage;
+          } else {
+            mk = &maps.kb;
+            mv = &maps.vb;
+            row = (b * a.hkv + g) * a.S;
+          }
+          uint8_t* kd = stages + s * C::STAGE + q * (kPage * 128);
+          uint8_t* vd = kd + C::KV_BYTES;
+#pragma unroll
+          for (int kb = 0; kb < C::KB; ++kb) {
+            tma_load_2d(kd + kb * C::KV_BLOCK, mk, &kvfull[s], kb * 64, row);
+            tma_load_2d(vd + kb * C::KV_BLOCK, mv, &kvfull[s], kb * 64, row);
+          }
+        }
+      }
+      issued = j + 1;
+    }
+    wait_then_q();
+    if (lane == 0) {
+      // never leave with copies in flight
+      mbar_wait(qfull, 0);
+      for (int j = max(0, issued - C::NS); j < issued; ++j)
+        mbar_wait(&kvfull[j % C::NS], (j / C::NS) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(qfull, 0);
+      if (!ok) raise_error(a.err, DFLASH_DEV_TIMEOUT);
+      const uint32_t qa = smem_u32(sq);
+      auto issue_s = [&](int j) {
+        const int s = j % C::NS, sb = j & 1;
+        if (!mbar_wait(&kvfull[s], (j / C::NS) & 1)) return false;
+        if (j >= 2 && !mbar_wait(&sfree[sb], ((j >> 1) - 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t kbase = smem_u32(stages + s * C::STAGE);
+        const uint32_t d = tmem + static_cast<uint32_t>(sb * C::KT);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint64_t ad = umma_desc_sw128(qa + (kk >> 2) * (128 * 128) + (kk & 3) * 32);
+          const uint64_t bd = umma_desc_sw128(kbase + (kk >> 2) * C::KV_BLOCK + (kk & 3) * 32);
+          umma_bf16(d, ad, bd, C::IDESC_S, kk != 0);
+        }
+        umma_commit(&sfull[sb]);
+        return true;
+      };
+      if (ok && nsteps > 0) ok = issue_s(0);
+      for (int j = 0; j < nsteps && ok; ++j) {
+        if (j + 1 < nsteps && !issue_s(j + 1)) { ok = false; break; }
+        if (!mbar_wait(pready, j & 1)) { ok = false; break; }
+        tc_fence_after();
+        const int s = j % C::NS;
+        const uint32_t vbase = smem_u32(stages + s * C::STAGE) + C::KV_BYTES;
+        const uint32_t d = tmem + C::O_COL;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t pbase = smem_u32(sp + h * C::P_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < C::KT / 16; ++kk) {
+            const uint64_t ad = umma_desc_sw128(pbase + kk * 32);
+            // V: MN-major (head dims contiguous), 8-key groups 1024 B apart, 64-column
+            // blocks of the head KV_BLOCK apart; 16 keys per MMA = two groups
+            const uint64_t bd = umma_desc_sw128_lbo(vbase + kk * 2048, C::KV_BLOCK, 1024);
+            umma_bf16(d, ad, bd, C::IDESC_O, (h | kk) != 0);
+          }
+        }
+        umma_commit(ofull);
+        umma_commit(&kvempty[s]);
+      }
+      if (!ok) raise_error(a.err, DFLASH_DEV_TIMEOUT);
+      umma_commit(done);
+      mbar_wait(done, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax warps
+    pdl_wait();
+    pdl_launch_dependents();
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;                     // query row = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    const float sc = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
+    float o[HD];
+#pragma unroll
+    for (int d = 0; d < HD; ++d) o[d] = 0.f;
+    float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
+    bool ok = true;
+    for (int j = 0; j < nsteps && ok; ++j) {
+      const int sb = j & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sfull[sb], (j >> 1) & 1))) { ok = false; break; }
+      tc_fence_after();
+      uint32_t s0[32], s1[32];
+      tmem_ld32(tmem + lane_base + sb * C::KT, s0);
+      tmem_ld32(tmem + lane_base + sb * C::KT + 32, s1);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sfree[sb]);
+      // mask keys past each page's valid count, scale to the log2 domain
+      float x[64];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < C::PG; ++q) {
+        const int pg = p0 + j * C::PG + q;
+        const int valid = pg >= p1 ? 0 : (pg < np) ? min(kPage, T - pg * kPage) : a.S;
+#pragma unroll
+        for (int k = 0; k < kPage; ++k) {
+          const int key = q * kPage + k;
+          const uint32_t raw = key < 32 ? s0[key & 31] : s1[key & 31];
+          const float v = k < valid ? __uint_as_float(raw) * sc : -INFINITY;
+          x[q * kPage + k] = v;
+          mx = fmaxf(mx, v);
+        }
+      }
+      const float mn = fmaxf(m, mx);
+      const float alpha = exp2f(m - mn);
+      m = mn;
+      float ps = 0.f;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) {
+        x[k] = exp2f(x[k] - mn);
+        ps += x[k];
+      }
+      l = l * alpha + ps;
+      // fold in the previous step's P V (its MMAs are done with the P buffer too)
+      if (j > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(ofull, (j - 1) & 1))) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + C::O_COL + c * 32, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int d = 0; d < 32; ++d) o[c * 32 + d] = o[c * 32 + d] * alpha_prev + __uint_as_float(ov[d]);
+        }
+      }
+      alpha_prev = alpha;
+      // P hi and lo, row r, 64 keys: 8 chunks of 16 B, 128-byte swizzle
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split_bf16x2(x[ch * 8 + 2 * e], x[ch * 8 + 2 * e + 1], hi[e], lo[e]);
+        const int off = r * 128 + ((ch ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(sp + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(sp + C::P_BYTES + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pready);
+    }
+    if (ok && nsteps > 0) {
+      if (__all_sync(0xffffffffu, mbar_wait(ofull, (nsteps - 1) & 1))) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + C::O_COL + c * 32, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int d = 0; d < 32; ++d) o[c * 32 + d] = o[c * 32 + d] * alpha_prev + __uint_as_float(ov[d]);
+        }
+      } else {
+        ok = false;
+      }
+    }
+    if (!ok && lane == 0) raise_error(a.err, DFLASH_DEV_TIMEOUT);
+    if (r < a.QR) {
+#pragma unroll
+      for (int d = 0; d < HD; d += 2) attn_emit<bf16>(a, b, g, split, r, d, o[d], o[d + 1], l);
+      if (a.nsplit > 1) {
+        const long long grp = (long long)b * a.hkv + g;
+        float* pm = a.part_ml + ((grp * a.nsplit + split) * a.QR + r) * 2;
+        pm[0] = m;
+        pm[1] = l;
+      }
+    }
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace dflash

@@ -1,0 +1,19 @@
+// tcgen05 attention instantiation (head_dim 64).
+#include "host.h"
+#include "attn_umma.cuh"
+
+namespace dflash {
+
+dflash_status launch_attn_umma(int hd, dim3 grid, const AuMaps& mp, const AttnArgs<bf16>& a,
+                               cudaStream_t st) {
+  if (hd != 64) return fail(DFLASH_EUNSUPPORTED, "tcgen05 attention: head_dim %d", hd);
+  using C = AuCfg<64>;
+  static bool set = false;
+  if (!set) {
+    DFLASH_TRY(set_smem(k_attn_umma<64>, C::SMEM));
+    set = true;
+  }
+  return launch(k_attn_umma<64>, grid, dim3(C::THREADS), C::SMEM, st, mp, a);
+}
+
+}  // namespace dflash

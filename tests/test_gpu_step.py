@@ -33,6 +33,14 @@ SMALL = {
         name="small-bf16-b6-tc128", batch=6, ctx_range=(20, 90), seed=16),
     "small-bf16-b20-tc256": configs.small_bf16(
         name="small-bf16-b20-tc256", batch=20, ctx_range=(16, 64), seed=17),
+    # head_dim 64 with 96 and 80 block rows: attention on the tcgen05 kernel with 128 and
+    # 64 query rows per kv head, ragged contexts over several splits and steps
+    "small-bf16-hd64-g8-b6-tc": configs.small_bf16(
+        name="small-bf16-hd64-g8-b6-tc", d_model=384, n_q_heads=16, n_kv_heads=2,
+        head_dim=64, ffn_dim=384, vocab=2176, batch=6, ctx_range=(16, 250), seed=19),
+    "small-bf16-hd64-g4-b5-tc": configs.small_bf16(
+        name="small-bf16-hd64-g4-b5-tc", d_model=384, n_q_heads=8, n_kv_heads=2,
+        head_dim=64, ffn_dim=384, vocab=2176, batch=5, ctx_range=(20, 180), seed=20),
     # 256 rows with K = 1024 and a 32000-token vocabulary: whole tiles per CTA as well
     "mid-bf16-b16-tc256": configs.small_bf16(
         name="mid-bf16-b16-tc256", d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128,
