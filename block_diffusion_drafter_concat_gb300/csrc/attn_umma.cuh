@@ -4,19 +4,20 @@
 // produces the same online-softmax state, but both contractions run as tcgen05.mma
 // with M = 128 query rows (the block's S*G rows of the kv head, padded to 128):
 //   S = Q K^T     N = 64 keys (four 16-key pages), K = head_dim;   fp32 in TMEM
-//   O_j = P V     N = head_dim, K = 64 keys, P as a bf16 pair hi + lo (two MMAs)
+//   O += P V      N = head_dim, K = 64 keys, P as a bf16 pair hi + lo (two MMAs)
 // Q and the K/V pages arrive by TMA with the 128-byte swizzle (K pages are K-major
 // operands, V pages MN-major ones, exactly as they sit in the cache); P is written to
 // shared memory by the softmax warps in the K-major swizzled layout.
 //
 // Warp roles (192 threads):
 //   warp 0      TMA producer: Q once, then four pages of K and V per ring stage
-//   warp 1      allocates TMEM (S double buffer 2 x 64 columns + O_j, head_dim columns)
+//   warp 1      allocates TMEM (S double buffer 2 x 64 columns + O, head_dim columns)
 //               and issues the MMAs from one thread: S of step j+1 is computed while
 //               the softmax warps work on step j
-//   warps 2..5  one query row per thread (TMEM lane): read S, mask, running max and
-//               sum in the log2 domain, write P, then fold O_j into registers:
-//               O = O * 2^(m_old - m_new) + O_j
+//   warps 2..5  one query row per thread (TMEM lane): read S, mask, exponentiate
+//               against a reference maximum in the log2 domain, write P; O accumulates
+//               in TMEM across steps and is rescaled in place only when the reference
+//               moves (by more than 8)
 // Every wait is bounded; a role whose wait gives up raises the error word and stops.
 #pragma once
 
@@ -43,7 +44,7 @@ struct AuCfg {
   static constexpr int KT = 64;                    // keys per step
   static constexpr int PG = KT / kPage;            // pages per step
   static constexpr int KB = HD / 64;               // 64-column blocks of a head
-  static constexpr int NS = HD == 64 ? 4 : 2;      // ring stages
+  static constexpr int NS = HD == 64 ? 3 : 2;      // ring stages
   static constexpr int Q_BYTES = 128 * HD * 2;
   static constexpr int KV_BLOCK = KT * 128;        // one 64-column block of K or V
   static constexpr int KV_BYTES = KB * KV_BLOCK;
@@ -62,7 +63,7 @@ struct AuCfg {
 };
 
 template <int HD>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, 2)
     k_attn_umma(const __grid_constant__ AuMaps maps, const AttnArgs<bf16> a) {
   using C = AuCfg<HD>;
   extern __shared__ uint8_t smem_raw[];
@@ -232,7 +233,7 @@ __global__ void __launch_bounds__(192, 1)
             // V: MN-major (head dims contiguous), 8-key groups 1024 B apart, 64-column
             // blocks of the head KV_BLOCK apart; 16 keys per MMA = two groups
             const uint64_t bd = umma_desc_sw128_lbo(vbase + kk * 2048, C::KV_BLOCK, 1024);
-            umma_bf16(d, ad, bd, C::IDESC_O, (h | kk) != 0);
+            umma_bf16(d, ad, bd, C::IDESC_O, (j | h | kk) != 0);
           }
         }
         umma_commit(ofull);
@@ -250,11 +251,13 @@ __global__ void __launch_bounds__(192, 1)
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;                     // query row = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t o_addr = tmem + lane_base + C::O_COL;
     const float sc = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
-    float o[HD];
-#pragma unroll
-    for (int d = 0; d < HD; ++d) o[d] = 0.f;
-    float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
+    // Reference maximum in the log2 domain: probabilities are 2^(s - mref), O and l
+    // accumulate against it (O in TMEM, by the MMAs).  mref moves only when a score
+    // exceeds it by more than 8 (a factor 256 stays well inside fp32), so O is rescaled
+    // in TMEM rarely; the result does not depend on the reference.
+    float mref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nsteps && ok; ++j) {
       const int sb = j & 1;
@@ -279,34 +282,41 @@ __global__ void __launch_bounds__(192, 1)
           const int key = q * kPage + k;
           const uint32_t raw = key < 32 ? s0[key & 31] : s1[key & 31];
           const float v = k < valid ? __uint_as_float(raw) * sc : -INFINITY;
-          x[q * kPage + k] = v;
+          x[key] = v;
           mx = fmaxf(mx, v);
         }
       }
-      const float mn = fmaxf(m, mx);
-      const float alpha = exp2f(m - mn);
-      m = mn;
+      const bool move = mx > mref + 8.f;
+      if (__any_sync(0xffffffffu, move)) {
+        const float mn = move ? mx : mref;
+        const float alpha = exp2f(mref - mn);         // 0 on the first step
+        l *= alpha;
+        mref = mn;
+        if (j > 0) {
+          // the previous step's P V must have landed before O is rescaled in place
+          if (!__all_sync(0xffffffffu, mbar_wait(ofull, (j - 1) & 1))) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(o_addr + c * 32, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int d = 0; d < 32; ++d) ov[d] = __float_as_uint(__uint_as_float(ov[d]) * alpha);
+            tmem_st32(o_addr + c * 32, ov);
+          }
+          tmem_st_wait();
+        }
+      }
       float ps = 0.f;
 #pragma unroll
       for (int k = 0; k < 64; ++k) {
-        x[k] = exp2f(x[k] - mn);
+        x[k] = exp2f(x[k] - mref);
         ps += x[k];
       }
-      l = l * alpha + ps;
-      // fold in the previous step's P V (its MMAs are done with the P buffer too)
-      if (j > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(ofull, (j - 1) & 1))) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(tmem + lane_base + C::O_COL + c * 32, ov);
-          tmem_ld_wait();
-#pragma unroll
-          for (int d = 0; d < 32; ++d) o[c * 32 + d] = o[c * 32 + d] * alpha_prev + __uint_as_float(ov[d]);
-        }
-      }
-      alpha_prev = alpha;
+      l += ps;
+      // the P buffer is free once the previous step's P V has completed
+      if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(ofull, (j - 1) & 1))) { ok = false; break; }
       // P hi and lo, row r, 64 keys: 8 chunks of 16 B, 128-byte swizzle
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
@@ -322,16 +332,19 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(pready);
     }
+    float o[HD];
+#pragma unroll
+    for (int d = 0; d < HD; ++d) o[d] = 0.f;
     if (ok && nsteps > 0) {
       if (__all_sync(0xffffffffu, mbar_wait(ofull, (nsteps - 1) & 1))) {
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < HD / 32; ++c) {
           uint32_t ov[32];
-          tmem_ld32(tmem + lane_base + C::O_COL + c * 32, ov);
+          tmem_ld32(o_addr + c * 32, ov);
           tmem_ld_wait();
 #pragma unroll
-          for (int d = 0; d < 32; ++d) o[c * 32 + d] = o[c * 32 + d] * alpha_prev + __uint_as_float(ov[d]);
+          for (int d = 0; d < 32; ++d) o[c * 32 + d] = __uint_as_float(ov[d]);
         }
       } else {
         ok = false;
@@ -344,7 +357,7 @@ __global__ void __launch_bounds__(192, 1)
       if (a.nsplit > 1) {
         const long long grp = (long long)b * a.hkv + g;
         float* pm = a.part_ml + ((grp * a.nsplit + split) * a.QR + r) * 2;
-        pm[0] = m;
+        pm[0] = mref;
         pm[1] = l;
       }
     }
