@@ -257,7 +257,9 @@ dflash_status rmsnorm(const H* h, const Tin* x, const void* gain, T* y, int rows
 
 // ------------------------------------------------------------------ attention plan
 // Blocks of many rows (a batch of sequences) with head_dim 64 run attention on the
-// tcgen05 kernel; the rest on the mma.sync kernel.
+// tcgen05 kernel; a single block (latency-bound) and head_dim 128 (whose 64 query rows
+// per kv head would leave half of the 128-row tile idle at one CTA per SM, measured
+// slower) on the mma.sync kernel.
 bool use_attn_umma(const dflash_config& c, int M) {
   const int QR = c.block_size * (c.n_q_heads / c.n_kv_heads);
   return c.dtype == DFLASH_BF16 && c.head_dim == 64 && M > 64 && QR <= 128;

@@ -154,14 +154,20 @@ __global__ void __launch_bounds__(192, 2)
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(&kvfull[s], cnt * 2 * C::PAGE_BYTES);
-      for (int q = 0; q < cnt; ++q) {
+      // Pages past the split's last one are loaded from beyond the pool (zero fill):
+      // their scores are masked, but P = 0 must meet finite V rows.
+      if (lane == 0) mbar_arrive_expect_tx(&kvfull[s], C::PG * 2 * C::PAGE_BYTES);
+      for (int q = 0; q < C::PG; ++q) {
         const int page_q = __shfl_sync(0xffffffffu, my_page, q);
         if (lane == 0) {
           const int pg = p0 + pa + q;
           const CUtensorMap *mk, *mv;
           int row;
-          if (pg < np) {
+          if (q >= cnt) {
+            mk = &maps.k;
+            mv = &maps.v;
+            row = a.num_pages * a.hkv * kPage;   // first row past the pool
+          } else if (pg < np) {
             int page = page_q;
             if (page < 0 || page >= a.num_pages) {
               raise_error(a.err, DFLASH_DEV_BAD_INDEX);
@@ -332,28 +338,24 @@ __global__ void __launch_bounds__(192, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(pready);
     }
-    float o[HD];
+    if (ok && nsteps > 0 && !__all_sync(0xffffffffu, mbar_wait(ofull, (nsteps - 1) & 1))) ok = false;
+    if (!ok && lane == 0) raise_error(a.err, DFLASH_DEV_TIMEOUT);
+    tc_fence_after();
+    // O from TMEM 32 columns at a time (the loads are warp-wide; rows past QR skip the
+    // stores only)
 #pragma unroll
-    for (int d = 0; d < HD; ++d) o[d] = 0.f;
-    if (ok && nsteps > 0) {
-      if (__all_sync(0xffffffffu, mbar_wait(ofull, (nsteps - 1) & 1))) {
-        tc_fence_after();
+    for (int c = 0; c < HD / 32; ++c) {
+      uint32_t ov[32];
+      tmem_ld32(o_addr + c * 32, ov);
+      tmem_ld_wait();
+      if (r < a.QR && ok) {
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(o_addr + c * 32, ov);
-          tmem_ld_wait();
-#pragma unroll
-          for (int d = 0; d < 32; ++d) o[c * 32 + d] = __uint_as_float(ov[d]);
-        }
-      } else {
-        ok = false;
+        for (int d = 0; d < 32; d += 2)
+          attn_emit<bf16>(a, b, g, split, r, c * 32 + d, __uint_as_float(ov[d]),
+                          __uint_as_float(ov[d + 1]), l);
       }
     }
-    if (!ok && lane == 0) raise_error(a.err, DFLASH_DEV_TIMEOUT);
     if (r < a.QR) {
-#pragma unroll
-      for (int d = 0; d < HD; d += 2) attn_emit<bf16>(a, b, g, split, r, d, o[d], o[d + 1], l);
       if (a.nsplit > 1) {
         const long long grp = (long long)b * a.hkv + g;
         float* pm = a.part_ml + ((grp * a.nsplit + split) * a.QR + r) * 2;

@@ -39,7 +39,9 @@
  *     available from dflash_last_error().
  *   - KV cache: per drafter layer, one K pool and one V pool, each
  *     [num_pages][n_kv_heads][page_size][head_dim] (page_size = 16).  A token at cache
- *     slot s lives in page s / page_size at offset s % page_size.
+ *     slot s lives in page s / page_size at offset s % page_size.  Slots of a
+ *     sequence's last page past its context length are read (with zero weight): they
+ *     must hold finite values, e.g. a pool zeroed once at allocation.
  */
 #ifndef DFLASH_H
 #define DFLASH_H
