@@ -30,7 +30,7 @@ METRIC = "draft+verify steps/sec and tokens/sec; achieved HBM GB/s vs ~8 TB/s (1
 DEFAULT_CONFIG = "qwen3-8b-shaped-b1"
 # DRAM read + write bytes of one LM-head launch on this workload, from an ncu capture of
 # the current kernel (None until the kernel has been captured since its last change)
-LM_HEAD_TRAFFIC = 1250015696
+LM_HEAD_TRAFFIC = 1250102456
 
 
 def parse():
@@ -291,7 +291,7 @@ def run_ours(args):
         "step_hbm_gbs": sb / (ms / 1e3) / 1e9,
         "step_roofline": {"bytes": sb, "flops": fl, "t_roof_us": t_roof * 1e6,
                           "frac": t_roof / (ms / 1e3), "peak_gbs": hbm, "peak_src": src},
-        "roofline": {"kernel": "k_gemm_tc<16,EPI_ARGMAX> + k_argmax_finalize (LM head)",
+        "roofline": {"kernel": "LM-head projection with the argmax fused (EPI_ARGMAX)",
                      "bound": "hbm", "achieved": lm_gbs, "peak": hbm, "unit": "GB/s",
                      "frac": lm_gbs / hbm,
                      "traffic": LM_HEAD_TRAFFIC if w.name == DEFAULT_CONFIG else None,

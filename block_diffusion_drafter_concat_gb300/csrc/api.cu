@@ -224,7 +224,7 @@ dflash_status gemm(const H* h, const void* A, int M, int K, const WSet& w, EpiAr
   if (EPI == EPI_F32 || EPI == EPI_RESID || EPI == EPI_ARGMAX) e.N = w.rows[0];
   // two control words per tile: arrivals and publications of split pieces
   const int ctl_per_tile = 2;
-  if (g.m_blocks * g.n_tiles * ctl_per_tile > kCtlWords)
+  if (g.m_blocks * g.n_tiles * ctl_per_tile > 2 * kTileWords)
     return fail(DFLASH_EUNSUPPORTED, "GEMM with %d tiles exceeds the control words",
                 g.m_blocks * g.n_tiles);
   if constexpr (std::is_same<T, bf16>::value) {
@@ -560,6 +560,14 @@ static dflash_status head_impl(H* h, const void* hidden, int rows, float tempera
   e.inv_temp = 1.0f / temperature;
   e.want_sum = lse != nullptr;
   e.err = h->d_err;
+  if (!lse && rows <= kKeyRows && h->bf16) {
+    // greedy: the argmax is finished inside the projection (packed keys, last CTA)
+    e.am_key = reinterpret_cast<unsigned long long*>(w.ctl + kKeyWord);
+    e.am_done = w.ctl + kDoneWord;
+    e.tok_out = tokens;
+    e.max_out = max_logit;
+    return gemm<EPI_ARGMAX, T>(h, hidden, rows, h->c.d_model, ws_, e, w.gpart, w.ctl, st);
+  }
   TRY((gemm<EPI_ARGMAX, T>(h, hidden, rows, h->c.d_model, ws_, e, w.gpart, w.ctl, st)));
   const int n_tiles = ceil_div(h->c.vocab, kBM);
   return launch(k_argmax_finalize, dim3(ceil_div(rows, kRowThreads / 32)), dim3(kRowThreads), 0,
@@ -848,7 +856,7 @@ dflash_status dflash_draft_block(dflash_handle h, const int32_t* block_ids,
   Carve cv{static_cast<char*>(ws)};
   DraftWs w = carve_draft(h, cv, batch, max_pages);
   TRY(check_ws(ws, ws_bytes, cv.off));
-  if ((long long)batch * h->c.n_kv_heads > kCtlWords) return fail(DFLASH_EUNSUPPORTED, "batch too large");
+  if ((long long)batch * h->c.n_kv_heads > 2 * kTileWords) return fail(DFLASH_EUNSUPPORTED, "batch too large");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (h->bf16)
     return draft_impl<bf16>(h, block_ids, ctx_lens, page_table, max_pages, batch, num_pages,
@@ -929,7 +937,7 @@ dflash_status dflash_verify_sample(dflash_handle h, const int32_t* draft, const 
   NEED(n_accepted, "n_accepted");
   NEED(n_emitted, "n_emitted");
   const int rows = batch * h->c.block_size;
-  if (rows > 65535 || rows + batch > kCtlWords) return fail(DFLASH_EUNSUPPORTED, "batch too large");
+  if (rows > 65535 || rows + batch > 2 * kTileWords) return fail(DFLASH_EUNSUPPORTED, "batch too large");
   Carve cv{static_cast<char*>(ws)};
   VerifyWs w = carve_verify(h, cv, batch, true);
   TRY(check_ws(ws, ws_bytes, cv.off));

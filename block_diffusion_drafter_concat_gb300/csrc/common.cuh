@@ -15,7 +15,16 @@ namespace dflash {
 constexpr int kPage = 16;          // tokens per KV page
 constexpr int kBM = 128;           // weight rows per GEMM tile
 constexpr int kBK = 64;            // K elements per pipeline stage (one 128-B row)
-constexpr int kCtlWords = 1 << 16; // int32 control words at the start of a workspace
+// int32 control words at the start of a workspace, zeroed once and kept zero between
+// calls by their users: [0, kTileWords) per-tile arrival counters, [kTileWords,
+// 2*kTileWords) per-tile publication counters (split tiles of one projection; the
+// verification kernels use the same first 2*kTileWords for their own counters), then
+// one CTA counter and kKeyRows packed (max, argmax) keys of the greedy LM head.
+constexpr int kTileWords = 1 << 15;
+constexpr int kKeyRows = 1 << 14;
+constexpr int kDoneWord = 2 * kTileWords;
+constexpr int kKeyWord = 2 * kTileWords + 4;   // 16-byte aligned, u64 keys
+constexpr int kCtlWords = kKeyWord + 2 * kKeyRows;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded waits give up after 2 s
 
 typedef __nv_bfloat16 bf16;
@@ -156,6 +165,22 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ------------------------------------------------------------------ argmax keys
+// A (value, index) pair packed so that the unsigned maximum is the largest value and,
+// among equal values, the lowest index: the order-preserving bits of the float above,
+// the complemented index below.  Key 0 is below every real value.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
+  unsigned u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<unsigned long long>(u) << 32) | (0xFFFFFFFFu - static_cast<unsigned>(idx));
+}
+__device__ __forceinline__ void argmax_unkey(unsigned long long k, float& v, int& idx) {
+  unsigned u = static_cast<unsigned>(k >> 32);
+  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+  v = __uint_as_float(u);
+  idx = static_cast<int>(0xFFFFFFFFu - static_cast<unsigned>(k));
+}
 
 // ------------------------------------------------------------------ reductions
 __device__ __forceinline__ float warp_sum(float v) {

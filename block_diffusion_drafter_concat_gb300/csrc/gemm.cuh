@@ -62,6 +62,12 @@ struct EpiArgs {
   float* am_sum;
   float inv_temp;
   int want_sum;
+  // greedy LM head without partials: per-row packed keys (atomic maximum), a CTA
+  // counter; the last CTA writes tokens (and max logits) and clears both
+  unsigned long long* am_key;
+  int* am_done;
+  int* tok_out;
+  float* max_out;
   int* err;
 };
 
@@ -304,10 +310,14 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
         s = warp_sum(s);
       }
       if (lane == 0) {
-        long long o = (long long)nt * e.M + m0 + r;
-        e.am_max[o] = best;
-        e.am_idx[o] = bi;
-        e.am_sum[o] = s;
+        if (e.am_key) {
+          atomicMax(e.am_key + m0 + r, argmax_key(best, bi));
+        } else {
+          long long o = (long long)nt * e.M + m0 + r;
+          e.am_max[o] = best;
+          e.am_idx[o] = bi;
+          e.am_sum[o] = s;
+        }
       }
     }
   }
@@ -404,6 +414,29 @@ struct UnitWalk {
     locate(g);
   }
 };
+
+// Greedy LM head: after this CTA's epilogues, count it; the last CTA of the grid turns
+// the rows' packed keys into tokens (and max logits) and clears keys and counter.
+template <typename T, typename Sync>
+__device__ __forceinline__ void argmax_keys_finish(const EpiArgs<T>& e, int M, int tid, int nthr,
+                                                   int* flag, Sync sync) {
+  sync();
+  if (tid == 0) {
+    __threadfence();
+    flag[0] = (atomicAdd(e.am_done, 1) == static_cast<int>(gridDim.x) - 1);
+  }
+  sync();
+  if (!flag[0]) return;
+  __threadfence();
+  for (int m = tid; m < M; m += nthr) {
+    float v;
+    int idx;
+    argmax_unkey(atomicExch(e.am_key + m, 0ull), v, idx);
+    e.tok_out[m] = idx;
+    if (e.max_out) e.max_out[m] = v;
+  }
+  if (tid == 0) *e.am_done = 0;
+}
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(160, 1)
@@ -569,7 +602,7 @@ __global__ void __launch_bounds__(160, 1)
       // are running and wait on nothing), then sums every piece in contributor order,
       // its own straight from shared memory.
       int* arrived = g.counters + t;
-      int* published = g.counters + kCtlWords / 2 + t;
+      int* published = g.counters + kTileWords + t;
       if (tid == 0) {
         const int nc = tile_contributors(g.units, grid, g.ks, t, nullptr);
         flag[0] = (atomicAdd(arrived, 1) == nc - 1);
@@ -652,6 +685,9 @@ __global__ void __launch_bounds__(160, 1)
     }
     consumer_sync();
     u = seg_end;
+  }
+  if constexpr (EPI == EPI_ARGMAX) {
+    if (e.am_key) argmax_keys_finish(e, g.M, tid, 128, flag, consumer_sync);
   }
 }
 

@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(192, 1)
         // who arrived last.
         const int slot = (u == u0) ? 0 : 1;
         int* arrived = g.counters + t;
-        int* published = g.counters + kCtlWords / 2 + t;
+        int* published = g.counters + kTileWords + t;
         if (et == 0) {
           const int ncontrib = tile_contributors(g.units, grid, g.ks, t, nullptr);
           flag[0] = (atomicAdd(arrived, 1) == ncontrib - 1);
@@ -440,6 +440,9 @@ __global__ void __launch_bounds__(192, 1)
       }
       u = seg_end;
       ++piece;
+    }
+    if constexpr (EPI == EPI_ARGMAX) {
+      if (e.am_key) argmax_keys_finish(e, g.M, et, 128, flag, epi_sync);
     }
   }
 
