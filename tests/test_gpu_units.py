@@ -46,6 +46,24 @@ def test_lm_head_argmax_stats(small, rows):
     np.testing.assert_allclose(lse.cpu().numpy(), ref, rtol=1e-4, atol=1e-4)
 
 
+@pytest.mark.parametrize("rows", [1, 16, 37, 100, 300])
+def test_lm_head_greedy_fused_argmax(small, rows):
+    """Without lse the argmax is finished inside the projection (packed keys); two calls
+    in a row also check that the keys and the CTA counter are left cleared."""
+    w = W_SMALL
+    W = orun.host_weights(w)
+    for call in range(2):
+        h = hidden_rows(w, rows, f"h_greedy{call}")
+        tok = torch.empty(rows, dtype=torch.int32, device="cuda")
+        mx = torch.empty(rows, dtype=torch.float32, device="cuda")
+        small.drafter.lm_head_argmax(h.cuda(), tok, small.ws, mx, None, temperature=1.0)
+        torch.cuda.synchronize()
+        z = O.lm_head(orun.np64(h), W["lm_head"])
+        check_drafts(tok.cpu().numpy(), O.argmax_lowest(z), O.top2_margin(z))
+        assert rel_err(mx, z.max(axis=1)) < 1e-4
+    assert small.drafter.device_error() == 0
+
+
 @pytest.mark.parametrize("n", [1, 16, 45, 200, 513])
 def test_fuse_features(small, n):
     w = W_SMALL
