@@ -174,7 +174,8 @@ def run_ours(args):
     from workload.configs import BY_NAME
 
     build.build()
-    from block_diffusion_drafter_concat_gb300.runner import (StepRunner, lm_head_bytes,
+    from block_diffusion_drafter_concat_gb300.runner import (PREFILL_CHUNK, StepRunner,
+                                                            lm_head_bytes,
                                                             step_bytes, step_flops)
 
     rep = replicas.from_env()
@@ -211,18 +212,38 @@ def run_ours(args):
     st = torch.cuda.current_stream()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
 
-    # ---- device-resident inputs: K graph replays between events
+    # ---- device-resident inputs: K graph replays, an event between consecutive replays
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     barrier()
     torch.cuda.synchronize()
     clk = Clocks(uuid)
     ev[0].record(st)
-    for _ in range(args.steps):
+    step_ev[0].record(st)
+    for i in range(args.steps):
         r.replay()
+        step_ev[i + 1].record(st)
     ev[1].record(st)
     torch.cuda.synchronize()
     clocks = clk.stop()
     barrier()
     t = max_over_ranks(ev[0].elapsed_time(ev[1]) / 1e3)
+    per_step = sorted(step_ev[i].elapsed_time(step_ev[i + 1]) * 1e3 for i in range(args.steps))
+
+    def pct(q):
+        return per_step[min(len(per_step) - 1, int(q * len(per_step)))]
+
+    # ---- the same steps with L2 flushed before each one (256 MB written, untimed)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    k_fl = max(3, min(20, args.steps))
+    fl_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * k_fl)]
+    for i in range(k_fl):
+        flush.zero_()
+        fl_ev[2 * i].record(st)
+        r.replay()
+        fl_ev[2 * i + 1].record(st)
+    torch.cuda.synchronize()
+    fl_us = sorted(fl_ev[2 * i].elapsed_time(fl_ev[2 * i + 1]) * 1e3 for i in range(k_fl))
+    del flush
     mean_emit = float(r.n_emit.float().mean())
     value = replicas.aggregate(args.steps, rep, t)
     ms = t / args.steps * 1e3
@@ -272,6 +293,27 @@ def run_ours(args):
     if r.drafter.device_error():
         raise RuntimeError("device error during the timed region")
 
+    # ---- context prefill by injection: fuse + K/V of sequence 0's context (one chunk)
+    from workload import inputs as winputs
+    rows_pf = min(int(r.lens[0]) - w.block_size, PREFILL_CHUNK)
+    x_pf = winputs.ctx_hidden(r.w, 0, 0, rows_pf, "cuda")
+    p_pf = torch.arange(0, rows_pf)
+    s_pf = winputs.slots_for(r.w, r.table_host, 0, p_pf).to(torch.int32).cuda()
+    p_pf = p_pf.to(torch.int32).cuda()
+    for _ in range(2):
+        r.drafter.inject_kv(p_pf, s_pf, r.cache, r.ws, x_cat=x_pf)
+    k_pf = 5
+    torch.cuda.synchronize()
+    ev[4].record(st)
+    for _ in range(k_pf):
+        r.drafter.inject_kv(p_pf, s_pf, r.cache, r.ws, x_cat=x_pf)
+    ev[5].record(st)
+    torch.cuda.synchronize()
+    t_pf = ev[4].elapsed_time(ev[5]) / 1e3 / k_pf
+    pf_flops = 2.0 * rows_pf * (w.fuse_in * w.d_model + w.n_layers * 2 * w.kv_width * w.d_model)
+    if r.drafter.device_error():
+        raise RuntimeError("device error during the prefill timing")
+
     hbm, bf16_tf, src = peaks()
     sb, fl = step_bytes(w), step_flops(w)
     t_roof = max(sb / (hbm * 1e9), fl / (bf16_tf * 1e12))
@@ -299,6 +341,13 @@ def run_ours(args):
                      "us_per_launch": t_lm * 1e6},
         "e2e": {"value": replicas.aggregate(k_e2e, rep, te), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
+        "step_us": {"median": pct(0.5), "p10": pct(0.1), "p90": pct(0.9)},
+        "l2_flushed": {"ms_per_step": statistics.median(fl_us) / 1e3,
+                       "value": 1e6 / statistics.median(fl_us), "unit": "steps/s",
+                       "note": f"256 MB written before each of {k_fl} timed steps"},
+        "prefill": {"rows": rows_pf, "us": t_pf * 1e6, "rows_per_s": rows_pf / t_pf,
+                    "tflops": pf_flops / t_pf / 1e12,
+                    "note": "fuse + K/V injection of sequence 0's context, all layers"},
         "gpu_launches": r.launches * args.steps,
         "launches_per_step": r.launches,
         "clocks": clocks,

@@ -221,7 +221,8 @@ dflash_status gemm(const H* h, const void* A, int M, int K, const WSet& w, EpiAr
   g.part = part;
   g.counters = ctr;
   e.M = M;
-  if (EPI == EPI_F32 || EPI == EPI_RESID || EPI == EPI_ARGMAX) e.N = w.rows[0];
+  if (EPI == EPI_F32 || EPI == EPI_RESID || EPI == EPI_ARGMAX || EPI == EPI_ARGKEY)
+    e.N = w.rows[0];
   // two control words per tile: arrivals and publications of split pieces
   const int ctl_per_tile = 2;
   if (g.m_blocks * g.n_tiles * ctl_per_tile > 2 * kTileWords)
@@ -560,13 +561,15 @@ static dflash_status head_impl(H* h, const void* hidden, int rows, float tempera
   e.inv_temp = 1.0f / temperature;
   e.want_sum = lse != nullptr;
   e.err = h->d_err;
-  if (!lse && rows <= kKeyRows && h->bf16) {
-    // greedy: the argmax is finished inside the projection (packed keys, last CTA)
+  if (!lse && rows <= 128 && h->bf16) {
+    // greedy, one or a few blocks: the argmax is finished inside the projection (packed
+    // keys, last CTA).  With more rows the per-row atomics contend (every n-tile hits
+    // every row's key), so tile partials and a reduction launch are used instead.
     e.am_key = reinterpret_cast<unsigned long long*>(w.ctl + kKeyWord);
     e.am_done = w.ctl + kDoneWord;
     e.tok_out = tokens;
     e.max_out = max_logit;
-    return gemm<EPI_ARGMAX, T>(h, hidden, rows, h->c.d_model, ws_, e, w.gpart, w.ctl, st);
+    return gemm<EPI_ARGKEY, T>(h, hidden, rows, h->c.d_model, ws_, e, w.gpart, w.ctl, st);
   }
   TRY((gemm<EPI_ARGMAX, T>(h, hidden, rows, h->c.d_model, ws_, e, w.gpart, w.ctl, st)));
   const int n_tiles = ceil_div(h->c.vocab, kBM);

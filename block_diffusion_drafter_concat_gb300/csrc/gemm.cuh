@@ -28,7 +28,8 @@ enum Epi : int {
   EPI_KV = 2,     // segments k0 | v0 | k1 | v1 ...: RoPE on k, scatter into cache pages
   EPI_RESID = 3,  // x[m, n] += v (fp32 residual stream)
   EPI_SWIGLU = 4, // paired tiles (64 gate rows | 64 up rows): act = silu(g) * u
-  EPI_ARGMAX = 5  // per-tile (max, argmax, sum exp) of each row for the LM head
+  EPI_ARGMAX = 5, // per-tile (max, argmax, sum exp) of each row for the LM head
+  EPI_ARGKEY = 6  // greedy LM head: per-row packed (max, argmax) keys, finished in-kernel
 };
 
 struct WMaps {
@@ -310,15 +311,24 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
         s = warp_sum(s);
       }
       if (lane == 0) {
-        if (e.am_key) {
-          atomicMax(e.am_key + m0 + r, argmax_key(best, bi));
-        } else {
-          long long o = (long long)nt * e.M + m0 + r;
-          e.am_max[o] = best;
-          e.am_idx[o] = bi;
-          e.am_sum[o] = s;
-        }
+        long long o = (long long)nt * e.M + m0 + r;
+        e.am_max[o] = best;
+        e.am_idx[o] = bi;
+        e.am_sum[o] = s;
       }
+    }
+  } else if constexpr (EPI == EPI_ARGKEY) {
+    // one warp per row: (max, argmax) of the tile's columns folded into the row's key
+    const int nc = min(kBM, e.N - nt * kBM);
+    for (int r = warp; r < mr; r += nw) {
+      float best = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int c = lane; c < nc; c += 32) {
+        float v = Cs[r * pitch + c];
+        if (v > best) { best = v; bi = nt * kBM + c; }
+      }
+      warp_argmax(best, bi);
+      if (lane == 0) atomicMax(e.am_key + m0 + r, argmax_key(best, bi));
     }
   }
 }
@@ -686,9 +696,7 @@ __global__ void __launch_bounds__(160, 1)
     consumer_sync();
     u = seg_end;
   }
-  if constexpr (EPI == EPI_ARGMAX) {
-    if (e.am_key) argmax_keys_finish(e, g.M, tid, 128, flag, consumer_sync);
-  }
+  if constexpr (EPI == EPI_ARGKEY) argmax_keys_finish(e, g.M, tid, 128, flag, consumer_sync);
 }
 
 // ------------------------------------------------------------------- fp32 SIMT kernel

@@ -14,6 +14,7 @@ static dflash_status by_epi(int epi, const CUtensorMap& tmA, const WMaps& wm, co
     case EPI_RESID: return launch_tc<BN, EPI_RESID>(tmA, wm, g, grid, e, st);
     case EPI_SWIGLU: return launch_tc<BN, EPI_SWIGLU>(tmA, wm, g, grid, e, st);
     case EPI_ARGMAX: return launch_tc<BN, EPI_ARGMAX>(tmA, wm, g, grid, e, st);
+    case EPI_ARGKEY: return launch_tc<BN, EPI_ARGKEY>(tmA, wm, g, grid, e, st);
   }
   return fail(DFLASH_EUNSUPPORTED, "unknown epilogue %d", epi);
 }

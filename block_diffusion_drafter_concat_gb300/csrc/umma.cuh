@@ -441,9 +441,7 @@ __global__ void __launch_bounds__(192, 1)
       u = seg_end;
       ++piece;
     }
-    if constexpr (EPI == EPI_ARGMAX) {
-      if (e.am_key) argmax_keys_finish(e, g.M, et, 128, flag, epi_sync);
-    }
+    if constexpr (EPI == EPI_ARGKEY) argmax_keys_finish(e, g.M, et, 128, flag, epi_sync);
   }
 
   // ---- teardown: every role is here, every MMA has completed; free TMEM
