@@ -294,41 +294,57 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
         }
       }
     }
-  } else if constexpr (EPI == EPI_ARGMAX) {
-    // one warp per row: lanes cover the 128 columns, then a (max, idx) shuffle reduce
+  } else if constexpr (EPI == EPI_ARGMAX || EPI == EPI_ARGKEY) {
+    // Four threads per row, every row of the chunk at once (a warp per row would walk
+    // its rows one after another, each behind a five-level shuffle chain).  Thread
+    // `sub` of a row takes columns sub, sub + 4, ... (conflict-free: the four threads
+    // and eight rows of a warp hit 32 distinct banks), then (max, lowest index) and the
+    // sum of exponentials are merged over the row's four threads with two shuffles.
     const int nc = min(kBM, e.N - nt * kBM);
-    for (int r = warp; r < mr; r += nw) {
+    const int sub = tid & 3;
+    for (int rb = 0; rb < mr; rb += nthr >> 2) {
+      const int r = rb + (tid >> 2);
+      const bool active = r < mr;
       float best = -INFINITY;
       int bi = 0x7fffffff;
-      for (int c = lane; c < nc; c += 32) {
-        float v = Cs[r * pitch + c];
-        if (v > best) { best = v; bi = nt * kBM + c; }
+      if (active) {
+#pragma unroll 8
+        for (int j = 0; j < kBM / 4; ++j) {
+          const int c = sub + 4 * j;
+          if (c < nc) {
+            const float v = Cs[r * pitch + c];
+            if (v > best) { best = v; bi = nt * kBM + c; }
+          }
+        }
       }
-      warp_argmax(best, bi);
-      float s = 0.f;
-      if (e.want_sum) {
-        for (int c = lane; c < nc; c += 32) s += __expf((Cs[r * pitch + c] - best) * e.inv_temp);
-        s = warp_sum(s);
+#pragma unroll
+      for (int o = 1; o <= 2; o <<= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
       }
-      if (lane == 0) {
-        long long o = (long long)nt * e.M + m0 + r;
-        e.am_max[o] = best;
-        e.am_idx[o] = bi;
-        e.am_sum[o] = s;
+      if constexpr (EPI == EPI_ARGMAX) {
+        float sum = 0.f;
+        if (e.want_sum) {
+          if (active) {
+#pragma unroll 8
+            for (int j = 0; j < kBM / 4; ++j) {
+              const int c = sub + 4 * j;
+              if (c < nc) sum += __expf((Cs[r * pitch + c] - best) * e.inv_temp);
+            }
+          }
+          sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+          sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        }
+        if (active && sub == 0) {
+          const long long o = (long long)nt * e.M + m0 + r;
+          e.am_max[o] = best;
+          e.am_idx[o] = bi;
+          e.am_sum[o] = sum;
+        }
+      } else {
+        if (active && sub == 0) atomicMax(e.am_key + m0 + r, argmax_key(best, bi));
       }
-    }
-  } else if constexpr (EPI == EPI_ARGKEY) {
-    // one warp per row: (max, argmax) of the tile's columns folded into the row's key
-    const int nc = min(kBM, e.N - nt * kBM);
-    for (int r = warp; r < mr; r += nw) {
-      float best = -INFINITY;
-      int bi = 0x7fffffff;
-      for (int c = lane; c < nc; c += 32) {
-        float v = Cs[r * pitch + c];
-        if (v > best) { best = v; bi = nt * kBM + c; }
-      }
-      warp_argmax(best, bi);
-      if (lane == 0) atomicMax(e.am_key + m0 + r, argmax_key(best, bi));
     }
   }
 }
