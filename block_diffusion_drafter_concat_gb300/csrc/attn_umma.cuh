@@ -157,37 +157,37 @@ __global__ void __launch_bounds__(192, 2)
       // Pages past the split's last one are loaded from beyond the pool (zero fill):
       // their scores are masked, but P = 0 must meet finite V rows.
       if (lane == 0) mbar_arrive_expect_tx(&kvfull[s], C::PG * 2 * C::PAGE_BYTES);
-      for (int q = 0; q < C::PG; ++q) {
-        const int page_q = __shfl_sync(0xffffffffu, my_page, q);
-        if (lane == 0) {
-          const int pg = p0 + pa + q;
-          const CUtensorMap *mk, *mv;
-          int row;
-          if (q >= cnt) {
-            mk = &maps.k;
-            mv = &maps.v;
-            row = a.num_pages * a.hkv * kPage;   // first row past the pool
-          } else if (pg < np) {
-            int page = page_q;
-            if (page < 0 || page >= a.num_pages) {
-              raise_error(a.err, DFLASH_DEV_BAD_INDEX);
-              page = 0;
-            }
-            mk = &maps.k;
-            mv = &maps.v;
-            row = (page * a.hkv + g) * kPage;
-          } else {
-            mk = &maps.kb;
-            mv = &maps.vb;
-            row = (b * a.hkv + g) * a.S;
+      __syncwarp();
+      // lane q issues page q's copies (the expected bytes are set above)
+      if (lane < C::PG) {
+        const int q = lane;
+        const int pg = p0 + pa + q;
+        const CUtensorMap *mk, *mv;
+        int row;
+        if (q >= cnt) {
+          mk = &maps.k;
+          mv = &maps.v;
+          row = a.num_pages * a.hkv * kPage;   // first row past the pool
+        } else if (pg < np) {
+          int page = my_page;
+          if (page < 0 || page >= a.num_pages) {
+            raise_error(a.err, DFLASH_DEV_BAD_INDEX);
+            page = 0;
           }
-          uint8_t* kd = stages + s * C::STAGE + q * (kPage * 128);
-          uint8_t* vd = kd + C::KV_BYTES;
+          mk = &maps.k;
+          mv = &maps.v;
+          row = (page * a.hkv + g) * kPage;
+        } else {
+          mk = &maps.kb;
+          mv = &maps.vb;
+          row = (b * a.hkv + g) * a.S;
+        }
+        uint8_t* kd = stages + s * C::STAGE + q * (kPage * 128);
+        uint8_t* vd = kd + C::KV_BYTES;
 #pragma unroll
-          for (int kb = 0; kb < C::KB; ++kb) {
-            tma_load_2d(kd + kb * C::KV_BLOCK, mk, &kvfull[s], kb * 64, row);
-            tma_load_2d(vd + kb * C::KV_BLOCK, mv, &kvfull[s], kb * 64, row);
-          }
+        for (int kb = 0; kb < C::KB; ++kb) {
+          tma_load_2d(kd + kb * C::KV_BLOCK, mk, &kvfull[s], kb * 64, row);
+          tma_load_2d(vd + kb * C::KV_BLOCK, mv, &kvfull[s], kb * 64, row);
         }
       }
       issued = j + 1;
