@@ -167,6 +167,35 @@ def test_device_errors_are_reported_not_trapped(small):
     assert d.device_error() == 0
 
 
+def test_device_errors_on_the_tcgen05_paths():
+    """The same device checks on blocks of 96 rows with head_dim 64: projections and
+    attention on the tcgen05 kernels (slot, page-id and position checks)."""
+    from block_diffusion_drafter_concat_gb300.runner import StepRunner
+    w = configs.small_bf16(name="err-hd64-b6", d_model=384, n_q_heads=16, n_kv_heads=2,
+                           head_dim=64, ffn_dim=384, vocab=2176, batch=6,
+                           ctx_range=(40, 200), seed=21)
+    r = StepRunner(w)
+    d = r.drafter
+    bad_table = r.page_table.clone()
+    bad_table[2, 1] = r.cache.num_pages + 7
+    d.draft_block(r.block_ids, r.ctx_lens, bad_table, r.cache, r.hidden, r.ws)
+    assert d.device_error() == 1
+    d.workspace_init(r.ws)
+    bad_slots = r.slots.clone()
+    bad_slots[50] = -4
+    d.inject_kv(r.positions, bad_slots, r.cache, r.ws, x_cat=r.x_step)
+    assert d.device_error() == 1
+    d.workspace_init(r.ws)
+    bad_pos = r.positions.clone()
+    bad_pos[17] = w.max_position + 2
+    d.inject_kv(bad_pos, r.slots, r.cache, r.ws, x_cat=r.x_step)
+    assert d.device_error() == 2
+    d.workspace_init(r.ws)
+    r.step()
+    torch.cuda.synchronize()
+    assert d.device_error() == 0
+
+
 def test_host_validation_statuses(small):
     r = small
     d = r.drafter
