@@ -276,22 +276,35 @@ __global__ void __launch_bounds__(192, 2)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sfree[sb]);
-      // mask keys past each page's valid count, scale to the log2 domain
+      // Raw scores; keys past a page's valid count are masked only in steps that have
+      // any (the last steps of a split): the common step is four full pages.  The max is
+      // taken on raw scores (the scale is positive) and the scale folded into one FMA
+      // with the reference below.
       float x[64];
-      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        x[k] = __uint_as_float(s0[k]);
+        x[32 + k] = __uint_as_float(s1[k]);
+      }
+      int vq[C::PG];
+      bool full = true;
 #pragma unroll
       for (int q = 0; q < C::PG; ++q) {
         const int pg = p0 + j * C::PG + q;
-        const int valid = pg >= p1 ? 0 : (pg < np) ? min(kPage, T - pg * kPage) : a.S;
-#pragma unroll
-        for (int k = 0; k < kPage; ++k) {
-          const int key = q * kPage + k;
-          const uint32_t raw = key < 32 ? s0[key & 31] : s1[key & 31];
-          const float v = k < valid ? __uint_as_float(raw) * sc : -INFINITY;
-          x[key] = v;
-          mx = fmaxf(mx, v);
-        }
+        vq[q] = pg >= p1 ? 0 : (pg < np) ? min(kPage, T - pg * kPage) : a.S;
+        full = full && vq[q] == kPage;
       }
+      if (!full) {
+#pragma unroll
+        for (int q = 0; q < C::PG; ++q)
+#pragma unroll
+          for (int k = 0; k < kPage; ++k)
+            if (k >= vq[q]) x[q * kPage + k] = -INFINITY;
+      }
+      float rmx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) rmx = fmaxf(rmx, x[k]);
+      const float mx = rmx * sc;
       const bool move = mx > mref + 8.f;
       if (__any_sync(0xffffffffu, move)) {
         const float mn = move ? mx : mref;
@@ -315,9 +328,10 @@ __global__ void __launch_bounds__(192, 2)
         }
       }
       float ps = 0.f;
+      const float nref = -mref;
 #pragma unroll
       for (int k = 0; k < 64; ++k) {
-        x[k] = exp2f(x[k] - mref);
+        x[k] = exp2f(fmaf(x[k], sc, nref));
         ps += x[k];
       }
       l += ps;
