@@ -258,31 +258,35 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         mma_bf16(sacc[0], qf[kk], kf[0], kf[1]);
         mma_bf16(sacc[1], qf[kk], kf[2], kf[3]);
       }
-      // scores -> log2 domain, mask keys past `valid`
+      // mask keys past `valid` (only a page's last keys can be), row max on raw scores
+      // (the scale is positive), then scale and reference in one FMA per key: the log2
+      // domain probabilities 2^(s*sc - m)
+      if (valid < kPage) {
 #pragma unroll
-      for (int n = 0; n < 2; ++n)
+        for (int n = 0; n < 2; ++n)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          int key = n * 8 + 2 * t4 + (c & 1);
-          sacc[n][c] = key < valid ? sacc[n][c] * sc : -INFINITY;
-        }
+          for (int c = 0; c < 4; ++c) {
+            const int key = n * 8 + 2 * t4 + (c & 1);
+            if (key >= valid) sacc[n][c] = -INFINITY;
+          }
+      }
       float mx0 = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
       float mx1 = fmaxf(fmaxf(sacc[0][2], sacc[0][3]), fmaxf(sacc[1][2], sacc[1][3]));
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
+      const float nm0 = fmaxf(m0, mx0 * sc), nm1 = fmaxf(m1, mx1 * sc);
       const float al0 = exp2f(m0 - nm0), al1 = exp2f(m1 - nm1);
       m0 = nm0;
       m1 = nm1;
       float p[2][4];
 #pragma unroll
       for (int n = 0; n < 2; ++n) {
-        p[n][0] = exp2f(sacc[n][0] - nm0);
-        p[n][1] = exp2f(sacc[n][1] - nm0);
-        p[n][2] = exp2f(sacc[n][2] - nm1);
-        p[n][3] = exp2f(sacc[n][3] - nm1);
+        p[n][0] = exp2f(fmaf(sacc[n][0], sc, -nm0));
+        p[n][1] = exp2f(fmaf(sacc[n][1], sc, -nm0));
+        p[n][2] = exp2f(fmaf(sacc[n][2], sc, -nm1));
+        p[n][3] = exp2f(fmaf(sacc[n][3], sc, -nm1));
       }
       l0 = l0 * al0 + p[0][0] + p[0][1] + p[1][0] + p[1][1];
       l1 = l1 * al1 + p[0][2] + p[0][3] + p[1][2] + p[1][3];
