@@ -6,14 +6,17 @@
 //   S = Q K^T     N = 64 keys (four 16-key pages), K = head_dim;   fp32 in TMEM
 //   O += P V      N = head_dim, K = 64 keys, P as a bf16 pair hi + lo (two MMAs)
 // Q and the K/V pages arrive by TMA with the 128-byte swizzle (K pages are K-major
-// operands, V pages MN-major ones, exactly as they sit in the cache); P is written to
-// shared memory by the softmax warps in the K-major swizzled layout.
+// operands, V pages MN-major ones, exactly as they sit in the cache).  P stays in
+// tensor memory: the softmax warps write it over the S columns it was computed from
+// (hi in the first 32, lo in the last 32) and the P V MMA reads its A operand there.
 //
 // Warp roles (192 threads):
 //   warp 0      TMA producer: Q once, then four pages of K and V per ring stage
-//   warp 1      allocates TMEM (S double buffer 2 x 64 columns + O, head_dim columns)
-//               and issues the MMAs from one thread: S of step j+1 is computed while
-//               the softmax warps work on step j
+//   warp 1      allocates TMEM (S/P double buffer 2 x 64 columns + O, head_dim
+//               columns) and issues the MMAs from one thread: S of step j+1 is
+//               computed while the softmax warps work on step j.  MMAs from one thread
+//               run in issue order, so S of step j+2 (issued after P V of step j)
+//               cannot overwrite P of step j before it has been read.
 //   warps 2..5  one query row per thread (TMEM lane): read S, mask, exponentiate
 //               against a reference maximum in the log2 domain, write P; O accumulates
 //               in TMEM across steps and is rescaled in place only when the reference
@@ -35,8 +38,31 @@ __device__ __forceinline__ uint64_t umma_desc_sw128_lbo(uint32_t saddr, uint32_t
          (static_cast<uint64_t>(2) << 61);
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+// D (+)= A B with A read from tensor memory (lane = row, two bf16 per column, K along
+// the columns) and B from a shared-memory descriptor.
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 2^x by the hardware approximation, subnormal results flushed to zero (the
+// probabilities here are relative to a reference at most 2^8 below the row maximum, so
+// a flushed value is below 2^-118 of the row's largest term).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
 }
 
 template <int HD>
@@ -44,17 +70,16 @@ struct AuCfg {
   static constexpr int KT = 64;                    // keys per step
   static constexpr int PG = KT / kPage;            // pages per step
   static constexpr int KB = HD / 64;               // 64-column blocks of a head
-  static constexpr int NS = HD == 64 ? 3 : 2;      // ring stages
+  static constexpr int NS = HD == 64 ? 4 : 2;      // ring stages
   static constexpr int Q_BYTES = 128 * HD * 2;
   static constexpr int KV_BLOCK = KT * 128;        // one 64-column block of K or V
   static constexpr int KV_BYTES = KB * KV_BLOCK;
   static constexpr int STAGE = 2 * KV_BYTES;       // K then V
   static constexpr int PAGE_BYTES = kPage * HD * 2;  // one page of K (or V)
-  static constexpr int P_BYTES = 128 * KT * 2;     // one bf16 P tile
-  static constexpr int NBAR = 2 * NS + 8;
-  static constexpr int SMEM = 1024 + Q_BYTES + NS * STAGE + 2 * P_BYTES + NBAR * 8 + 16;
+  static constexpr int NBAR = 2 * NS + 7;
+  static constexpr int SMEM = 1024 + Q_BYTES + NS * STAGE + NBAR * 8 + 16;
   static constexpr int TMEM_COLS = 256;
-  static constexpr int O_COL = 2 * KT;             // O_j columns [128, 128 + HD)
+  static constexpr int O_COL = 2 * KT;             // O: columns [128, 128 + HD)
   static constexpr int THREADS = 192;
   static constexpr uint32_t IDESC_S = umma_idesc_bf16<128, KT>();
   static constexpr uint32_t IDESC_O = umma_idesc_bf16<128, HD>() | (1u << 16);  // B MN-major
@@ -71,14 +96,12 @@ __global__ void __launch_bounds__(192, 2)
                                              ~uintptr_t(1023));
   uint8_t* sq = smem;                                   // Q: KB blocks of [128][64]
   uint8_t* stages = sq + C::Q_BYTES;                    // K blocks, then V blocks
-  uint8_t* sp = stages + C::NS * C::STAGE;              // P hi, P lo: [128][64 keys]
-  uint64_t* kvfull = reinterpret_cast<uint64_t*>(sp + 2 * C::P_BYTES);
+  uint64_t* kvfull = reinterpret_cast<uint64_t*>(stages + C::NS * C::STAGE);
   uint64_t* kvempty = kvfull + C::NS;
   uint64_t* qfull = kvempty + C::NS;
-  uint64_t* sfull = qfull + 1;    // [2]
-  uint64_t* sfree = sfull + 2;    // [2]
-  uint64_t* pready = sfree + 2;
-  uint64_t* ofull = pready + 1;
+  uint64_t* sfull = qfull + 1;    // [2] S of a step is in TMEM
+  uint64_t* pready = sfull + 2;   // [2] P of a step is in TMEM (over its S)
+  uint64_t* ofull = pready + 2;
   uint64_t* done = ofull + 1;
   uint32_t* tbase = reinterpret_cast<uint32_t*>(done + 1);
 
@@ -107,9 +130,8 @@ __global__ void __launch_bounds__(192, 2)
     mbar_init(qfull, 1);
     for (int k = 0; k < 2; ++k) {
       mbar_init(&sfull[k], 1);
-      mbar_init(&sfree[k], 4);
+      mbar_init(&pready[k], 4);
     }
-    mbar_init(pready, 4);
     mbar_init(ofull, 1);
     mbar_init(done, 1);
     mbar_fence_init();
@@ -208,8 +230,8 @@ __global__ void __launch_bounds__(192, 2)
       const uint32_t qa = smem_u32(sq);
       auto issue_s = [&](int j) {
         const int s = j % C::NS, sb = j & 1;
+        // buffer sb last held P of step j-2, read by the P V MMA issued before this one
         if (!mbar_wait(&kvfull[s], (j / C::NS) & 1)) return false;
-        if (j >= 2 && !mbar_wait(&sfree[sb], ((j >> 1) - 1) & 1)) return false;
         tc_fence_after();
         const uint32_t kbase = smem_u32(stages + s * C::STAGE);
         const uint32_t d = tmem + static_cast<uint32_t>(sb * C::KT);
@@ -225,21 +247,21 @@ __global__ void __launch_bounds__(192, 2)
       if (ok && nsteps > 0) ok = issue_s(0);
       for (int j = 0; j < nsteps && ok; ++j) {
         if (j + 1 < nsteps && !issue_s(j + 1)) { ok = false; break; }
-        if (!mbar_wait(pready, j & 1)) { ok = false; break; }
+        if (!mbar_wait(&pready[j & 1], (j >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const int s = j % C::NS;
         const uint32_t vbase = smem_u32(stages + s * C::STAGE) + C::KV_BYTES;
         const uint32_t d = tmem + C::O_COL;
+        const uint32_t pt = tmem + static_cast<uint32_t>((j & 1) * C::KT);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const uint32_t pbase = smem_u32(sp + h * C::P_BYTES);
 #pragma unroll
           for (int kk = 0; kk < C::KT / 16; ++kk) {
-            const uint64_t ad = umma_desc_sw128(pbase + kk * 32);
+            // P: 16 keys = 8 columns of bf16 pairs; hi then lo, 32 columns each
             // V: MN-major (head dims contiguous), 8-key groups 1024 B apart, 64-column
             // blocks of the head KV_BLOCK apart; 16 keys per MMA = two groups
             const uint64_t bd = umma_desc_sw128_lbo(vbase + kk * 2048, C::KV_BLOCK, 1024);
-            umma_bf16(d, ad, bd, C::IDESC_O, (j | h | kk) != 0);
+            umma_bf16_ta(d, pt + h * (C::KT / 2) + kk * 8, bd, C::IDESC_O, (j | h | kk) != 0);
           }
         }
         umma_commit(ofull);
@@ -267,15 +289,13 @@ __global__ void __launch_bounds__(192, 2)
     bool ok = true;
     for (int j = 0; j < nsteps && ok; ++j) {
       const int sb = j & 1;
+      const uint32_t s_addr = tmem + lane_base + static_cast<uint32_t>(sb * C::KT);
       if (!__all_sync(0xffffffffu, mbar_wait(&sfull[sb], (j >> 1) & 1))) { ok = false; break; }
       tc_fence_after();
       uint32_t s0[32], s1[32];
-      tmem_ld32(tmem + lane_base + sb * C::KT, s0);
-      tmem_ld32(tmem + lane_base + sb * C::KT + 32, s1);
+      tmem_ld32(s_addr, s0);
+      tmem_ld32(s_addr + 32, s1);
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sfree[sb]);
       // Raw scores; keys past a page's valid count are masked only in steps that have
       // any (the last steps of a split): the common step is four full pages.  The max is
       // taken on raw scores (the scale is positive) and the scale folded into one FMA
@@ -301,9 +321,16 @@ __global__ void __launch_bounds__(192, 2)
           for (int k = 0; k < kPage; ++k)
             if (k >= vq[q]) x[q * kPage + k] = -INFINITY;
       }
-      float rmx = -INFINITY;
+      // row max as a tree of three-input maxima (depth 4, not a 64-long chain)
+      float t3[22], u3[8];
 #pragma unroll
-      for (int k = 0; k < 64; ++k) rmx = fmaxf(rmx, x[k]);
+      for (int i = 0; i < 21; ++i) t3[i] = fmax3(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+      t3[21] = x[63];
+#pragma unroll
+      for (int i = 0; i < 7; ++i) u3[i] = fmax3(t3[3 * i], t3[3 * i + 1], t3[3 * i + 2]);
+      u3[7] = t3[21];
+      const float rmx = fmax3(fmax3(u3[0], u3[1], u3[2]), fmax3(u3[3], u3[4], u3[5]),
+                              fmaxf(u3[6], u3[7]));
       const float mx = rmx * sc;
       const bool move = mx > mref + 8.f;
       if (__any_sync(0xffffffffu, move)) {
@@ -327,30 +354,29 @@ __global__ void __launch_bounds__(192, 2)
           tmem_st_wait();
         }
       }
-      float ps = 0.f;
       const float nref = -mref;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < 64; ++k) {
-        x[k] = exp2f(fmaf(x[k], sc, nref));
-        ps += x[k];
+        x[k] = ex2_ftz(fmaf(x[k], sc, nref));
+        ps[k & 3] += x[k];
       }
-      l += ps;
-      // the P buffer is free once the previous step's P V has completed
+      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      // P over this step's S columns: hi pairs in the first 32, lo pairs in the last 32
+      {
+        uint32_t hi[32], lo[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) split_bf16x2(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
+        tmem_st32(s_addr, hi);
+        tmem_st32(s_addr + 32, lo);
+      }
+      tmem_st_wait();
+      // Keep the softmax at most one P V ahead: the ofull phases seen by the waits here,
+      // in the rescale above and after the loop are then never ambiguous.
       if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(ofull, (j - 1) & 1))) { ok = false; break; }
-      // P hi and lo, row r, 64 keys: 8 chunks of 16 B, 128-byte swizzle
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) split_bf16x2(x[ch * 8 + 2 * e], x[ch * 8 + 2 * e + 1], hi[e], lo[e]);
-        const int off = r * 128 + ((ch ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(sp + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(sp + C::P_BYTES + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      }
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(pready);
+      if (lane == 0) mbar_arrive(&pready[sb]);
     }
     if (ok && nsteps > 0 && !__all_sync(0xffffffffu, mbar_wait(ofull, (nsteps - 1) & 1))) ok = false;
     if (!ok && lane == 0) raise_error(a.err, DFLASH_DEV_TIMEOUT);
