@@ -20,7 +20,7 @@
 //   warps 2..5  one query row per thread (TMEM lane): read S, mask, exponentiate
 //               against a reference maximum in the log2 domain, write P; O accumulates
 //               in TMEM across steps and is rescaled in place only when the reference
-//               moves (by more than 8)
+//               moves (when a probability could exceed 2^8)
 // Every wait is bounded; a role whose wait gives up raises the error word and stops.
 #pragma once
 
@@ -57,6 +57,62 @@ __device__ __forceinline__ float ex2_ftz(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Paired fp32 arithmetic (two lanes of a 64-bit register pair per instruction).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// Probabilities 2^(x*sc - mref) of 64 scores in place; returns their sum (four partial
+// sums, added pairwise).
+__device__ __forceinline__ float exp2_row64(float (&x)[64], float sc, float nref) {
+  const uint64_t sc2 = f2_pack(sc, sc), nr2 = f2_pack(nref, nref);
+  uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    float t0, t1;
+    f2_unpack(f2_fma(f2_pack(x[2 * e], x[2 * e + 1]), sc2, nr2), t0, t1);
+    x[2 * e] = ex2_ftz(t0);
+    x[2 * e + 1] = ex2_ftz(t1);
+    const uint64_t pp = f2_pack(x[2 * e], x[2 * e + 1]);
+    if (e & 1) acc1 = f2_add(acc1, pp);
+    else acc0 = f2_add(acc0, pp);
+  }
+  float a0, a1, b0, b1;
+  f2_unpack(acc0, a0, a1);
+  f2_unpack(acc1, b0, b1);
+  return (a0 + a1) + (b0 + b1);
+}
+
+// bf16 pair hi (round to nearest even) and the pair of residuals lo = bf16(x - hi).
+__device__ __forceinline__ void split_bf16x2_f2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  hi = *reinterpret_cast<uint32_t*>(&h);
+  float r0, r1;
+  f2_unpack(f2_sub(f2_pack(a, b), f2_pack(hf.x, hf.y)), r0, r1);
+  lo = pack_bf16x2(r0, r1);
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -282,9 +338,9 @@ __global__ void __launch_bounds__(192, 2)
     const uint32_t o_addr = tmem + lane_base + C::O_COL;
     const float sc = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
     // Reference maximum in the log2 domain: probabilities are 2^(s - mref), O and l
-    // accumulate against it (O in TMEM, by the MMAs).  mref moves only when a score
-    // exceeds it by more than 8 (a factor 256 stays well inside fp32), so O is rescaled
-    // in TMEM rarely; the result does not depend on the reference.
+    // accumulate against it (O in TMEM, by the MMAs).  mref moves (to the row max) only
+    // when a step's probabilities could exceed 2^8, which stays well inside fp32, so O
+    // is rescaled in TMEM rarely; the result does not depend on the reference.
     float mref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nsteps && ok; ++j) {
@@ -314,59 +370,78 @@ __global__ void __launch_bounds__(192, 2)
         vq[q] = pg >= p1 ? 0 : (pg < np) ? min(kPage, T - pg * kPage) : a.S;
         full = full && vq[q] == kPage;
       }
-      if (!full) {
-#pragma unroll
-        for (int q = 0; q < C::PG; ++q)
-#pragma unroll
-          for (int k = 0; k < kPage; ++k)
-            if (k >= vq[q]) x[q * kPage + k] = -INFINITY;
+      // Fast path (full steps after the first): exponentiate against the current
+      // reference without a row max; the reference only has to move when a probability
+      // could exceed 2^8, and a row sum <= 2^8 rules that out.  Otherwise (and on the
+      // first step and masked steps) S is read again and the reference moved to the
+      // row max.
+      float ps = 0.f;
+      bool slow = j == 0 || !full;
+      bool tried = false;
+      if (!slow) {
+        tried = true;
+        ps = exp2_row64(x, sc, -mref);
+        slow = __any_sync(0xffffffffu, !(ps <= 256.f));
       }
-      // row max as a tree of three-input maxima (depth 4, not a 64-long chain)
-      float t3[22], u3[8];
+      if (slow) {
+        if (tried) {
+          tmem_ld32(s_addr, s0);
+          tmem_ld32(s_addr + 32, s1);
+          tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 21; ++i) t3[i] = fmax3(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
-      t3[21] = x[63];
-#pragma unroll
-      for (int i = 0; i < 7; ++i) u3[i] = fmax3(t3[3 * i], t3[3 * i + 1], t3[3 * i + 2]);
-      u3[7] = t3[21];
-      const float rmx = fmax3(fmax3(u3[0], u3[1], u3[2]), fmax3(u3[3], u3[4], u3[5]),
-                              fmaxf(u3[6], u3[7]));
-      const float mx = rmx * sc;
-      const bool move = mx > mref + 8.f;
-      if (__any_sync(0xffffffffu, move)) {
-        const float mn = move ? mx : mref;
-        const float alpha = exp2f(mref - mn);         // 0 on the first step
-        l *= alpha;
-        mref = mn;
-        if (j > 0) {
-          // the previous step's P V must have landed before O is rescaled in place
-          if (!__all_sync(0xffffffffu, mbar_wait(ofull, (j - 1) & 1))) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(o_addr + c * 32, ov);
-            tmem_ld_wait();
-#pragma unroll
-            for (int d = 0; d < 32; ++d) ov[d] = __float_as_uint(__uint_as_float(ov[d]) * alpha);
-            tmem_st32(o_addr + c * 32, ov);
+          for (int k = 0; k < 32; ++k) {
+            x[k] = __uint_as_float(s0[k]);
+            x[32 + k] = __uint_as_float(s1[k]);
           }
-          tmem_st_wait();
         }
-      }
-      const float nref = -mref;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        if (!full) {
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
-        x[k] = ex2_ftz(fmaf(x[k], sc, nref));
-        ps[k & 3] += x[k];
+          for (int q = 0; q < C::PG; ++q)
+#pragma unroll
+            for (int k = 0; k < kPage; ++k)
+              if (k >= vq[q]) x[q * kPage + k] = -INFINITY;
+        }
+        // row max as a tree of three-input maxima (depth 4, not a 64-long chain)
+        float t3[22], u3[8];
+#pragma unroll
+        for (int i = 0; i < 21; ++i) t3[i] = fmax3(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+        t3[21] = x[63];
+#pragma unroll
+        for (int i = 0; i < 7; ++i) u3[i] = fmax3(t3[3 * i], t3[3 * i + 1], t3[3 * i + 2]);
+        u3[7] = t3[21];
+        const float rmx = fmax3(fmax3(u3[0], u3[1], u3[2]), fmax3(u3[3], u3[4], u3[5]),
+                                fmaxf(u3[6], u3[7]));
+        const float mx = rmx * sc;
+        const bool move = mx > mref;
+        if (__any_sync(0xffffffffu, move)) {
+          const float mn = move ? mx : mref;
+          const float alpha = exp2f(mref - mn);         // 0 on the first step
+          l *= alpha;
+          mref = mn;
+          if (j > 0) {
+            // the previous step's P V must have landed before O is rescaled in place
+            if (!__all_sync(0xffffffffu, mbar_wait(ofull, (j - 1) & 1))) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < HD / 32; ++c) {
+              uint32_t ov[32];
+              tmem_ld32(o_addr + c * 32, ov);
+              tmem_ld_wait();
+#pragma unroll
+              for (int d = 0; d < 32; ++d) ov[d] = __float_as_uint(__uint_as_float(ov[d]) * alpha);
+              tmem_st32(o_addr + c * 32, ov);
+            }
+            tmem_st_wait();
+          }
+        }
+        ps = exp2_row64(x, sc, -mref);
       }
-      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      l += ps;
       // P over this step's S columns: hi pairs in the first 32, lo pairs in the last 32
       {
         uint32_t hi[32], lo[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) split_bf16x2(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
+        for (int e = 0; e < 32; ++e) split_bf16x2_f2(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
         tmem_st32(s_addr, hi);
         tmem_st32(s_addr + 32, lo);
       }
