@@ -271,10 +271,30 @@ struct AttnPlan {
 };
 
 AttnPlan plan_attn(const H* h, int B, int max_pages) {
-  // About eight (b, kv head, split) CTAs per SM at the longest context, so that ragged
-  // lengths and the last wave of CTAs balance; at least 8 pages and at most 64 splits.
   const int kp = max_pages + 1;
   const long long groups = (long long)B * h->c.n_kv_heads;
+  if (use_attn_umma(h->c, B * h->c.block_size)) {
+    // tcgen05 kernel, two CTAs per SM, four pages per step: whole steps per split and
+    // the fewest waves of CTAs times steps per CTA (plus about three steps of per-CTA
+    // prologue and epilogue); among plans within 2 % of the best, the fewest splits.
+    const long long slots = 2LL * h->sms;
+    AttnPlan best{0, 0};
+    long long best_cost = 0;
+    for (int ns = 1; ns <= std::min(64, ceil_div(kp, 4)); ++ns) {
+      const int pps = ceil_div(ceil_div(kp, ns), 4) * 4;
+      const int nsr = ceil_div(kp, pps);
+      if (nsr != ns) continue;
+      const long long cost = (groups * ns + slots - 1) / slots * (pps / 4 + 3);
+      if (best.nsplit == 0 || cost * 50 < best_cost * 49) {
+        best = {pps, ns};
+        best_cost = cost;
+      }
+    }
+    return best;
+  }
+  // mma.sync kernel: about eight (b, kv head, split) CTAs per SM at the longest context,
+  // so that ragged lengths and the last wave of CTAs balance; at least 8 pages and at
+  // most 64 splits.
   const long long want = std::max<long long>(1, (8LL * h->sms + groups - 1) / groups);
   const long long cap = std::min(64, ceil_div(kp, 8));
   const int ns = static_cast<int>(std::min(want, cap));
