@@ -112,9 +112,10 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
 
   if constexpr (EPI == EPI_F32 || EPI == EPI_RESID) {
     const int nc = min(kBM, e.N - nt * kBM);
-    if (nc == kBM && (e.ldy & 3) == 0 && (pitch & 3) == 0) {
-      // lane -> columns 4*lane .. 4*lane+3
-      for (int rb = warp; rb < mr; rb += nw * RB) {
+    if ((nc & 3) == 0 && (e.ldy & 3) == 0 && (pitch & 3) == 0) {
+      // lane -> columns 4*lane .. 4*lane+3 (lanes past a ragged last tile's columns idle)
+      const int rlim = 4 * lane < nc ? mr : 0;
+      for (int rb = warp; rb < rlim; rb += nw * RB) {
         float4 o[RB];
         if constexpr (EPI == EPI_RESID) {
 #pragma unroll

@@ -147,6 +147,38 @@ struct UmCfg {
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// Residual rows of one 32-row epilogue chunk for the four epilogue warps: warp w takes
+// rows w, w + 4, ..., w + 28 of the chunk, lane the four columns 4*lane .. 4*lane + 3 of
+// the tile's `nc` (a multiple of 4; fewer than 128 only in the ragged last tile).
+__device__ __forceinline__ void resid_fetch(float4 (&x)[8], const EpiArgs<bf16>& e, int m0,
+                                            int mr, int col0, int nc, int w, int lane) {
+  if (4 * lane >= nc) return;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int r = w + 4 * k;
+    if (r < mr)
+      x[k] = reinterpret_cast<const float4*>(e.y + static_cast<long long>(m0 + r) * e.ldy + col0)[lane];
+  }
+}
+
+// y = residual + accumulator for the same rows and columns, accumulator from Cs.
+__device__ __forceinline__ void resid_apply(const float4 (&x)[8], const float* Cs, int pitch,
+                                            const EpiArgs<bf16>& e, int m0, int mr, int col0,
+                                            int nc, int w, int lane) {
+  if (4 * lane >= nc) return;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int r = w + 4 * k;
+    if (r >= mr) continue;
+    float4 v = *reinterpret_cast<const float4*>(Cs + r * pitch + lane * 4);
+    v.x += x[k].x;
+    v.y += x[k].y;
+    v.z += x[k].z;
+    v.w += x[k].w;
+    reinterpret_cast<float4*>(e.y + static_cast<long long>(m0 + r) * e.ldy + col0)[lane] = v;
+  }
+}
+
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(192, 1)
@@ -313,17 +345,25 @@ __global__ void __launch_bounds__(192, 1)
       const long long tile_end = static_cast<long long>(t + 1) * g.ks;
       const long long seg_end = min(tile_end, u1);
       const int ab = piece & 1, use = piece >> 1;
-      if (ok && !__all_sync(0xffffffffu, mbar_wait(&tfull[ab], use & 1))) {
-        if (lane == 0) raise_error(e.err, DFLASH_DEV_TIMEOUT);
-        ok = false;
-      }
-      tc_fence_after();
       const uint32_t tacc = tmem + lane_base + static_cast<uint32_t>(ab * BN);
       const int mb = t / g.n_tiles, nt = t - mb * g.n_tiles;
       const int m_first = mb * BN;
       const int rows = min(BN, g.M - m_first);            // valid activation rows
       const int nch = (rows + C::CH - 1) / C::CH;         // chunks holding them
       const bool whole = (ks0 == 0) && (seg_end == tile_end);
+      // Residual epilogue of a whole tile: the residual rows of chunk c + 1 are loaded
+      // while chunk c is finished, those of chunk 0 while the accumulator is still being
+      // computed.
+      const int ncol = min(kBM, e.N - nt * kBM);          // columns of the tile (ragged last)
+      const bool resid_pipe = EPI == EPI_RESID && whole && (ncol & 3) == 0 && (e.ldy & 3) == 0;
+      float4 xres[8];
+      if (resid_pipe)
+        resid_fetch(xres, e, m_first, min(C::CH, rows), nt * kBM, ncol, et >> 5, lane);
+      if (ok && !__all_sync(0xffffffffu, mbar_wait(&tfull[ab], use & 1))) {
+        if (lane == 0) raise_error(e.err, DFLASH_DEV_TIMEOUT);
+        ok = false;
+      }
+      tc_fence_after();
 
       // Reads chunk c of the accumulator into v; after the last chunk the accumulator is
       // handed back to the MMA issuer.
@@ -342,7 +382,26 @@ __global__ void __launch_bounds__(192, 1)
         }
       };
 
-      if (whole) {
+      if (resid_pipe) {
+        for (int c = 0; c < nch; ++c) {
+          uint32_t v[32];
+          read_chunk(c, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) Cs[j * C::PITCH + feat] = __uint_as_float(v[j]);
+          epi_sync();
+          float4 xnext[8];
+          const int m0 = m_first + c * C::CH;
+          if (c + 1 < nch)
+            resid_fetch(xnext, e, m0 + C::CH, min(C::CH, rows - (c + 1) * C::CH), nt * kBM, ncol,
+                        et >> 5, lane);
+          if (ok)
+            resid_apply(xres, Cs, C::PITCH, e, m0, min(C::CH, rows - c * C::CH), nt * kBM, ncol,
+                        et >> 5, lane);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) xres[k] = xnext[k];
+          epi_sync();
+        }
+      } else if (whole) {
         for (int c = 0; c < nch; ++c) {
           uint32_t v[32];
           read_chunk(c, v);
