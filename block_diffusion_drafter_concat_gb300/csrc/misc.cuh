@@ -227,6 +227,46 @@ __global__ void __launch_bounds__(kRowThreads)
 }
 
 // ------------------------------------------------------------ temperature-tau verify
+// Eight consecutive values as floats from a 16-byte aligned address.
+__device__ __forceinline__ void load8_stream(const bf16* p, float (&x)[8]) {
+  const uint4 raw = __ldcs(reinterpret_cast<const uint4*>(p));
+  const bf16* e = reinterpret_cast<const bf16*>(&raw);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) x[j] = __bfloat162float(e[j]);
+}
+__device__ __forceinline__ void load8_stream(const float* p, float (&x)[8]) {
+  const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void load8(const bf16* p, float (&x)[8]) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(p);
+  const bf16* e = reinterpret_cast<const bf16*>(&raw);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) x[j] = __bfloat162float(e[j]);
+}
+__device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *(reinterpret_cast<const float4*>(p) + 1);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+// Merges running (max m, sum s of exp((x - m) * it)) states.
+__device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2, float it) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    s = s2;
+  } else if (m2 > m) {
+    s = s * __expf((m - m2) * it) + s2;
+    m = m2;
+  } else {
+    s += s2 * __expf((m2 - m) * it);
+  }
+}
+
 // Pass 1, grid (chunks, B*S): per chunk of target row r the max and sum exp of
 // logits/tau; the last CTA of a row forms lse_t[r] and p_r(d_r); the last row of a
 // sequence walks the acceptance test u[i,0] < p_i(d_i) / q_i(d_i), writes the accepted
@@ -254,18 +294,45 @@ __global__ void __launch_bounds__(kRowThreads)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const T* src = logits + (long long)row * V;
   const int v0 = c * chunk, v1 = min(V, v0 + chunk);
-  float mx = -INFINITY;
-  for (int v = v0 + threadIdx.x; v < v1; v += kRowThreads) mx = fmaxf(mx, to_f32<T>(src[v]));
-  mx = warp_max(mx);
-  if (lane == 0) redm[warp] = mx;
+  // one pass: running (max, sum of exp((x - max) / tau)) per thread, 16-byte loads
+  float mx = -INFINITY, s = 0.f;
+  const bool vec_ok = (reinterpret_cast<uintptr_t>(src + v0) & 15) == 0;
+  const int nv = vec_ok ? (v1 - v0) / 8 : 0;
+  for (int k = threadIdx.x; k < nv; k += kRowThreads) {
+    float x[8];
+    load8_stream(src + v0 + 8 * k, x);
+    float lm = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
+                     fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+    if (lm > mx) {
+      s = mx == -INFINITY ? 0.f : s * __expf((mx - lm) * inv_temp);
+      mx = lm;
+    }
+    if (mx == -INFINITY) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s += __expf((x[j] - mx) * inv_temp);
+  }
+  for (int v = v0 + 8 * nv + threadIdx.x; v < v1; v += kRowThreads) {
+    const float x = to_f32<T>(src[v]);
+    if (x > mx) {
+      s = mx == -INFINITY ? 0.f : s * __expf((mx - x) * inv_temp);
+      mx = x;
+    }
+    if (mx != -INFINITY) s += __expf((x - mx) * inv_temp);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, mx, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    ms_merge(mx, s, m2, s2, inv_temp);
+  }
+  if (lane == 0) {
+    redm[warp] = mx;
+    red[warp] = s;
+  }
   __syncthreads();
-  mx = -INFINITY;
-  for (int w = 0; w < kRowThreads / 32; ++w) mx = fmaxf(mx, redm[w]);
-  float s = 0.f;
-  for (int v = v0 + threadIdx.x; v < v1; v += kRowThreads)
-    s += __expf((to_f32<T>(src[v]) - mx) * inv_temp);
-  s = block_sum(s, red);
   if (threadIdx.x == 0) {
+    mx = redm[0];
+    s = red[0];
+    for (int w = 1; w < kRowThreads / 32; ++w) ms_merge(mx, s, redm[w], red[w], inv_temp);
     part_m[(long long)row * nch + c] = mx;
     part_s[(long long)row * nch + c] = s;
   }
@@ -310,7 +377,19 @@ __global__ void __launch_bounds__(kRowThreads)
 
 // Pass 2, grid (chunks, B), after the drafter logits zr [B, V] of each rejected slot
 // were recomputed: r_v = max(0, p_v - q_v) per chunk; the last chunk of a sequence
-// finds the chunk holding u[n,1] * sum(r) and scans it for the sampled token.
+// finds the chunk holding u[n,1] * sum(r) and, inside it, the token: each thread sums
+// a contiguous segment, one block scan of the segment sums places the target in one
+// segment, and that thread walks it.  Rounding (the chunk sums and the walk add in
+// different orders) can leave the target just past the last mass: then the last index
+// with mass is taken.
+template <typename T>
+__device__ __forceinline__ float resid_val(const T* lt, const float* lz, int v, float it,
+                                           float lset, float lsez, bool use_p) {
+  const float p = __expf(to_f32<T>(lt[v]) * it - lset);
+  const float q = __expf(lz[v] * it - lsez);
+  return use_p ? p : fmaxf(0.f, p - q);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads)
     k_verify_sample_residual(const T* __restrict__ logits, const float* __restrict__ zr,
@@ -321,11 +400,10 @@ __global__ void __launch_bounds__(kRowThreads)
                              int* __restrict__ out_tokens) {
   __shared__ float red[kRowThreads / 32];
   __shared__ int flag;
-  __shared__ float scan[kRowThreads];
-  __shared__ int found;
   pdl_wait();
   pdl_launch_dependents();
   const int c = blockIdx.x, b = blockIdx.y, nch = gridDim.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n = rej[b];
   if (n >= S) return;  // everything accepted: nothing to sample (counter unused)
   const long long r = (long long)b * S + n;
@@ -334,9 +412,23 @@ __global__ void __launch_bounds__(kRowThreads)
   const float lset = lse_t[r], lsez = dlse[r];
   const int v0 = c * chunk, v1 = min(V, v0 + chunk);
   float sr = 0.f, sp = 0.f;
-  for (int v = v0 + threadIdx.x; v < v1; v += kRowThreads) {
-    float p = __expf(to_f32<T>(lt[v]) * inv_temp - lset);
-    float q = __expf(lz[v] * inv_temp - lsez);
+  const bool vec_ok = ((reinterpret_cast<uintptr_t>(lt + v0) | reinterpret_cast<uintptr_t>(lz + v0)) & 15) == 0;
+  const int nv = vec_ok ? (v1 - v0) / 8 : 0;
+  for (int k = threadIdx.x; k < nv; k += kRowThreads) {
+    float x[8], z[8];
+    load8(lt + v0 + 8 * k, x);
+    load8(lz + v0 + 8 * k, z);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float p = __expf(x[j] * inv_temp - lset);
+      const float q = __expf(z[j] * inv_temp - lsez);
+      sr += fmaxf(0.f, p - q);
+      sp += p;
+    }
+  }
+  for (int v = v0 + 8 * nv + threadIdx.x; v < v1; v += kRowThreads) {
+    const float p = __expf(to_f32<T>(lt[v]) * inv_temp - lset);
+    const float q = __expf(lz[v] * inv_temp - lsez);
     sr += fmaxf(0.f, p - q);
     sp += p;
   }
@@ -347,76 +439,99 @@ __global__ void __launch_bounds__(kRowThreads)
     part_p[(long long)b * nch + c] = sp;
   }
   if (!elect_last(&counters[b], nch, &flag)) return;
-  // choose the residual (or p itself when the residual is all zero)
-  __shared__ int use_p;
-  __shared__ float target;
-  __shared__ int cstar;
-  __shared__ float before;
+  // choose the residual (or p itself when the residual is all zero), then the chunk
+  __shared__ int use_p_s, cstar, found, lastnz;
+  __shared__ float target_s, before_s;
+  __shared__ float wtot[kRowThreads / 32];
   if (threadIdx.x == 0) {
     float Z = 0.f;
     for (int k = 0; k < nch; ++k) Z += __ldcg(part_r + (long long)b * nch + k);
     const float* pr = part_r;
-    use_p = (Z <= 0.f);
-    if (use_p) {
+    use_p_s = (Z <= 0.f);
+    if (use_p_s) {
       Z = 0.f;
       for (int k = 0; k < nch; ++k) Z += __ldcg(part_p + (long long)b * nch + k);
       pr = part_p;
     }
-    target = u[r * 2 + 1] * Z;
+    const float target = u[r * 2 + 1] * Z;
     float acc = 0.f;
     int k = 0, last_nz = -1;
     for (; k < nch; ++k) {
-      float w = __ldcg(pr + (long long)b * nch + k);
+      const float w = __ldcg(pr + (long long)b * nch + k);
       if (w > 0.f) last_nz = k;
       if (acc + w >= target && w > 0.f) break;
       acc += w;
     }
-    if (k == nch) { k = last_nz < 0 ? 0 : last_nz; acc = -1.f; }  // rounding: take the last mass
+    if (k == nch) {  // rounding: no prefix reached the target; the last mass is taken
+      k = last_nz < 0 ? 0 : last_nz;
+      acc = INFINITY;
+    }
     cstar = k;
-    before = acc;
-    found = -1;
+    before_s = acc;
+    target_s = target;
+    found = 0x7fffffff;
+    lastnz = -1;
   }
   __syncthreads();
-  // inclusive scan of chunk cstar in index order, kRowThreads elements at a time
+  const bool use_p = use_p_s != 0;
+  const float target = target_s, before = before_s;
   const int w0 = cstar * chunk, w1 = min(V, w0 + chunk);
-  float acc = before;
-  const bool last_mass = before < 0.f;
-  int last_pos = -1;
-  for (int base = w0; base < w1; base += kRowThreads) {
-    const int v = base + threadIdx.x;
-    float val = 0.f;
-    if (v < w1) {
-      float p = __expf(to_f32<T>(lt[v]) * inv_temp - lset);
-      float q = __expf(lz[v] * inv_temp - lsez);
-      val = use_p ? p : fmaxf(0.f, p - q);
+  const int seg = ((w1 - w0 + kRowThreads - 1) / kRowThreads + 7) & ~7;
+  const int a0 = min(w1, w0 + threadIdx.x * seg), a1 = min(w1, a0 + seg);
+  const bool seg_vec = ((reinterpret_cast<uintptr_t>(lt + a0) | reinterpret_cast<uintptr_t>(lz + a0)) & 15) == 0;
+  float my = 0.f;
+  int my_last = -1;
+  int v = a0;
+  if (seg_vec) {
+    for (; v + 8 <= a1; v += 8) {
+      float x[8], z[8];
+      load8(lt + v, x);
+      load8(lz + v, z);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float p = __expf(x[j] * inv_temp - lset);
+        const float q = __expf(z[j] * inv_temp - lsez);
+        const float val = use_p ? p : fmaxf(0.f, p - q);
+        my += val;
+        if (val > 0.f) my_last = v + j;
+      }
     }
-    scan[threadIdx.x] = val;
-    __syncthreads();
-    for (int off = 1; off < kRowThreads; off <<= 1) {
-      float t = threadIdx.x >= off ? scan[threadIdx.x - off] : 0.f;
-      __syncthreads();
-      scan[threadIdx.x] += t;
-      __syncthreads();
+  }
+  for (; v < a1; ++v) {
+    const float val = resid_val(lt, lz, v, inv_temp, lset, lsez, use_p);
+    my += val;
+    if (val > 0.f) my_last = v;
+  }
+  // exclusive scan of the segment sums in thread (= index) order
+  float incl = my;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) wtot[warp] = incl;
+  __syncthreads();
+  float woff = 0.f;
+  for (int w = 0; w < warp; ++w) woff += wtot[w];
+  const float excl = woff + incl - my;
+  const float lo = before + excl;
+  const bool last_mass = !(before < INFINITY);
+  if (!last_mass && my > 0.f && lo + my >= target && (lo < target || excl == 0.f)) {
+    float acc = lo;
+    int hit = my_last;   // the walk may fall just short through rounding
+    for (int w = a0; w < a1; ++w) {
+      const float val = resid_val(lt, lz, w, inv_temp, lset, lsez, use_p);
+      acc += val;
+      if (val > 0.f && acc >= target) {
+        hit = w;
+        break;
+      }
     }
-    if (!last_mass && found < 0 && val > 0.f && acc + scan[threadIdx.x] >= target)
-      atomicMin(reinterpret_cast<unsigned*>(&found), static_cast<unsigned>(v));
-    if (val > 0.f) last_pos = v;
-    __syncthreads();
-    acc += scan[kRowThreads - 1];
-    __syncthreads();
-    if (found >= 0) break;
+    atomicMin(&found, hit);
   }
-  if (last_mass) {
-    // no prefix reached the target through rounding: the last index with mass
-    __shared__ int lp;
-    if (threadIdx.x == 0) lp = -1;
-    __syncthreads();
-    if (last_pos >= 0) atomicMax(&lp, last_pos);
-    __syncthreads();
-    if (threadIdx.x == 0) out_tokens[r] = lp;
-  } else if (threadIdx.x == 0) {
-    out_tokens[r] = found;
-  }
+  if (my_last >= 0) atomicMax(&lastnz, my_last);
+  __syncthreads();
+  if (threadIdx.x == 0) out_tokens[r] = found != 0x7fffffff ? found : lastnz;
 }
 
 }  // namespace dflash
