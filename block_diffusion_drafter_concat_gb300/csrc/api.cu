@@ -257,13 +257,17 @@ dflash_status rmsnorm(const H* h, const Tin* x, const void* gain, T* y, int rows
 }
 
 // ------------------------------------------------------------------ attention plan
-// Blocks of many rows (a batch of sequences) with head_dim 64 run attention on the
-// tcgen05 kernel; a single block (latency-bound) and head_dim 128 (whose 64 query rows
-// per kv head would leave half of the 128-row tile idle at one CTA per SM, measured
-// slower) on the mma.sync kernel.
+// Blocks of many rows (a batch of sequences) run attention on the tcgen05 kernel: with
+// head_dim 64 and up to 128 query rows per kv head one row per TMEM lane, with at most
+// 64 rows (head_dim 64 or 128) in key-split mode (each row on two lanes, half of every
+// step's keys each).  A single block (latency-bound) stays on the mma.sync kernel.
+bool attn_ksplit(const dflash_config& c) {
+  return c.block_size * (c.n_q_heads / c.n_kv_heads) <= 64;
+}
 bool use_attn_umma(const dflash_config& c, int M) {
   const int QR = c.block_size * (c.n_q_heads / c.n_kv_heads);
-  return c.dtype == DFLASH_BF16 && c.head_dim == 64 && M > 64 && QR <= 128;
+  if (c.dtype != DFLASH_BF16 || M <= 64) return false;
+  return (c.head_dim == 64 && QR <= 128) || (c.head_dim == 128 && QR <= 64);
 }
 
 struct AttnPlan {
@@ -289,6 +293,15 @@ AttnPlan plan_attn(const H* h, int B, int max_pages) {
         best = {pps, ns};
         best_cost = cost;
       }
+    }
+    // Key-split mode (head_dim 128, steps bound by K/V bandwidth): the model assumes
+    // every sequence has the longest context.  When it leaves one CTA more than 40
+    // steps, a batch of ragged lengths would wait on its longest sequence's few CTAs,
+    // so splits of 24 steps are taken instead (measured on GB300: ragged batch 32
+    // 2604 -> 2498 us per step; a uniform batch 8 keeps its 33-step plan).
+    if (attn_ksplit(h->c) && best.pps / 4 > 40) {
+      const int pps = std::max(96, ceil_div(ceil_div(kp, 64), 4) * 4);   // <= 64 splits
+      best = {pps, ceil_div(kp, pps)};
     }
     return best;
   }
@@ -517,9 +530,10 @@ static dflash_status draft_impl(H* h, const int32_t* block_ids, const int32_t* c
           am.v = mp.v;
           am.kb = mp.kb;
           am.vb = mp.vb;
+          const bool ks = attn_ksplit(c);
           TRY(encode_bf16(&am.q, w.q, (uint64_t)B * c.n_kv_heads * QR, c.head_dim, c.head_dim,
-                          128));
-          TRY(launch_attn_umma(c.head_dim, grid, am, a, st));
+                          ks ? 64 : 128));
+          TRY(launch_attn_umma(c.head_dim, ks, grid, am, a, st));
         } else {
           const int smem = 1024 + kAttnStages * (2 * kPage * c.head_dim * 2 + 16) + 16;
           TRY(launch_attn_tc(c.head_dim, QR / 16, grid, smem, mp, a, st));

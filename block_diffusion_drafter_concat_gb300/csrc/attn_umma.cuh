@@ -84,13 +84,14 @@ __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
   return r;
 }
 
-// Probabilities 2^(x*sc - mref) of 64 scores in place; returns their sum (four partial
+// Probabilities 2^(x*sc - mref) of N scores in place; returns their sum (four partial
 // sums, added pairwise).
-__device__ __forceinline__ float exp2_row64(float (&x)[64], float sc, float nref) {
+template <int N>
+__device__ __forceinline__ float exp2_row(float (&x)[N], float sc, float nref) {
   const uint64_t sc2 = f2_pack(sc, sc), nr2 = f2_pack(nref, nref);
   uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
+  for (int e = 0; e < N / 2; ++e) {
     float t0, t1;
     f2_unpack(f2_fma(f2_pack(x[2 * e], x[2 * e + 1]), sc2, nr2), t0, t1);
     x[2 * e] = ex2_ftz(t0);
@@ -104,6 +105,10 @@ __device__ __forceinline__ float exp2_row64(float (&x)[64], float sc, float nref
   f2_unpack(acc1, b0, b1);
   return (a0 + a1) + (b0 + b1);
 }
+
+// Maximum of N values as a tree of three-input maxima.
+template <int N>
+__device__ __forceinline__ float max_tree(const float (&x)[N]);
 
 // bf16 pair hi (round to nearest even) and the pair of residuals lo = bf16(x - hi).
 __device__ __forceinline__ void split_bf16x2_f2(float a, float b, uint32_t& hi, uint32_t& lo) {
@@ -121,12 +126,37 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return y;
 }
 
-template <int HD>
+template <>
+__device__ __forceinline__ float max_tree<64>(const float (&x)[64]) {
+  float t3[22], u3[8];
+#pragma unroll
+  for (int i = 0; i < 21; ++i) t3[i] = fmax3(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+  t3[21] = x[63];
+#pragma unroll
+  for (int i = 0; i < 7; ++i) u3[i] = fmax3(t3[3 * i], t3[3 * i + 1], t3[3 * i + 2]);
+  u3[7] = t3[21];
+  return fmax3(fmax3(u3[0], u3[1], u3[2]), fmax3(u3[3], u3[4], u3[5]), fmaxf(u3[6], u3[7]));
+}
+
+template <>
+__device__ __forceinline__ float max_tree<32>(const float (&x)[32]) {
+  float t3[11], u3[4];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) t3[i] = fmax3(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+  t3[10] = fmaxf(x[30], x[31]);
+#pragma unroll
+  for (int i = 0; i < 3; ++i) u3[i] = fmax3(t3[3 * i], t3[3 * i + 1], t3[3 * i + 2]);
+  u3[3] = fmaxf(t3[9], t3[10]);
+  return fmax3(u3[0], u3[1], fmaxf(u3[2], u3[3]));
+}
+
+template <int HD, bool KSPLIT>
 struct AuCfg {
   static constexpr int KT = 64;                    // keys per step
   static constexpr int PG = KT / kPage;            // pages per step
   static constexpr int KB = HD / 64;               // 64-column blocks of a head
   static constexpr int NS = HD == 64 ? 4 : 2;      // ring stages
+  static constexpr int NK = KSPLIT ? KT / 2 : KT;  // keys of a step per softmax thread
   static constexpr int Q_BYTES = 128 * HD * 2;
   static constexpr int KV_BLOCK = KT * 128;        // one 64-column block of K or V
   static constexpr int KV_BYTES = KB * KV_BLOCK;
@@ -141,12 +171,14 @@ struct AuCfg {
   static constexpr uint32_t IDESC_O = umma_idesc_bf16<128, HD>() | (1u << 16);  // B MN-major
   static_assert(O_COL + HD <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
+  // key-split merge buffer (64 rows of O and (m, l)) reuses the K/V ring
+  static_assert(!KSPLIT || 64 * HD * 4 + 64 * 8 <= NS * STAGE, "merge buffer");
 };
 
-template <int HD>
+template <int HD, bool KSPLIT>
 __global__ void __launch_bounds__(192, 2)
     k_attn_umma(const __grid_constant__ AuMaps maps, const AttnArgs<bf16> a) {
-  using C = AuCfg<HD>;
+  using C = AuCfg<HD, KSPLIT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -214,8 +246,16 @@ __global__ void __launch_bounds__(192, 2)
       if (lane == 0) {
         mbar_arrive_expect_tx(qfull, C::Q_BYTES);
 #pragma unroll
-        for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_2d(sq + kb * (128 * 128), &maps.q, qfull, kb * 64, (b * a.hkv + g) * a.QR);
+        for (int kb = 0; kb < C::KB; ++kb) {
+          if constexpr (KSPLIT) {
+            // the group's (up to) 64 query rows in tile rows 0-63 and again in 64-127
+            tma_load_2d(sq + kb * (128 * 128), &maps.q, qfull, kb * 64, (b * a.hkv + g) * a.QR);
+            tma_load_2d(sq + kb * (128 * 128) + 64 * 128, &maps.q, qfull, kb * 64,
+                        (b * a.hkv + g) * a.QR);
+          } else {
+            tma_load_2d(sq + kb * (128 * 128), &maps.q, qfull, kb * 64, (b * a.hkv + g) * a.QR);
+          }
+        }
       }
     };
     for (int j = 0; j < nsteps && ok; ++j) {
@@ -333,7 +373,13 @@ __global__ void __launch_bounds__(192, 2)
     pdl_wait();
     pdl_launch_dependents();
     const int q4 = warp & 3;
-    const int r = q4 * 32 + lane;                     // query row = TMEM lane
+    const int r = q4 * 32 + lane;                     // TMEM lane
+    // key split: lanes r and r + 64 hold the same query row; lane r takes keys 0-31 of
+    // every step and lane r + 64 keys 32-63, each with its own softmax state and O row,
+    // merged after the last step.  Otherwise lane r is query row r with all 64 keys.
+    const int half = KSPLIT ? (r >> 6) : 0;
+    const int qrow = KSPLIT ? (r & 63) : r;
+    constexpr int NK = C::NK;
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t o_addr = tmem + lane_base + C::O_COL;
     const float sc = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
@@ -348,20 +394,27 @@ __global__ void __launch_bounds__(192, 2)
       const uint32_t s_addr = tmem + lane_base + static_cast<uint32_t>(sb * C::KT);
       if (!__all_sync(0xffffffffu, mbar_wait(&sfull[sb], (j >> 1) & 1))) { ok = false; break; }
       tc_fence_after();
-      uint32_t s0[32], s1[32];
-      tmem_ld32(s_addr, s0);
-      tmem_ld32(s_addr + 32, s1);
-      tmem_ld_wait();
       // Raw scores; keys past a page's valid count are masked only in steps that have
       // any (the last steps of a split): the common step is four full pages.  The max is
       // taken on raw scores (the scale is positive) and the scale folded into one FMA
       // with the reference below.
-      float x[64];
+      float x[NK];
+      auto load_s = [&]() {
+        uint32_t s0[32];
+        tmem_ld32(s_addr + half * 32, s0);
+        if constexpr (NK == 64) {
+          uint32_t s1[32];
+          tmem_ld32(s_addr + 32, s1);
+          tmem_ld_wait();
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        x[k] = __uint_as_float(s0[k]);
-        x[32 + k] = __uint_as_float(s1[k]);
-      }
+          for (int k = 0; k < 32; ++k) x[32 + k] = __uint_as_float(s1[k]);
+        } else {
+          tmem_ld_wait();
+        }
+#pragma unroll
+        for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(s0[k]);
+      };
+      load_s();
       int vq[C::PG];
       bool full = true;
 #pragma unroll
@@ -380,38 +433,22 @@ __global__ void __launch_bounds__(192, 2)
       bool tried = false;
       if (!slow) {
         tried = true;
-        ps = exp2_row64(x, sc, -mref);
+        ps = exp2_row<NK>(x, sc, -mref);
         slow = __any_sync(0xffffffffu, !(ps <= 256.f));
       }
       if (slow) {
-        if (tried) {
-          tmem_ld32(s_addr, s0);
-          tmem_ld32(s_addr + 32, s1);
-          tmem_ld_wait();
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            x[k] = __uint_as_float(s0[k]);
-            x[32 + k] = __uint_as_float(s1[k]);
-          }
-        }
+        if (tried) load_s();
         if (!full) {
+          // this thread's keys are pages [q0, q0 + NK / 16) of the step
 #pragma unroll
-          for (int q = 0; q < C::PG; ++q)
+          for (int q = 0; q < NK / kPage; ++q) {
+            const int vv = (KSPLIT && half) ? vq[NK / kPage + q] : vq[q];
 #pragma unroll
             for (int k = 0; k < kPage; ++k)
-              if (k >= vq[q]) x[q * kPage + k] = -INFINITY;
+              if (k >= vv) x[q * kPage + k] = -INFINITY;
+          }
         }
-        // row max as a tree of three-input maxima (depth 4, not a 64-long chain)
-        float t3[22], u3[8];
-#pragma unroll
-        for (int i = 0; i < 21; ++i) t3[i] = fmax3(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
-        t3[21] = x[63];
-#pragma unroll
-        for (int i = 0; i < 7; ++i) u3[i] = fmax3(t3[3 * i], t3[3 * i + 1], t3[3 * i + 2]);
-        u3[7] = t3[21];
-        const float rmx = fmax3(fmax3(u3[0], u3[1], u3[2]), fmax3(u3[3], u3[4], u3[5]),
-                                fmaxf(u3[6], u3[7]));
-        const float mx = rmx * sc;
+        const float mx = max_tree<NK>(x) * sc;
         const bool move = mx > mref;
         if (__any_sync(0xffffffffu, move)) {
           const float mn = move ? mx : mref;
@@ -434,14 +471,34 @@ __global__ void __launch_bounds__(192, 2)
             tmem_st_wait();
           }
         }
-        ps = exp2_row64(x, sc, -mref);
+        if (mref == -INFINITY) {
+          // no valid key of this thread yet (a key-split half of a one-page split)
+#pragma unroll
+          for (int k = 0; k < NK; ++k) x[k] = 0.f;
+          ps = 0.f;
+        } else {
+          ps = exp2_row<NK>(x, sc, -mref);
+        }
       }
       l += ps;
-      // P over this step's S columns: hi pairs in the first 32, lo pairs in the last 32
+      // P over this step's S columns: hi pairs in the first 32, lo pairs in the last 32;
+      // a key-split thread writes its 16 pairs and zeros for the other half's
       {
         uint32_t hi[32], lo[32];
+        if constexpr (NK == 64) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) split_bf16x2_f2(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
+          for (int e = 0; e < 32; ++e) split_bf16x2_f2(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            uint32_t h2, l2;
+            split_bf16x2_f2(x[2 * e], x[2 * e + 1], h2, l2);
+            hi[e] = half ? 0u : h2;
+            hi[16 + e] = half ? h2 : 0u;
+            lo[e] = half ? 0u : l2;
+            lo[16 + e] = half ? l2 : 0u;
+          }
+        }
         tmem_st32(s_addr, hi);
         tmem_st32(s_addr + 32, lo);
       }
@@ -456,24 +513,68 @@ __global__ void __launch_bounds__(192, 2)
     if (ok && nsteps > 0 && !__all_sync(0xffffffffu, mbar_wait(ofull, (nsteps - 1) & 1))) ok = false;
     if (!ok && lane == 0) raise_error(a.err, DFLASH_DEV_TIMEOUT);
     tc_fence_after();
-    // O from TMEM 32 columns at a time (the loads are warp-wide; rows past QR skip the
-    // stores only)
+    if constexpr (KSPLIT) {
+      // The K/V ring is idle (every MMA has completed): lanes 64-127 leave their O row
+      // and (m, l) there, lanes 0-63 merge them into theirs.  Row q's columns are
+      // rotated by q so that a warp's 32 stores of one column hit 32 banks.
+      float* mo = reinterpret_cast<float*>(stages);               // [64][HD]
+      float* mml = mo + 64 * HD;                                  // [64][2]
+      if (half) {
 #pragma unroll
-    for (int c = 0; c < HD / 32; ++c) {
-      uint32_t ov[32];
-      tmem_ld32(o_addr + c * 32, ov);
-      tmem_ld_wait();
-      if (r < a.QR && ok) {
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(o_addr + c * 32, ov);
+          tmem_ld_wait();
 #pragma unroll
-        for (int d = 0; d < 32; d += 2)
-          attn_emit<bf16>(a, b, g, split, r, c * 32 + d, __uint_as_float(ov[d]),
-                          __uint_as_float(ov[d + 1]), l);
+          for (int d = 0; d < 32; ++d) mo[qrow * HD + ((c * 32 + d + qrow) & (HD - 1))] = __uint_as_float(ov[d]);
+        }
+        mml[2 * qrow] = mref;
+        mml[2 * qrow + 1] = l;
+      }
+      epi_sync();
+      if (!half) {
+        const float m2 = mml[2 * qrow], l2 = mml[2 * qrow + 1];
+        const float M = fmaxf(mref, m2);
+        const float w1 = exp2f(mref - M), w2 = exp2f(m2 - M);
+        l = l * w1 + l2 * w2;
+        mref = M;
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(o_addr + c * 32, ov);
+          tmem_ld_wait();
+          if (qrow < a.QR && ok) {
+#pragma unroll
+            for (int d = 0; d < 32; d += 2) {
+              const float o0 = __uint_as_float(ov[d]) * w1 +
+                               mo[qrow * HD + ((c * 32 + d + qrow) & (HD - 1))] * w2;
+              const float o1 = __uint_as_float(ov[d + 1]) * w1 +
+                               mo[qrow * HD + ((c * 32 + d + 1 + qrow) & (HD - 1))] * w2;
+              attn_emit<bf16>(a, b, g, split, qrow, c * 32 + d, o0, o1, l);
+            }
+          }
+        }
+      }
+    } else {
+      // O from TMEM 32 columns at a time (the loads are warp-wide; rows past QR skip the
+      // stores only)
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(o_addr + c * 32, ov);
+        tmem_ld_wait();
+        if (r < a.QR && ok) {
+#pragma unroll
+          for (int d = 0; d < 32; d += 2)
+            attn_emit<bf16>(a, b, g, split, r, c * 32 + d, __uint_as_float(ov[d]),
+                            __uint_as_float(ov[d + 1]), l);
+        }
       }
     }
-    if (r < a.QR) {
+    if (!half && qrow < a.QR) {
       if (a.nsplit > 1) {
         const long long grp = (long long)b * a.hkv + g;
-        float* pm = a.part_ml + ((grp * a.nsplit + split) * a.QR + r) * 2;
+        float* pm = a.part_ml + ((grp * a.nsplit + split) * a.QR + qrow) * 2;
         pm[0] = mref;
         pm[1] = l;
       }

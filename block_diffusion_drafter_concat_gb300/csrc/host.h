@@ -77,9 +77,10 @@ dflash_status launch_gemm_f32(int epi, dim3 grid, const float* A, int lda, const
 dflash_status launch_attn_tc(int hd, int nw, dim3 grid, int smem, const AttnMaps& mp,
                              const AttnArgs<bf16>& a, cudaStream_t st);
 dflash_status launch_attn_f32(dim3 grid, int smem, const AttnArgs<float>& a, cudaStream_t st);
-// tu_attn_umma.cu: tcgen05 attention (head_dim 64, up to 128 query rows per kv head)
-dflash_status launch_attn_umma(int hd, dim3 grid, const AuMaps& mp, const AttnArgs<bf16>& a,
-                               cudaStream_t st);
+// tu_attn_umma.cu: tcgen05 attention (head_dim 64 with up to 128 query rows per kv head;
+// key-split mode for up to 64 rows, head_dim 64 or 128)
+dflash_status launch_attn_umma(int hd, bool ksplit, dim3 grid, const AuMaps& mp,
+                               const AttnArgs<bf16>& a, cudaStream_t st);
 dflash_status launch_attn_combine(int B, const AttnArgs<bf16>& a, cudaStream_t st);
 dflash_status launch_attn_combine(int B, const AttnArgs<float>& a, cudaStream_t st);
 

@@ -1,23 +1,26 @@
-// tcgen05 attention instantiation (head_dim 64).
+// tcgen05 attention instantiations: head_dim 64 with 128 query rows per kv head, and
+// head_dim 64 or 128 with at most 64 (key-split mode).
 #include "host.h"
 #include "attn_umma.cuh"
 
 namespace dflash {
 
-template <int HD>
+template <int HD, bool KSPLIT>
 static dflash_status one(dim3 grid, const AuMaps& mp, const AttnArgs<bf16>& a, cudaStream_t st) {
-  using C = AuCfg<HD>;
+  using C = AuCfg<HD, KSPLIT>;
   static bool set = false;
   if (!set) {
-    DFLASH_TRY(set_smem(k_attn_umma<HD>, C::SMEM));
+    DFLASH_TRY(set_smem(k_attn_umma<HD, KSPLIT>, C::SMEM));
     set = true;
   }
-  return launch(k_attn_umma<HD>, grid, dim3(C::THREADS), C::SMEM, st, mp, a);
+  return launch(k_attn_umma<HD, KSPLIT>, grid, dim3(C::THREADS), C::SMEM, st, mp, a);
 }
 
-dflash_status launch_attn_umma(int hd, dim3 grid, const AuMaps& mp, const AttnArgs<bf16>& a,
-                               cudaStream_t st) {
-  if (hd == 64) return one<64>(grid, mp, a, st);
+dflash_status launch_attn_umma(int hd, bool ksplit, dim3 grid, const AuMaps& mp,
+                               const AttnArgs<bf16>& a, cudaStream_t st) {
+  if (hd == 64 && !ksplit) return one<64, false>(grid, mp, a, st);
+  if (hd == 64 && ksplit) return one<64, true>(grid, mp, a, st);
+  if (hd == 128 && ksplit) return one<128, true>(grid, mp, a, st);
   return fail(DFLASH_EUNSUPPORTED, "tcgen05 attention: head_dim %d", hd);
 }
 
