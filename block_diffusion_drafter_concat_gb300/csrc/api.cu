@@ -278,10 +278,11 @@ AttnPlan plan_attn(const H* h, int B, int max_pages) {
   const int kp = max_pages + 1;
   const long long groups = (long long)B * h->c.n_kv_heads;
   if (use_attn_umma(h->c, B * h->c.block_size)) {
-    // tcgen05 kernel, two CTAs per SM, four pages per step: whole steps per split and
-    // the fewest waves of CTAs times steps per CTA (plus about three steps of per-CTA
-    // prologue and epilogue); among plans within 2 % of the best, the fewest splits.
-    const long long slots = 2LL * h->sms;
+    // tcgen05 kernel (two CTAs per SM at head_dim 64, one at 128), four pages per step:
+    // whole steps per split and the fewest waves of CTAs times steps per CTA (plus about
+    // three steps of per-CTA prologue and epilogue); among plans within 2 % of the best,
+    // the fewest splits.
+    const long long slots = (h->c.head_dim == 64 ? 2LL : 1LL) * h->sms;
     AttnPlan best{0, 0};
     long long best_cost = 0;
     for (int ns = 1; ns <= std::min(64, ceil_div(kp, 4)); ++ns) {

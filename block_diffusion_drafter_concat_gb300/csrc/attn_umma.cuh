@@ -155,7 +155,10 @@ struct AuCfg {
   static constexpr int KT = 64;                    // keys per step
   static constexpr int PG = KT / kPage;            // pages per step
   static constexpr int KB = HD / 64;               // 64-column blocks of a head
-  static constexpr int NS = HD == 64 ? 4 : 2;      // ring stages
+  // head_dim 128: one CTA per SM with a five-stage ring (two CTAs would leave room for
+  // two 32 KB stages each, one step of lookahead: the loads, not the softmax, bound it)
+  static constexpr int CPS = HD == 64 ? 2 : 1;     // CTAs per SM
+  static constexpr int NS = HD == 64 ? 4 : 5;      // ring stages
   static constexpr int NK = KSPLIT ? KT / 2 : KT;  // keys of a step per softmax thread
   static constexpr int Q_BYTES = 128 * HD * 2;
   static constexpr int KV_BLOCK = KT * 128;        // one 64-column block of K or V
@@ -176,7 +179,7 @@ struct AuCfg {
 };
 
 template <int HD, bool KSPLIT>
-__global__ void __launch_bounds__(192, 2)
+__global__ void __launch_bounds__(192, AuCfg<HD, KSPLIT>::CPS)
     k_attn_umma(const __grid_constant__ AuMaps maps, const AttnArgs<bf16> a) {
   using C = AuCfg<HD, KSPLIT>;
   extern __shared__ uint8_t smem_raw[];
