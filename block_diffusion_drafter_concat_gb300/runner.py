@@ -176,45 +176,6 @@ def step_flops(w: Workload, lens=None) -> int:
 
 
 def lm_head_bytes(w: Workload) -> int:
-    e = 2 if w.dtype == "bf16" else 4
-    return e * (w.vocab * w.d_model + w.rows * w.d_model) + w.rows * 12
-
-
-# ---------------------------------------------------------------------- roofline model
-def weight_bytes(w: Workload) -> int:
-    """Bytes of every weight one step streams once (the embedding contributes only the
-    block's rows)."""
-    e = 2 if w.dtype == "bf16" else 4
-    d, F = w.d_model, w.ffn_dim
-    per_layer = (w.q_width * d + 2 * w.kv_width * d + d * w.q_width + 3 * F * d + 2 * d)
-    return e * (d * w.fuse_in + d + w.n_layers * per_layer + d + w.vocab * d
-                + w.rows * d)
-
-
-def step_bytes(w: Workload, lens=None) -> int:
-    """Algorithmic HBM bytes of one step: weights once, context K/V read once, the S
-    new K/V rows written, target hidden features and verify logits read, outputs."""
-    e = 2 if w.dtype == "bf16" else 4
-    lens = inputs.ctx_lens(w) if lens is None else lens
-    kv_row = w.n_layers * 2 * w.kv_width * e
-    ctx = int(lens.sum()) * kv_row
-    new = w.rows * kv_row
-    return (weight_bytes(w) + ctx + new + w.rows * w.fuse_in * e + w.rows * w.vocab * e
-            + w.rows * w.d_model * e + w.rows * 4 * 4)
-
-
-def step_flops(w: Workload, lens=None) -> int:
-    lens = inputs.ctx_lens(w) if lens is None else lens
-    d, F, R = w.d_model, w.ffn_dim, w.rows
-    lin = 2 * R * (d * w.fuse_in + w.n_layers * (2 * w.kv_width * d)
-                   + w.n_layers * (w.q_width * d + 2 * w.kv_width * d + d * w.q_width
-                                   + 3 * F * d) + w.vocab * d)
-    keys = int(lens.sum()) + w.batch * w.block_size
-    attn = w.n_layers * 4 * w.block_size * w.n_q_heads * w.head_dim * keys
-    return lin + attn
-
-
-def lm_head_bytes(w: Workload) -> int:
     """Algorithmic bytes of one LM-head launch: the head's weights, the hidden rows, and
     the per-row token, max and log-sum-exp outputs."""
     e = 2 if w.dtype == "bf16" else 4
