@@ -21,6 +21,10 @@
 //               against a reference maximum in the log2 domain, write P; O accumulates
 //               in TMEM across steps and is rescaled in place only when the reference
 //               moves (when a probability could exceed 2^8)
+// Key-split mode (at most 64 query rows per kv head, head_dim 64 or 128): the rows are
+// loaded twice, into tile rows 0-63 and 64-127; lane r takes keys 0-31 of every step
+// and lane r + 64 keys 32-63 of the same query, each with its own reference, row sum
+// and O row, and the two states are merged after the last step.
 // Every wait is bounded; a role whose wait gives up raises the error word and stops.
 #pragma once
 
