@@ -50,7 +50,7 @@ def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return d["hbm_gbs"], d.get("bf16_tflops", 1958.0), "measured"
+        return d["hbm_gbs"], d.get("bf16_tflops", 1900.0), "measured"
     return 6800.0, 1900.0, "fallback"
 
 
