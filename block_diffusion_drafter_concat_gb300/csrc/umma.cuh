@@ -138,7 +138,8 @@ struct UmCfg {
   static constexpr int TMEM_COLS = 2 * BN;           // two fp32 accumulators
   static constexpr int MAXC = 512;                   // contributors of one split tile
   static constexpr int NBAR = 2 * NS + 5;            // full, empty, tfull[2], tempty[2], done
-  static constexpr int SMEM = 1024 + NS * STAGE + CS_BYTES + NBAR * 8 + 32 + MAXC * 4;
+  static constexpr int ROWS_BYTES = 256 * (4 + 8);     // rotary epilogue: positions, offsets
+  static constexpr int SMEM = 1024 + NS * STAGE + CS_BYTES + NBAR * 8 + 32 + MAXC * 4 + ROWS_BYTES;
   static constexpr int THREADS = 192;
   static constexpr uint32_t IDESC = umma_idesc_bf16<kBM, BN>();
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -158,6 +159,53 @@ __device__ __forceinline__ void resid_fetch(float4 (&x)[8], const EpiArgs<bf16>&
     const int r = w + 4 * k;
     if (r < mr)
       x[k] = reinterpret_cast<const float4*>(e.y + static_cast<long long>(m0 + r) * e.ldy + col0)[lane];
+  }
+}
+
+// Rotary / K-V epilogue, row information of output row m: the rotary position (-1 for
+// V rows, and for rows reported bad) and the base offset of its destination (-1 when
+// the row is reported bad), checked in the same order as the generic epilogue.
+template <int EPI>
+__device__ __forceinline__ void qkv_row_info(const EpiArgs<bf16>& e, int kind, int G, int m,
+                                             int& p, long long& base) {
+  const int hd = e.hd;
+  p = -1;
+  base = -1;
+  bool ok = true;
+  if (kind != 2) {
+    const int pp = e.pos[m];
+    ok = pp >= 0 && pp < e.max_pos;
+    if (!ok) raise_error(e.err, DFLASH_DEV_BAD_POSITION);
+    else p = pp;
+  }
+  if constexpr (EPI == EPI_QKV) {
+    const int b = m / e.S, ii = m - b * e.S;
+    if (ok)
+      base = kind == 0 ? (((long long)b * e.hkv * e.S + ii) * G) * hd   // + (gk*S*G + hh)*hd
+                       : ((long long)b * e.hkv * e.S + ii) * hd;        // + head*S*hd
+  } else {
+    const int slot = e.slots[m];
+    if (slot < 0 || slot >= e.num_slots) {
+      raise_error(e.err, DFLASH_DEV_BAD_INDEX);
+      ok = false;
+    }
+    if (ok) base = ((long long)(slot / kPage) * e.hkv * kPage + slot % kPage) * hd;
+  }
+  if (!ok) p = -1;
+}
+
+// Rotary table entries (cos, sin) of the rows w, w + 4, ..., w + 28 of a 32-row chunk
+// (positions from shared memory) for this lane's two pair indices jv[0], jv[1].
+__device__ __forceinline__ void rope_fetch(float2 (&cs)[8][2], const EpiArgs<bf16>& e,
+                                           const int* rp, int mr, const int (&jv)[2], int w) {
+  const int half = e.hd >> 1;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int r = w + 4 * q;
+    const int p = r < mr ? rp[r] : -1;
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      cs[q][k] = p >= 0 ? e.rope[(long long)p * half + jv[k]] : make_float2(0.f, 0.f);
   }
 }
 
@@ -198,6 +246,8 @@ __global__ void __launch_bounds__(192, 1)
   uint32_t* tbase = reinterpret_cast<uint32_t*>(done + 1);
   int* flag = reinterpret_cast<int*>(tbase + 4);
   int* cslot = flag + 4;
+  int* rpos = cslot + C::MAXC;                                       // [256]
+  long long* rowbase = reinterpret_cast<long long*>(rpos + 256);     // [256]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grid = gridDim.x, cta = blockIdx.x;
@@ -359,6 +409,54 @@ __global__ void __launch_bounds__(192, 1)
       float4 xres[8];
       if (resid_pipe)
         resid_fetch(xres, e, m_first, min(C::CH, rows), nt * kBM, ncol, et >> 5, lane);
+      // Rotary / K-V epilogue of a whole tile: the tile's positions and destination
+      // offsets go to shared memory and the rotary entries of chunk c + 1 are loaded
+      // while chunk c is finished (chunk 0's while the accumulator is computed).
+      constexpr bool kRope = EPI == EPI_QKV || EPI == EPI_KV;
+      const bool rope_pipe = kRope && whole;
+      int kind = 0, layer = 0, r0 = 0;
+      int cv[2] = {0, 0}, hv[2] = {0, 0}, jv[2] = {0, 0};
+      float2 csr[8][2];
+      if constexpr (kRope) {
+        if (rope_pipe) {
+          int seg = 0;
+          while (seg + 1 < g.nseg && nt >= g.seg_tile0[seg + 1]) ++seg;
+          r0 = (nt - g.seg_tile0[seg]) * kBM;               // first row within the segment
+          if constexpr (EPI == EPI_QKV) {
+            kind = seg;
+          } else {
+            layer = seg >> 1;
+            kind = 1 + (seg & 1);
+          }
+          const int hd = e.hd, half = hd >> 1;
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            if (kind == 2) {
+              // V: lane -> columns 2*lane + 64*k, head and offset fixed per lane
+              const int f = r0 + 2 * lane + 64 * k;
+              hv[k] = f / hd;
+              jv[k] = f - hv[k] * hd;
+              cv[k] = 2 * lane + 64 * k;
+            } else {
+              // rotary pairs (j, j + hd/2) of one head lie in the same 128-column tile:
+              // lane -> pair indices lane and lane + 32 of the tile's 64 pairs
+              const int cc = lane + 32 * k;
+              const int hl = cc / half;
+              jv[k] = cc - hl * half;
+              cv[k] = hl * hd + jv[k];
+              hv[k] = (r0 + cv[k]) / hd;
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int rr = et + 128 * k;
+            if (rr < rows)
+              qkv_row_info<EPI>(e, kind, e.hq / e.hkv, m_first + rr, rpos[rr], rowbase[rr]);
+          }
+          epi_sync();
+          if (kind != 2) rope_fetch(csr, e, rpos, min(C::CH, rows), jv, et >> 5);
+        }
+      }
       if (ok && !__all_sync(0xffffffffu, mbar_wait(&tfull[ab], use & 1))) {
         if (lane == 0) raise_error(e.err, DFLASH_DEV_TIMEOUT);
         ok = false;
@@ -382,7 +480,73 @@ __global__ void __launch_bounds__(192, 1)
         }
       };
 
-      if (resid_pipe) {
+      if (kRope && rope_pipe) {
+        const int hd = e.hd, half = hd >> 1, G = e.hq / e.hkv;
+        const int nheads = kind == 0 ? e.hq : e.hkv;
+        const int w = et >> 5;
+        for (int c = 0; c < nch; ++c) {
+          uint32_t v[32];
+          read_chunk(c, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) Cs[j * C::PITCH + feat] = __uint_as_float(v[j]);
+          epi_sync();
+          const int mr = min(C::CH, rows - c * C::CH);
+          float2 csn[8][2];
+          if (kind != 2 && c + 1 < nch)
+            rope_fetch(csn, e, rpos + (c + 1) * C::CH, min(C::CH, rows - (c + 1) * C::CH), jv, w);
+          if (ok) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int r = w + 4 * q;
+              if (r >= mr) continue;
+              const int row = c * C::CH + r;
+              const long long base = rowbase[row];
+              if (base < 0) continue;
+              if (kind == 2) {
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                  if (hv[k] >= e.hkv) continue;
+                  const float2 x = *reinterpret_cast<const float2*>(Cs + r * C::PITCH + cv[k]);
+                  if constexpr (EPI == EPI_QKV) {
+                    store_pair<bf16>(e.vb + base + (long long)hv[k] * e.S * hd + jv[k], x.x, x.y);
+                  } else {
+                    store_pair<bf16>(e.vpool[layer] + base + (long long)hv[k] * kPage * hd + jv[k],
+                                     x.x, x.y);
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                  const int head = hv[k];
+                  if (head >= nheads) continue;
+                  const float x0 = Cs[r * C::PITCH + cv[k]], x1 = Cs[r * C::PITCH + cv[k] + half];
+                  const bf16 y0 = from_f32<bf16>(x0 * csr[q][k].x - x1 * csr[q][k].y);
+                  const bf16 y1 = from_f32<bf16>(x1 * csr[q][k].x + x0 * csr[q][k].y);
+                  bf16* dst;
+                  if constexpr (EPI == EPI_QKV) {
+                    if (kind == 0) {
+                      const int gk = head / G, hh = head - gk * G;
+                      dst = e.q + base + ((long long)gk * e.S * G + hh) * hd;
+                    } else {
+                      dst = e.kb + base + (long long)head * e.S * hd;
+                    }
+                  } else {
+                    dst = e.kpool[layer] + base + (long long)head * kPage * hd;
+                  }
+                  dst[jv[k]] = y0;
+                  dst[jv[k] + half] = y1;
+                }
+              }
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            csr[q][0] = csn[q][0];
+            csr[q][1] = csn[q][1];
+          }
+          epi_sync();
+        }
+      } else if (resid_pipe) {
         for (int c = 0; c < nch; ++c) {
           uint32_t v[32];
           read_chunk(c, v);
