@@ -195,7 +195,8 @@ __device__ __forceinline__ void qkv_row_info(const EpiArgs<bf16>& e, int kind, i
 }
 
 // Rotary table entries (cos, sin) of the rows w, w + 4, ..., w + 28 of a 32-row chunk
-// (positions from shared memory) for this lane's two pair indices jv[0], jv[1].
+// (positions from shared memory) for this lane's adjacent pair indices jv[0], jv[0] + 1:
+// one 16-byte load per row.
 __device__ __forceinline__ void rope_fetch(float2 (&cs)[8][2], const EpiArgs<bf16>& e,
                                            const int* rp, int mr, const int (&jv)[2], int w) {
   const int half = e.hd >> 1;
@@ -203,9 +204,10 @@ __device__ __forceinline__ void rope_fetch(float2 (&cs)[8][2], const EpiArgs<bf1
   for (int q = 0; q < 8; ++q) {
     const int r = w + 4 * q;
     const int p = r < mr ? rp[r] : -1;
-#pragma unroll
-    for (int k = 0; k < 2; ++k)
-      cs[q][k] = p >= 0 ? e.rope[(long long)p * half + jv[k]] : make_float2(0.f, 0.f);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p >= 0) v = *reinterpret_cast<const float4*>(e.rope + (long long)p * half + jv[0]);
+    cs[q][0] = make_float2(v.x, v.y);
+    cs[q][1] = make_float2(v.z, v.w);
   }
 }
 
@@ -439,8 +441,9 @@ __global__ void __launch_bounds__(192, 1)
               cv[k] = 2 * lane + 64 * k;
             } else {
               // rotary pairs (j, j + hd/2) of one head lie in the same 128-column tile:
-              // lane -> pair indices lane and lane + 32 of the tile's 64 pairs
-              const int cc = lane + 32 * k;
+              // lane -> the adjacent pair indices 2*lane and 2*lane + 1 of the tile's 64
+              // pairs (same head: half is even), stored as bf16 pairs
+              const int cc = 2 * lane + k;
               const int hl = cc / half;
               jv[k] = cc - hl * half;
               cv[k] = hl * hd + jv[k];
@@ -515,13 +518,10 @@ __global__ void __launch_bounds__(192, 1)
                   }
                 }
               } else {
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                  const int head = hv[k];
-                  if (head >= nheads) continue;
-                  const float x0 = Cs[r * C::PITCH + cv[k]], x1 = Cs[r * C::PITCH + cv[k] + half];
-                  const bf16 y0 = from_f32<bf16>(x0 * csr[q][k].x - x1 * csr[q][k].y);
-                  const bf16 y1 = from_f32<bf16>(x1 * csr[q][k].x + x0 * csr[q][k].y);
+                const int head = hv[0];   // both pair indices belong to this head
+                if (head < nheads) {
+                  const float2 a = *reinterpret_cast<const float2*>(Cs + r * C::PITCH + cv[0]);
+                  const float2 bb = *reinterpret_cast<const float2*>(Cs + r * C::PITCH + cv[0] + half);
                   bf16* dst;
                   if constexpr (EPI == EPI_QKV) {
                     if (kind == 0) {
@@ -533,8 +533,10 @@ __global__ void __launch_bounds__(192, 1)
                   } else {
                     dst = e.kpool[layer] + base + (long long)head * kPage * hd;
                   }
-                  dst[jv[k]] = y0;
-                  dst[jv[k] + half] = y1;
+                  store_pair<bf16>(dst + jv[0], a.x * csr[q][0].x - bb.x * csr[q][0].y,
+                                   a.y * csr[q][1].x - bb.y * csr[q][1].y);
+                  store_pair<bf16>(dst + jv[0] + half, bb.x * csr[q][0].x + a.x * csr[q][0].y,
+                                   bb.y * csr[q][1].x + a.y * csr[q][1].y);
                 }
               }
             }
