@@ -214,11 +214,13 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
       }
     } else {
       // rotary pairs (j, j + hd/2) of one head lie in the same 128-column tile; lane ->
-      // pair indices lane and lane + 32 of the tile's 64 pairs
+      // the adjacent pair indices 2*lane and 2*lane + 1 of the tile's 64 pairs when half
+      // head_dim is even (one head: results stored as pairs), else lane and lane + 32
+      const bool adj = (half & 1) == 0;
       int cv[2], hv[2], jv[2];
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const int cc = lane + 32 * k;
+        const int cc = adj ? 2 * lane + k : lane + 32 * k;
         const int hl = cc / half;
         jv[k] = cc - hl * half;
         cv[k] = hl * hd + jv[k];
@@ -263,34 +265,53 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
         }
         float2 cs[RR][2];
 #pragma unroll
-        for (int q = 0; q < RR; ++q)
+        for (int q = 0; q < RR; ++q) {
+          if (adj) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (pv[q] >= 0) v = *reinterpret_cast<const float4*>(e.rope + (long long)pv[q] * half + jv[0]);
+            cs[q][0] = make_float2(v.x, v.y);
+            cs[q][1] = make_float2(v.z, v.w);
+          } else {
 #pragma unroll
-          for (int k = 0; k < 2; ++k)
-            cs[q][k] = pv[q] >= 0 ? e.rope[(long long)pv[q] * half + jv[k]] : make_float2(0.f, 0.f);
+            for (int k = 0; k < 2; ++k)
+              cs[q][k] = pv[q] >= 0 ? e.rope[(long long)pv[q] * half + jv[k]] : make_float2(0.f, 0.f);
+          }
+        }
+        auto dst_of = [&](int head, long long base) -> T* {
+          if constexpr (EPI == EPI_QKV) {
+            if (kind == 0) {
+              const int gk = head / G, hh = head - gk * G;
+              return e.q + base + ((long long)gk * e.S * G + hh) * hd;
+            }
+            return e.kb + base + (long long)head * e.S * hd;
+          } else {
+            return e.kpool[layer] + base + (long long)head * kPage * hd;
+          }
+        };
 #pragma unroll
         for (int q = 0; q < RR; ++q) {
           const int r = rb + q * nw;
           if (pv[q] < 0) continue;   // past the chunk, or reported above
+          float y0[2], y1[2];
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
-            const int head = hv[k];
-            if (head >= nheads) continue;
             const float x0 = Cs[r * pitch + cv[k]], x1 = Cs[r * pitch + cv[k] + half];
-            const T y0 = from_f32<T>(x0 * cs[q][k].x - x1 * cs[q][k].y);
-            const T y1 = from_f32<T>(x1 * cs[q][k].x + x0 * cs[q][k].y);
-            T* dst;
-            if constexpr (EPI == EPI_QKV) {
-              if (kind == 0) {
-                const int gk = head / G, hh = head - gk * G;
-                dst = e.q + rbase[q] + ((long long)gk * e.S * G + hh) * hd;
-              } else {
-                dst = e.kb + rbase[q] + (long long)head * e.S * hd;
-              }
-            } else {
-              dst = e.kpool[layer] + rbase[q] + (long long)head * kPage * hd;
+            y0[k] = x0 * cs[q][k].x - x1 * cs[q][k].y;
+            y1[k] = x1 * cs[q][k].x + x0 * cs[q][k].y;
+          }
+          if (adj) {
+            if (hv[0] >= nheads) continue;   // both indices belong to head hv[0]
+            T* dst = dst_of(hv[0], rbase[q]);
+            store_pair<T>(dst + jv[0], y0[0], y0[1]);
+            store_pair<T>(dst + jv[0] + half, y1[0], y1[1]);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              if (hv[k] >= nheads) continue;
+              T* dst = dst_of(hv[k], rbase[q]);
+              dst[jv[k]] = from_f32<T>(y0[k]);
+              dst[jv[k] + half] = from_f32<T>(y1[k]);
             }
-            dst[jv[k]] = y0;
-            dst[jv[k] + half] = y1;
           }
         }
       }

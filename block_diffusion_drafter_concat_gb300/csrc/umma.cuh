@@ -415,7 +415,8 @@ __global__ void __launch_bounds__(192, 1)
       // offsets go to shared memory and the rotary entries of chunk c + 1 are loaded
       // while chunk c is finished (chunk 0's while the accumulator is computed).
       constexpr bool kRope = EPI == EPI_QKV || EPI == EPI_KV;
-      const bool rope_pipe = kRope && whole;
+      // (pairs of adjacent rotary indices need an even half head_dim)
+      const bool rope_pipe = kRope && whole && (e.hd & 3) == 0;
       int kind = 0, layer = 0, r0 = 0;
       int cv[2] = {0, 0}, hv[2] = {0, 0}, jv[2] = {0, 0};
       float2 csr[8][2];
