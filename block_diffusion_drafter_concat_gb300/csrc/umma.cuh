@@ -19,6 +19,10 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator 32 activation rows at a time
 //               (warp w reads TMEM lanes 32*(w%4)..+31, i.e. those weight rows), fp32
 //               tile chunk in shared memory, then the fused epilogue of the projection.
+//               For whole tiles the residual and rotary / K-V epilogues fetch what they
+//               read from memory (residual rows; positions, destination offsets and
+//               rotary entries) one chunk ahead, the first chunk's while the
+//               accumulator is still being computed.
 // Two TMEM accumulators let the MMA of the next tile piece run under the epilogue of
 // the previous one.  Every mbarrier wait is bounded; a wait that gives up raises the
 // device error word and its role stops waiting, so the CTA always reaches the final
