@@ -41,6 +41,15 @@ SMALL = {
     "small-bf16-hd64-g4-b5-tc": configs.small_bf16(
         name="small-bf16-hd64-g4-b5-tc", d_model=384, n_q_heads=8, n_kv_heads=2,
         head_dim=64, ffn_dim=384, vocab=2176, batch=5, ctx_range=(20, 180), seed=20),
+    # one-page contexts (16 tokens: the split's single step holds the context page and
+    # the block, so the tcgen05 key-split lanes of the step's second half see no valid
+    # key) with 96 block rows at head_dim 128, and a mix of one- and two-page contexts
+    # with 80 block rows at head_dim 64 (64 query rows per kv head)
+    "small-bf16-b6-tc128-short": configs.small_bf16(
+        name="small-bf16-b6-tc128-short", batch=6, ctx_range=(16, 16), seed=22),
+    "small-bf16-hd64-g4-b5-short": configs.small_bf16(
+        name="small-bf16-hd64-g4-b5-short", d_model=384, n_q_heads=8, n_kv_heads=2,
+        head_dim=64, ffn_dim=384, vocab=2176, batch=5, ctx_range=(16, 24), seed=23),
     # 256 rows with K = 1024 and a 32000-token vocabulary: whole tiles per CTA as well
     "mid-bf16-b16-tc256": configs.small_bf16(
         name="mid-bf16-b16-tc256", d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128,
