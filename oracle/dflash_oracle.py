@@ -256,3 +256,166 @@ def draft_step(x_cat, ctx_len, block_ids, W, cfg, bf16):
     z = lm_head(h, W["lm_head"])
     return dict(fused=fused, K=K, V=V, h=h, z=z, draft=argmax_lowest(z),
                 margin=top2_margin(z))
+
+
+# ------------------------------------------------ causal passes (input fusion, target)
+def causal_attention(q, k, v, n_kv_heads, n_prefix):
+    """softmax(q k^T / sqrt(head_dim)) v for Sq new tokens after n_prefix cached ones:
+    new token i sees the n_prefix cached keys and the new keys 0..i.
+
+    q [Sq, hq, hd]; k, v [n_prefix + Sq, hkv, hd]; q head h reads kv head h // (hq // hkv)."""
+    sq, hq, hd = q.shape
+    group = hq // n_kv_heads
+    seen = np.arange(n_prefix + sq)[None, :] <= n_prefix + np.arange(sq)[:, None]   # [Sq, Tk]
+    out = np.zeros((sq, hq, hd))
+    for h in range(hq):
+        g = h // group
+        scores = q[:, h, :] @ k[:, g, :].T / np.sqrt(hd)
+        scores = np.where(seen, scores, -np.inf)
+        scores = scores - scores.max(axis=1, keepdims=True)
+        p = np.exp(scores)
+        p = p / p.sum(axis=1, keepdims=True)
+        out[:, h, :] = p @ v[:, g, :]
+    return out
+
+
+def causal_stack(x, W, cfg, bf16, tap_layers=()):
+    """The layer stack run causally over a whole sequence of N tokens at positions
+    0..N-1 whose layer-0 inputs are the rows of x [N, d] (a token embedding, or fused
+    target features in the input-fusion variant): per layer RMSNorm, Q/K/V + RoPE,
+    causal attention (token i sees tokens 0..i), output projection + residual, RMSNorm,
+    SwiGLU MLP + residual, with the rounding points of draft_block.
+
+    Returns (K, V, taps, h): per-layer K/V [N, hkv, hd] (what a cache holds), the
+    residual stream after each layer in tap_layers (1-based) concatenated [N, n*d]
+    (rounded like a stored feature), and the final RMSNorm output h [N, d]."""
+    eps, theta = cfg.rms_eps, cfg.rope_theta
+    hq, hkv = cfg.n_q_heads, cfg.n_kv_heads
+    x = np.asarray(x, dtype=np.float64)
+    N = x.shape[0]
+    pos = np.arange(N)
+    K, V, taps = [], [], {}
+    for l in range(cfg.n_layers):
+        L = lambda name: W[f"l{l}.{name}"]  # noqa: E731
+        n = _maybe_bf16(rms_norm(x, L("g_attn"), eps), bf16)
+        q = _maybe_bf16(rope((n @ L("w_q").T).reshape(N, hq, -1), pos, theta), bf16)
+        k = _maybe_bf16(rope((n @ L("w_k").T).reshape(N, hkv, -1), pos, theta), bf16)
+        v = _maybe_bf16((n @ L("w_v").T).reshape(N, hkv, -1), bf16)
+        K.append(k)
+        V.append(v)
+        o = _maybe_bf16(causal_attention(q, k, v, hkv, 0).reshape(N, -1), bf16)
+        x = x + o @ L("w_o").T
+        n2 = _maybe_bf16(rms_norm(x, L("g_mlp"), eps), bf16)
+        act = _maybe_bf16(silu(n2 @ L("w_gate").T) * (n2 @ L("w_up").T), bf16)
+        x = x + act @ L("w_down").T
+        if l + 1 in tap_layers:
+            taps[l + 1] = _maybe_bf16(x, bf16)
+    tap = np.concatenate([taps[t] for t in tap_layers], axis=1) if tap_layers else None
+    return K, V, tap, _maybe_bf16(rms_norm(x, W["g_final"], eps), bf16)
+
+
+def input_fusion_context(fused, W, cfg, bf16):
+    """[DFlash FAQ 1, the input-fusion ablation] the fused target features of the
+    context tokens are the drafter's input: they run through the drafter's layers
+    causally (full per-token processing, which KV injection skips) and each layer's
+    K/V of the context tokens are what the block then attends to.  Returns (K, V)."""
+    K, V, _, _ = causal_stack(fused, W, cfg, bf16)
+    return K, V
+
+
+def draft_step_input_fusion(x_cat, ctx_len, block_ids, W, cfg, bf16):
+    """draft_step for the input-fusion variant: fuse the context features, run them
+    through the layer stack (input_fusion_context), draft the block, LM head."""
+    fused = fuse_features(x_cat[:ctx_len], W["w_fuse"], W["g_fuse"], cfg.rms_eps, bf16)
+    K, V = input_fusion_context(fused, W, cfg, bf16)
+    h = draft_block(K, V, ctx_len, block_ids, W, cfg, bf16)
+    z = lm_head(h, W["lm_head"])
+    return dict(fused=fused, K=K, V=V, h=h, z=z, draft=argmax_lowest(z), margin=top2_margin(z))
+
+
+def target_forward(tokens, Wt, cfg_t, bf16, tap_layers):
+    """A plain causal transformer (the target of the speculative loop) over tokens
+    0..N-1: returns (taps [N, n_taps*d], logits [N, V]); row p of the logits scores the
+    token at position p + 1."""
+    x = np.asarray(Wt["embed"], dtype=np.float64)[np.asarray(tokens)]
+    _, _, taps, h = causal_stack(x, Wt, cfg_t, bf16, tap_layers)
+    return taps, lm_head(h, Wt["lm_head"])
+
+
+def plant_agreement(logits, drafts, u, p):
+    """Synthetic agreement of the loop's target with the drafter (no trained pair exists
+    here): row i of the block's target logits gets logit[draft_{i+1}] = max_i + 1 when
+    u_i < p (i < S-1).  Returns a planted copy."""
+    out = np.array(logits, dtype=np.float64, copy=True)
+    for i in range(out.shape[0] - 1):
+        if u[i] < p:
+            out[i, drafts[i + 1]] = out[i].max() + 1.0
+    return out
+
+
+def spec_step(committed, draft_fn, Wt, cfg_t, bf16, tap_layers, S, plant_u=None, plant_p=0.0):
+    """[DFlash wiki, 사용법 (spec_generate); NVIDIA blog, how it works: draft a block,
+    verify it with the target in one pass, accept the longest valid prefix] one step of
+    greedy speculative decoding.  committed: the tokens so far (the last one is the
+    anchor, not yet processed by the target).  draft_fn(committed, feats) -> drafts
+    [S] for block slots 1..S-1 (slot 0 is the anchor; drafts[0] is ignored), where feats
+    are the target's tap features of tokens 0..len-2.
+
+    The target runs over [committed ; drafts 1..S-1]; its logits at the anchor and the
+    drafts, t_i = argmax row i (lowest index), accept d_{i+1} while it equals t_i; the
+    emitted tokens are t_0..t_n (the accepted drafts and one target token).
+    Returns (emitted tokens, n accepted, drafts, the block's target logits)."""
+    N = len(committed)
+    feats, _ = target_forward(committed[:N - 1], Wt, cfg_t, bf16, tap_layers) if N > 1 else \
+        (None, None)
+    drafts = np.asarray(draft_fn(committed, feats))
+    seq = np.concatenate([committed, drafts[1:S]])
+    _, logits = target_forward(seq, Wt, cfg_t, bf16, tap_layers)
+    block = logits[N - 1:N - 1 + S]
+    if plant_u is not None:
+        block = plant_agreement(block, drafts, plant_u, plant_p)
+    t = argmax_lowest(block)
+    n = 0
+    while n < S - 1 and drafts[n + 1] == t[n]:
+        n += 1
+    return t[:n + 1], n, drafts, block
+
+
+def greedy_decode(prompt, n_new, Wt, cfg_t, bf16):
+    """Plain autoregressive greedy decoding of the target (the reference that lossless
+    speculative decoding must reproduce token for token)."""
+    seq = list(prompt)
+    for _ in range(n_new):
+        _, logits = target_forward(np.asarray(seq), Wt, cfg_t, bf16, ())
+        seq.append(int(argmax_lowest(logits[-1])))
+    return seq[len(prompt):]
+
+
+def dflash_drafter(W, cfg, bf16, mask_id=0, variant="kv"):
+    """draft_fn of spec_step for the DFlash drafter: fuse the context's target features,
+    put them into every layer's K/V (variant "kv": inject_kv at positions 0..T-1;
+    "input": input_fusion_context), draft the block [anchor, mask, ..., mask] at
+    positions T..T+S-1, LM-head argmax.  The function also records each call's logits
+    in fn.calls (for margin checks)."""
+    S = cfg.block_size
+
+    def fn(committed, feats):
+        T = len(committed) - 1
+        fused = fuse_features(feats, W["w_fuse"], W["g_fuse"], cfg.rms_eps, bf16)
+        if variant == "kv":
+            K, V = [], []
+            for l in range(cfg.n_layers):
+                k, v = inject_kv(fused, np.arange(T), W[f"l{l}.w_k"], W[f"l{l}.w_v"],
+                                 cfg.n_kv_heads, cfg.rope_theta, bf16)
+                K.append(k)
+                V.append(v)
+        else:
+            K, V = input_fusion_context(fused, W, cfg, bf16)
+        ids = np.full(S, mask_id)
+        ids[0] = committed[-1]
+        z = lm_head(draft_block(K, V, T, ids, W, cfg, bf16), W["lm_head"])
+        fn.calls.append(z)
+        return argmax_lowest(z)
+
+    fn.calls = []
+    return fn

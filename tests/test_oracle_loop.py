@@ -1,0 +1,175 @@
+"""Pins of the oracle's causal passes, its input-fusion variant and its speculative loop
+against facts other than themselves: explicit per-query/per-key loops, causality
+(prefix invariance), the layer-0 identity between input fusion and KV injection, and
+the losslessness of greedy speculative decoding (the loop reproduces the target's own
+autoregressive greedy decoding whatever the drafter proposes).  CPU only."""
+from types import SimpleNamespace
+
+import numpy as np
+import pytest
+
+from oracle import dflash_oracle as O
+
+from test_oracle import tiny_cfg, tiny_weights
+
+
+def _brute_causal(q, k, v, hkv, n_prefix):
+    sq, hq, hd = q.shape
+    out = np.zeros_like(q)
+    for i in range(sq):
+        for h in range(hq):
+            g = h // (hq // hkv)
+            keys = range(n_prefix + i + 1)
+            s = [float(q[i, h] @ k[j, g]) / np.sqrt(hd) for j in keys]
+            m = max(s)
+            e = [np.exp(x - m) for x in s]
+            out[i, h] = sum(e[j] * v[j, g] for j in keys) / sum(e)
+    return out
+
+
+@pytest.mark.parametrize("sq,hq,hkv,hd,prefix", [(4, 4, 2, 8, 3), (1, 2, 1, 4, 0), (5, 6, 3, 2, 0)])
+def test_causal_attention_matches_explicit_loop(sq, hq, hkv, hd, prefix):
+    rng = np.random.default_rng(sq * 100 + prefix)
+    q = rng.normal(0, 1, (sq, hq, hd))
+    k = rng.normal(0, 1, (prefix + sq, hkv, hd))
+    v = rng.normal(0, 1, (prefix + sq, hkv, hd))
+    np.testing.assert_allclose(O.causal_attention(q, k, v, hkv, prefix),
+                               _brute_causal(q, k, v, hkv, prefix), rtol=1e-12, atol=1e-12)
+
+
+def test_causal_attention_first_token_without_prefix_returns_its_value():
+    rng = np.random.default_rng(3)
+    q, k, v = (rng.normal(0, 1, (3, 2, 4)) for _ in range(3))
+    out = O.causal_attention(q, k, v, 2, 0)
+    np.testing.assert_allclose(out[0], v[0], rtol=1e-14)
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_causal_stack_is_prefix_invariant(bf16):
+    """Token p's K/V, taps and final state do not depend on the tokens after it."""
+    cfg = tiny_cfg(block_size=4)
+    rng = np.random.default_rng(5)
+    W = tiny_weights(cfg, rng)
+    x = rng.normal(0, 1, (11, cfg.d))
+    K1, V1, t1, h1 = O.causal_stack(x[:7], W, cfg, bf16, (1, 2))
+    K2, V2, t2, h2 = O.causal_stack(x, W, cfg, bf16, (1, 2))
+    # fp64 products of different lengths may round their last bit differently; bf16
+    # rounding of this seed's values lands the same way
+    same = (np.testing.assert_array_equal if bf16 else
+            lambda a, b: np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12))
+    for l in range(cfg.n_layers):
+        same(K1[l], K2[l][:7])
+        same(V1[l], V2[l][:7])
+    same(t1, t2[:7])
+    same(h1, h2[:7])
+    assert not np.allclose(h2[7:], 0)
+
+
+def test_input_fusion_layer0_kv_equals_kv_injection_with_unit_gains():
+    """With unit gains the fused rows are already RMS-normalised, so the pre-attention
+    norm of layer 0 leaves them unchanged (up to eps) and the input-fusion drafter's
+    layer-0 K/V are the KV-injection K/V of the same fused rows."""
+    cfg = tiny_cfg(block_size=4)
+    rng = np.random.default_rng(6)
+    W = tiny_weights(cfg, rng)
+    W["l0.g_attn"] = np.ones(cfg.d)
+    Lh = 3
+    x_cat = rng.normal(0, 1, (9, Lh * cfg.d))
+    W["w_fuse"] = rng.normal(0, 0.3, (cfg.d, Lh * cfg.d))
+    W["g_fuse"] = np.ones(cfg.d)
+    fused = O.fuse_features(x_cat, W["w_fuse"], W["g_fuse"], 0.0, False)
+    K, V = O.input_fusion_context(fused, W, SimpleNamespace(**{**vars(cfg), "rms_eps": 0.0}),
+                                  False)
+    k0, v0 = O.inject_kv(fused, np.arange(9), W["l0.w_k"], W["l0.w_v"], cfg.n_kv_heads,
+                         cfg.rope_theta, False)
+    np.testing.assert_allclose(K[0], k0, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(V[0], v0, rtol=1e-12, atol=1e-12)
+    # deeper layers see the mixed context, so they differ from injecting the rows
+    k1, _ = O.inject_kv(fused, np.arange(9), W["l1.w_k"], W["l1.w_v"], cfg.n_kv_heads,
+                        cfg.rope_theta, False)
+    assert not np.allclose(K[1], k1)
+
+
+def _loop(prompt, draft_fn, Wt, cfg, n_new, plant=None):
+    seq, accepted = list(prompt), []
+    step = 0
+    while len(seq) - len(prompt) < n_new:
+        u = None if plant is None else plant[0][step]
+        em, n, _, _ = O.spec_step(np.asarray(seq), draft_fn, Wt, cfg, False, (1, 2),
+                                  cfg.block_size, u, 0.0 if plant is None else plant[1])
+        assert len(em) == n + 1 and 0 <= n <= cfg.block_size - 1
+        seq += [int(t) for t in em]
+        accepted.append(n)
+        step += 1
+    return seq[len(prompt):len(prompt) + n_new], accepted
+
+
+def test_speculative_loop_is_lossless_for_any_drafter():
+    """Greedy speculative decoding emits exactly the target's greedy continuation:
+    with a perfect drafter (every draft accepted, S tokens per step), with a random one
+    (only the target's token each step) and with one wrong at a fixed slot."""
+    cfg = tiny_cfg(block_size=4)
+    rng = np.random.default_rng(7)
+    Wt = tiny_weights(cfg, rng)
+    prompt = rng.integers(0, cfg.V, 6)
+    n_new = 13
+    ref = O.greedy_decode(prompt, n_new + cfg.block_size, Wt, cfg, False)
+
+    def perfect(committed, feats):
+        cont = O.greedy_decode(committed, cfg.block_size - 1, Wt, cfg, False)
+        return np.concatenate([[committed[-1]], cont])
+
+    def wrong_at_2(committed, feats):
+        d = perfect(committed, feats)
+        d[2] = (d[2] + 1) % cfg.V
+        return d
+
+    out, acc = _loop(prompt, perfect, Wt, cfg, n_new)
+    assert out == ref[:n_new] and all(a == cfg.block_size - 1 for a in acc)
+    out, acc = _loop(prompt, lambda c, f: rng.integers(0, cfg.V, cfg.block_size), Wt, cfg, n_new)
+    assert out == ref[:n_new]
+    out, acc = _loop(prompt, wrong_at_2, Wt, cfg, n_new)
+    assert out == ref[:n_new] and all(a == 1 for a in acc)
+
+
+def test_planted_agreement_accepts_every_planted_prefix():
+    """With every position planted the target takes the drafts: S-1 accepted drafts plus
+    the target's token at the last slot; with none planted a random drafter is refused."""
+    cfg = tiny_cfg(block_size=4)
+    rng = np.random.default_rng(8)
+    Wt = tiny_weights(cfg, rng)
+    prompt = rng.integers(0, cfg.V, 5)
+    rnd = lambda c, f: rng.integers(0, cfg.V, cfg.block_size)  # noqa: E731
+    ones = np.zeros((20, cfg.block_size))
+    _, acc = _loop(prompt, rnd, Wt, cfg, 12, plant=(ones, 1.0))
+    assert all(a == cfg.block_size - 1 for a in acc)
+    z = rng.normal(0, 1, (cfg.block_size, cfg.V))
+    d = rng.integers(0, cfg.V, cfg.block_size)
+    u = np.array([0.1, 0.9, 0.2, 0.0])
+    p = O.plant_agreement(z, d, u, 0.5)
+    assert O.argmax_lowest(p)[0] == d[1] and O.argmax_lowest(p)[2] == d[3]
+    np.testing.assert_array_equal(p[1], z[1])
+    np.testing.assert_array_equal(p[3], z[3])      # the last row scores no draft
+
+
+def test_target_forward_is_causal_and_drafter_matches_the_step_path():
+    """The target's logits at position p ignore later tokens; the loop's DFlash drafter
+    (fuse the target's taps, inject, draft [anchor, mask...]) equals the step path of
+    draft_step on the same features with the anchor's id in slot 0."""
+    cfg = tiny_cfg(block_size=4)
+    rng = np.random.default_rng(9)
+    Wt = tiny_weights(cfg, rng)
+    toks = rng.integers(0, cfg.V, 10)
+    taps6, lg6 = O.target_forward(toks[:6], Wt, cfg, False, (1, 2))
+    taps10, lg10 = O.target_forward(toks, Wt, cfg, False, (1, 2))
+    np.testing.assert_allclose(lg6, lg10[:6], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(taps6, taps10[:6], rtol=1e-12, atol=1e-12)
+    Wd = tiny_weights(cfg, rng)
+    Wd["embed"], Wd["lm_head"] = Wt["embed"], Wt["lm_head"]
+    Wd["w_fuse"] = rng.normal(0, 0.3, (cfg.d, 2 * cfg.d))
+    Wd["g_fuse"] = 1 + rng.normal(0, 0.1, cfg.d)
+    fn = O.dflash_drafter(Wd, cfg, False, mask_id=0)
+    d = fn(toks[:7], taps6)
+    ids = np.array([toks[6], 0, 0, 0])
+    ref = O.draft_step(taps6, 6, ids, Wd, cfg, False)
+    np.testing.assert_array_equal(d, ref["draft"])
