@@ -419,3 +419,46 @@ def dflash_drafter(W, cfg, bf16, mask_id=0, variant="kv"):
 
     fn.calls = []
     return fn
+
+
+# ------------------------------------------------------- low-precision weight streaming
+E4M3_MAX = 448.0   # largest finite float8 e4m3 value: 1.75 * 2^8
+
+
+def round_e4m3(x):
+    """Round fp64 values to the nearest float8 e4m3 value (1 sign, 4 exponent bits with
+    bias 7, 3 mantissa bits; subnormals in steps of 2^-9; no infinities), ties to even,
+    for |x| <= 448.  Returned as fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -6.0)                        # below 2^-6 the spacing stays 2^-9
+    ulp = np.exp2(e - 3.0)
+    return np.sign(x) * np.round(a / ulp) * ulp    # np.round: halves to even
+
+
+def quantize_rows_fp8(w):
+    """[NVIDIA blog, Blackwell Ultra paragraph: low-precision tensor formats] per output
+    row n of an [out, in] matrix: a power-of-two scale s_n = 2^ceil(log2(max|w_n| / 448))
+    (1 for an all-zero row), so that w / s is exact and at most 448 in magnitude, and
+    codes q = e4m3(w / s).  Returns (q [out, in] as fp64 values, s [out])."""
+    w = np.asarray(w, dtype=np.float64)
+    amax = np.abs(w).max(axis=1)
+    s = np.where(amax > 0, np.exp2(np.ceil(np.log2(np.where(amax > 0, amax, 1.0) / E4M3_MAX))),
+                 1.0)
+    return round_e4m3(w / s[:, None]), s
+
+
+FP8_MATRICES = ("w_fuse", "w_q", "w_k", "w_v", "w_o", "w_gate", "w_up", "w_down", "lm_head")
+
+
+def fp8_weights(W):
+    """The drafter's weights as the FP8 weight-streaming path holds them: every
+    projection matrix (fusion, Q/K/V/O, gate/up/down, LM head) replaced by its
+    dequantized per-row FP8 form q * s; embedding and gains unchanged."""
+    out = dict(W)
+    for name, m in W.items():
+        if name.split(".")[-1] in FP8_MATRICES:
+            q, s = quantize_rows_fp8(m)
+            out[name] = q * s[:, None]
+    return out

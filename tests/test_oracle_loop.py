@@ -173,3 +173,67 @@ def test_target_forward_is_causal_and_drafter_matches_the_step_path():
     ids = np.array([toks[6], 0, 0, 0])
     ref = O.draft_step(taps6, 6, ids, Wd, cfg, False)
     np.testing.assert_array_equal(d, ref["draft"])
+
+
+# ------------------------------------------------------------ FP8 weight quantizer
+def _all_e4m3():
+    """Every finite e4m3 value, decoded from its bit fields (sign, exponent, mantissa)."""
+    vals = []
+    for code in range(256):
+        s, e, m = code >> 7, (code >> 3) & 15, code & 7
+        if e == 15 and m == 7:
+            continue                                # the NaN encoding
+        v = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+        vals.append((-v if s else v, code))
+    return vals
+
+
+def test_round_e4m3_is_the_nearest_code_ties_to_even():
+    vals = _all_e4m3()
+    grid = np.array(sorted({v for v, _ in vals}))
+    assert grid.max() == 448.0 and np.isclose(grid[grid > 0].min(), 2.0 ** -9)
+    rng = np.random.default_rng(11)
+    x = np.concatenate([rng.normal(0, 30, 3000), rng.normal(0, 0.01, 1000),
+                        rng.uniform(-448, 448, 1000)])
+    mids = (grid[1:] + grid[:-1]) / 2                 # exact ties
+    x = np.concatenate([x, mids])
+    q = O.round_e4m3(x)
+    for xi, qi in zip(x, q):
+        d = np.abs(grid - xi)
+        best = grid[d == d.min()]
+        if len(best) == 1:
+            assert qi == best[0], (xi, qi, best)
+        else:                                         # tie: the even code (mantissa lsb 0)
+            even = [v for v, c in vals if v in best and (c & 1) == 0]
+            assert qi == even[0], (xi, qi, best)
+
+
+def test_round_e4m3_matches_the_library_float8_conversion():
+    import torch
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8")
+    rng = np.random.default_rng(12)
+    x = np.concatenate([rng.normal(0, 20, 20000), rng.normal(0, 0.005, 5000)])
+    x = np.clip(x, -448, 448).astype(np.float32).astype(np.float64)
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.round_e4m3(x), ref)
+
+
+def test_row_quantization_scales_and_error_bound():
+    rng = np.random.default_rng(13)
+    w = rng.normal(0, 0.02, (64, 300))
+    w[3] = 0.0
+    w[5, 7] = 9.0                                     # an outlier row
+    q, s = O.quantize_rows_fp8(w)
+    assert s[3] == 1.0 and np.all(q[3] == 0)
+    assert np.all(np.log2(s) == np.round(np.log2(s)))            # powers of two
+    assert np.all(np.abs(q).max(axis=1) <= 448.0)
+    assert np.all(np.abs(w).max(axis=1)[s != 1.0] / s[s != 1.0] > 224.0)   # no wasted binade
+    # relative error of normal codes is at most half a mantissa step (2^-4)
+    deq = q * s[:, None]
+    big = np.abs(w / s[:, None]) >= 2.0 ** -6
+    assert np.all(np.abs(deq - w)[big] <= 2.0 ** -4 * np.abs(w)[big] + 1e-300)
+    W = {"l0.w_q": w, "l0.g_attn": np.ones(300), "embed": w}
+    F = O.fp8_weights(W)
+    np.testing.assert_array_equal(F["l0.w_q"], deq)
+    assert F["embed"] is W["embed"] and F["l0.g_attn"] is W["l0.g_attn"]
