@@ -41,6 +41,10 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip timing the other workloads after the headline one")
+    ap.add_argument("--no-next", action="store_true",
+                    help="skip the input-fusion variant and the speculative loop")
     ap.add_argument("--cpu-budget", type=float, default=120.0,
                     help="seconds of oracle time the reference arm may spend")
     return ap.parse_args()
@@ -102,9 +106,11 @@ class Clocks:
 
 
 # ------------------------------------------------------------------------ oracle
-def oracle_timing(w, budget, max_steps, warmup):
+def oracle_timing(w, budget, max_steps, warmup, one_thread=False):
     """Times the fp64 oracle step of sequence 0 on the host cores (context K/V of the
-    earlier positions prepared untimed).  Returns (seconds per oracle step, steps)."""
+    earlier positions prepared untimed).  Returns (seconds per oracle step, steps); with
+    one_thread the timed steps run with BLAS limited to one thread (None when no limit
+    could be applied)."""
     import numpy as np
     from oracle import run as orun
     from workload import inputs
@@ -118,6 +124,16 @@ def oracle_timing(w, budget, max_steps, warmup):
     u = inputs.uniforms(w)[0].numpy()
     for _ in range(min(warmup, 1)):
         orun.step_sequence(w, W, 0, (K, V), row, u)
+    if one_thread:
+        with blas_threads(1) as lim:
+            if not lim.ok:
+                return None, 0
+            return oracle_timing_loop(w, W, K, V, row, u, budget, max_steps)
+    return oracle_timing_loop(w, W, K, V, row, u, budget, max_steps)
+
+
+def oracle_timing_loop(w, W, K, V, row, u, budget, max_steps):
+    from oracle import run as orun
     times = []
     t_all = time.perf_counter()
     while len(times) < max(1, max_steps):
@@ -127,6 +143,55 @@ def oracle_timing(w, budget, max_steps, warmup):
         if time.perf_counter() - t_all > budget:
             break
     return sum(times) / len(times), len(times)
+
+
+class blas_threads:
+    """Limits the BLAS library numpy uses to n threads inside a with-block (through
+    threadpoolctl when it is installed, else the OpenBLAS thread-count call found among
+    the loaded libraries).  `ok` tells whether a limit could be applied."""
+
+    SYMS = ("openblas_set_num_threads", "scipy_openblas_set_num_threads64_",
+            "openblas_set_num_threads64_", "scipy_openblas_set_num_threads")
+    GET = ("openblas_get_num_threads", "scipy_openblas_get_num_threads64_",
+           "openblas_get_num_threads64_", "scipy_openblas_get_num_threads")
+
+    def __init__(self, n):
+        self.n, self.ok, self._undo = n, False, None
+
+    def __enter__(self):
+        try:
+            from threadpoolctl import threadpool_limits
+            self._undo = threadpool_limits(limits=self.n, user_api="blas")
+            self.ok = True
+            return self
+        except Exception:
+            pass
+        import ctypes
+        try:
+            libs = {ln.split()[-1] for ln in open("/proc/self/maps") if "blas" in ln.lower()}
+        except OSError:
+            libs = set()
+        for path in libs:
+            try:
+                lib = ctypes.CDLL(path)
+            except OSError:
+                continue
+            for s, g in zip(self.SYMS, self.GET):
+                if hasattr(lib, s) and hasattr(lib, g):
+                    prev = getattr(lib, g)()
+                    getattr(lib, s)(self.n)
+                    self._undo = lambda f=getattr(lib, s), p=prev: f(p)
+                    self.ok = True
+                    return self
+        return self
+
+    def __exit__(self, *exc):
+        if self._undo is None:
+            return
+        if callable(self._undo):
+            self._undo()
+        else:
+            self._undo.restore_original_limits()
 
 
 def cpu_threads():
@@ -162,6 +227,171 @@ def run_reference(args):
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------ per config
+def measure_config(w, steps, warmup, hbm, bf16_tf):
+    """One workload timed on its own: the step in a CUDA graph (K replays between CUDA
+    events), its step roofline, and each library call of an eager step timed between
+    events (no programmatic overlap between calls there, so they sum to more than the
+    graph step).  Returns a dict for the bench line's per_config object."""
+    import torch
+
+    from block_diffusion_drafter_concat_gb300.runner import (StepRunner, lm_head_bytes,
+                                                            step_bytes, step_flops)
+    r = StepRunner(w)
+    r.step()
+    torch.cuda.synchronize()
+    r.plant(r.draft.cpu())
+    r.capture()
+    for _ in range(max(3, warmup)):
+        r.replay()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(st)
+    for _ in range(steps):
+        r.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    calls = r.timed_calls(reps=3)
+    if r.drafter.device_error():
+        raise RuntimeError(f"device error on {w.name}")
+    sb, fl = step_bytes(w), step_flops(w)
+    t_roof = max(sb / (hbm * 1e9), fl / (bf16_tf * 1e12))
+    lm_us = calls["lm_head_argmax"]
+    lm_gbs = lm_head_bytes(w) / (lm_us * 1e-6) / 1e9
+    lm_tf = 2.0 * w.rows * w.vocab * w.d_model / (lm_us * 1e-6) / 1e12
+    lm_tensor = (2.0 * w.rows * w.vocab * w.d_model / lm_head_bytes(w)
+                 > bf16_tf * 1e12 / (hbm * 1e9))
+    out = {
+        "ms_per_step": ms, "steps_per_s": 1e3 / ms, "batch": w.batch,
+        "mean_emitted": float(r.n_emit.float().mean()),
+        "tokens_per_s": 1e3 / ms * w.batch * float(r.n_emit.float().mean()),
+        "step_roofline": {"bytes": sb, "flops": fl, "t_roof_us": t_roof * 1e6,
+                          "frac": t_roof / (ms / 1e3)},
+        "eager_call_us": calls,
+        "lm_head": ({"bound": "tensor", "achieved": lm_tf, "unit": "TFLOP/s",
+                     "frac": lm_tf / bf16_tf, "us_per_launch": lm_us} if lm_tensor else
+                    {"bound": "hbm", "achieved": lm_gbs, "unit": "GB/s", "frac": lm_gbs / hbm,
+                     "us_per_launch": lm_us}),
+        "launches_per_step": r.launches,
+        "steps": steps,
+    }
+    del r
+    torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------------------ NEXT rows
+def measure_input_fusion(w, steps, warmup, hbm, bf16_tf):
+    """The input-fusion variant of the headline workload: its graph step beside the KV
+    injection step, and the context prefill of sequence 0 both ways."""
+    import torch
+
+    from block_diffusion_drafter_concat_gb300.runner import StepRunner, step_bytes
+    from workload import inputs as winputs
+    r = StepRunner(w, variant="input")
+    r.step()
+    torch.cuda.synchronize()
+    r.plant(r.draft.cpu())
+    r.capture()
+    for _ in range(max(3, warmup)):
+        r.replay()
+    st = torch.cuda.current_stream()
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    torch.cuda.synchronize()
+    e[0].record(st)
+    for _ in range(steps):
+        r.replay()
+    e[1].record(st)
+    torch.cuda.synchronize()
+    ms = e[0].elapsed_time(e[1]) / steps
+    # prefill of sequence 0's context through the layer stack (chunks of S rows)
+    S = w.block_size
+    T = int(r.lens[0]) - S
+    x = torch.empty(w.rows, w.fuse_in, dtype=r.dt, device="cuda")
+    chunks = list(range(0, T, S))
+    xs = [winputs.ctx_hidden(w, 0, c0, c0 + S, "cuda") for c0 in chunks]
+    ctx = [torch.tensor([c0] * w.batch, dtype=torch.int32, device="cuda") for c0 in chunks]
+    torch.cuda.synchronize()
+    e[2].record(st)
+    for xc, cc in zip(xs, ctx):
+        x[:S].copy_(xc)
+        r.drafter.inject_inputs(x, cc, r.page_table, r.cache, r.ws)
+    e[3].record(st)
+    torch.cuda.synchronize()
+    pf_us = e[2].elapsed_time(e[3]) * 1e3
+    if r.drafter.device_error():
+        raise RuntimeError("device error in the input-fusion variant")
+    out = {"ms_per_step": ms, "steps_per_s": 1e3 / ms,
+           "step_hbm_gbs": step_bytes(w) / (ms / 1e3) / 1e9,
+           "prefill": {"rows": T, "us": pf_us, "chunks": len(chunks),
+                       "note": "context of sequence 0 through the layer stack, causal "
+                               "chunks of S rows (input fusion), timed with the copies "
+                               "of the chunk inputs"},
+           "note": "fused features as the drafter's input: the S new context rows run "
+                   "through every layer (causal) instead of being injected as K/V"}
+    del r
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_spec_loop(sw, steps, warmup):
+    """The greedy speculative loop with a random causal target: prefill (untimed), a
+    few eager steps, then one step captured in a CUDA graph and replayed; tokens/s from
+    the tokens the timed steps emitted (planted agreement, see the workload)."""
+    import torch
+
+    from block_diffusion_drafter_concat_gb300.spec import SpecRunner
+    steps = max(1, min(steps, sw.steps - warmup - 1))
+    r = SpecRunner(sw)
+    r.prefill()
+    for _ in range(warmup):
+        r.step()
+    torch.cuda.synchronize()
+    n0 = int(r.n_generated.sum())
+    r.capture()
+    st = torch.cuda.current_stream()
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    torch.cuda.synchronize()
+    e[0].record(st)
+    for _ in range(steps):
+        r.replay()
+    e[1].record(st)
+    torch.cuda.synchronize()
+    ms = e[0].elapsed_time(e[1]) / steps
+    emitted = int(r.n_generated.sum()) - n0
+    if r.drafter.device_error() or r.target.device_error():
+        raise RuntimeError("device error in the speculative loop")
+    # one target pass over a block alone (what one greedy token costs without drafting
+    # at batch 1, where the pass streams the target's weights whatever its row count)
+    w = sw.drafter
+    ids = torch.zeros(w.batch, w.block_size, dtype=torch.int32, device="cuda")
+    ctx = r.ctx_lens.clone()
+    for _ in range(2):
+        r.target.target_forward(ids, ctx, r.table, r.tcache, r.tws)
+    torch.cuda.synchronize()
+    e[2].record(st)
+    for _ in range(5):
+        r.target.target_forward(ids, ctx, r.table, r.tcache, r.tws)
+    e[3].record(st)
+    torch.cuda.synchronize()
+    t_pass = e[2].elapsed_time(e[3]) / 5
+    tok_s = emitted / (ms * steps / 1e3)
+    out = {"workload": sw.name, "target_layers": sw.target_layers,
+           "tap_layers": list(sw.tap_layers), "batch": w.batch, "prompt": sw.prompt_len,
+           "steps": steps, "ms_per_step": ms, "tokens_per_s": tok_s,
+           "mean_emitted": emitted / (steps * w.batch), "plant_p": sw.plant_p,
+           "launches_per_step": r.launches,
+           "target_pass_ms": t_pass,
+           "tokens_per_s_one_target_pass_per_token": w.batch * 1e3 / t_pass,
+           "note": "draft -> target pass -> verify -> commit -> inject in one CUDA graph per "
+                   "step; random weights, so acceptance comes from planted agreement"}
+    del r
+    torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------------------ ours
@@ -363,6 +593,22 @@ def run_ours(args):
         "launches_per_step": r.launches,
         "clocks": clocks,
     }
+    if not args.no_per_config:
+        from workload.configs import ALL
+        per = {w.name: {"headline": True, "ms_per_step": ms,
+                        "step_roofline": {"frac": t_roof / (ms / 1e3)}}}
+        for wo in ALL:
+            if wo.name == w.name:
+                continue
+            per[wo.name] = measure_config(replicas.shard(wo, rank), min(args.steps, 30),
+                                          args.warmup, hbm, bf16_tf)
+        line["per_config"] = per
+    if not args.no_next and w.name == DEFAULT_CONFIG:
+        from workload.configs import SPEC_QWEN3_8B
+        line["input_fusion"] = measure_input_fusion(replicas.shard(w, rank), min(args.steps, 50),
+                                                    args.warmup, hbm, bf16_tf)
+        line["input_fusion"]["kv_injection_ms_per_step"] = ms
+        line["spec_loop"] = measure_spec_loop(SPEC_QWEN3_8B, args.steps, 3)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tc, n = oracle_timing(w, 30.0, 3, 1)
         line["cpu_baseline"] = {
@@ -370,6 +616,15 @@ def run_ours(args):
             "kind": "oracle",
             "sample": f"{n} fp64 oracle step(s) of sequence 0 of {w.batch}, context K/V "
                       "prepared untimed; scaled to whole steps"}
+        # the same oracle with BLAS on one thread, on the tiny and the headline workload
+        one = {}
+        for wo in (BY_NAME["tiny-f32"], w):
+            t1, n1 = oracle_timing(wo, 30.0, 3 if wo.name == "tiny-f32" else 1, 1,
+                                   one_thread=True)
+            one[wo.name] = (None if t1 is None else
+                            {"value": 1.0 / (t1 * wo.batch), "unit": "steps/s", "cores": 1,
+                             "sample": f"{n1} oracle step(s) of sequence 0"})
+        line["cpu_baseline"]["one_thread"] = one
     if rank == 0:
         print(json.dumps(line), flush=True)
     if rep.distributed:

@@ -22,8 +22,11 @@ DEV_ERRORS = {0: "ok", 1: "index out of range", 2: "position out of range", 3: "
 
 API = ["dflash_create", "dflash_destroy", "dflash_workspace_size", "dflash_workspace_init",
        "dflash_fuse_features", "dflash_inject_kv", "dflash_draft_block",
+       "dflash_inject_inputs", "dflash_target_forward", "dflash_spec_workspace_size",
+       "dflash_spec_workspace_init", "dflash_spec_step",
        "dflash_lm_head_argmax", "dflash_verify_greedy", "dflash_verify_sample",
-       "dflash_verify_greedy_static",
+       "dflash_verify_greedy_static", "dflash_test_force_timeout", "dflash_fp8_packed_bytes",
+       "dflash_pack_fp8",
        "dflash_get_device_error", "dflash_last_error", "dflash_last_launch_count"]
 
 
@@ -37,7 +40,8 @@ class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "d_model", "n_layers", "n_q_heads", "n_kv_heads", "head_dim", "ffn_dim", "vocab",
         "block_size", "n_target_layers", "target_width", "page_size", "max_position")] + [
-        ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float), ("dtype", ctypes.c_int32)]
+        ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float), ("dtype", ctypes.c_int32),
+        ("weight_format", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -48,6 +52,16 @@ class Weights(ctypes.Structure):
     _fields_ = [("w_fuse", _P), ("g_fuse", _P)] + [(n, _PP) for n in (
         "g_attn", "w_q", "w_k", "w_v", "w_o", "g_mlp", "w_gate", "w_up", "w_down")] + [
         ("g_final", _P), ("embed", _P), ("lm_head", _P)]
+
+
+class SpecState(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("block_ids", _P), ("ctx_lens", _P),
+                ("page_table", _P), ("max_pages", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("d_k_pool", _PP), ("d_v_pool", _PP), ("t_k_pool", _PP), ("t_v_pool", _PP),
+                ("tap_layers", _P), ("mask_id", ctypes.c_int32), ("generated", _P),
+                ("max_new", ctypes.c_int32), ("n_generated", _P), ("n_emitted", _P), ("drafts", _P),
+                ("step", _P), ("plant_u", _P), ("plant_steps", ctypes.c_int32),
+                ("plant_p", ctypes.c_float)]
 
 
 _lib = None
@@ -72,10 +86,18 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "dflash_fuse_features": [P, P, i32, P, P, sz, P],
         "dflash_inject_kv": [P, P, P, i32, P, P, i32, PP, PP, P, P, sz, P],
         "dflash_draft_block": [P, P, P, P, i32, i32, i32, PP, PP, P, P, sz, P],
+        "dflash_inject_inputs": [P, P, P, P, i32, i32, i32, PP, PP, P, P, sz, P],
+        "dflash_spec_workspace_size": [P, P, i32, i32, ctypes.POINTER(sz)],
+        "dflash_spec_workspace_init": [P, P, i32, i32, P, sz, P],
+        "dflash_spec_step": [P, P, ctypes.POINTER(SpecState), P, sz, P],
+        "dflash_target_forward": [P, P, P, P, i32, i32, i32, PP, PP, P, i32, P, P, P, sz, P],
         "dflash_lm_head_argmax": [P, P, i32, ctypes.c_float, P, P, P, P, sz, P],
         "dflash_verify_greedy": [P, P, P, i32, P, P, P, P, sz, P],
         "dflash_verify_sample": [P, P, P, P, P, P, P, ctypes.c_float, i32, P, P, P, P, sz, P],
         "dflash_verify_greedy_static": [P, P, P, i32, P, P, P, P],
+        "dflash_test_force_timeout": [P, i32],
+        "dflash_fp8_packed_bytes": [i32, i32, ctypes.POINTER(sz)],
+        "dflash_pack_fp8": [P, i32, i32, P, P],
         "dflash_get_device_error": [P, ctypes.POINTER(i32), i32],
         "dflash_last_error": [],
         "dflash_last_launch_count": [],
@@ -107,6 +129,27 @@ def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
+def pack_fp8(w: torch.Tensor) -> torch.Tensor:
+    """The packed FP8 form of a bf16 [rows, cols] CUDA matrix (dflash_pack_fp8), as a
+    uint8 CUDA tensor."""
+    lib = load()
+    rows, cols = w.shape
+    n = ctypes.c_size_t()
+    _check(lib.dflash_fp8_packed_bytes(rows, cols, ctypes.byref(n)))
+    out = torch.empty(n.value, dtype=torch.uint8, device=w.device)
+    _check(lib.dflash_pack_fp8(_ptr(w.contiguous()), rows, cols, _ptr(out), _stream()))
+    return out
+
+
+def unpack_fp8(packed: torch.Tensor, rows: int, cols: int):
+    """(codes [rows, cols] uint8, scales [rows] fp32) views of a packed FP8 matrix."""
+    ld = (cols + 15) // 16 * 16
+    off = (rows * ld + 255) // 256 * 256
+    codes = packed[:rows * ld].view(rows, ld)[:, :cols]
+    scales = packed[off:off + 4 * rows].view(torch.float32)
+    return codes, scales
+
+
 def last_launch_count() -> int:
     return int(load().dflash_last_launch_count())
 
@@ -128,7 +171,8 @@ class Drafter:
 
     ``weights`` maps the names w_fuse, g_fuse, l{l}.g_attn, l{l}.w_q, l{l}.w_k,
     l{l}.w_v, l{l}.w_o, l{l}.g_mlp, l{l}.w_gate, l{l}.w_up, l{l}.w_down, g_final, embed,
-    lm_head to contiguous CUDA tensors of the config dtype."""
+    lm_head to contiguous CUDA tensors of the config dtype (without w_fuse and g_fuse:
+    a plain transformer, e.g. the target of the speculative loop)."""
 
     LAYER = ("g_attn", "w_q", "w_k", "w_v", "w_o", "g_mlp", "w_gate", "w_up", "w_down")
 
@@ -136,7 +180,7 @@ class Drafter:
         lib = load()
         self.cfg = dict(cfg)
         self.dtype = torch.bfloat16 if cfg["dtype"] == BF16 else torch.float32
-        self.c = Config(**{k: cfg[k] for k, _ in Config._fields_})
+        self.c = Config(**{k: cfg.get(k, 0) for k, _ in Config._fields_})
         self._w = weights
         self._arrays = {}
         fields = {}
@@ -144,7 +188,7 @@ class Drafter:
             ts = [weights[f"l{l}.{name}"] for l in range(cfg["n_layers"])]
             fields[name], self._arrays[name] = _ptr_array(ts)
         for name in ("w_fuse", "g_fuse", "g_final", "embed", "lm_head"):
-            fields[name] = _ptr(weights[name])
+            fields[name] = _ptr(weights.get(name))
         self.w = Weights(**fields)
         h = ctypes.c_void_p()
         _check(lib.dflash_create(ctypes.byref(self.c), ctypes.byref(self.w), ctypes.byref(h)))
@@ -198,6 +242,22 @@ class Drafter:
             _ptr(ws), ws.numel(), _stream()))
         return final_hidden
 
+    def inject_inputs(self, x_cat, ctx_lens, page_table, cache: KVCache, ws, fused_out=None):
+        _check(self.lib.dflash_inject_inputs(
+            self.h, _ptr(x_cat), _ptr(ctx_lens), _ptr(page_table), page_table.shape[1],
+            ctx_lens.shape[0], cache.num_pages, cache._kp, cache._vp, _ptr(fused_out), _ptr(ws),
+            ws.numel(), _stream()))
+
+    def target_forward(self, ids, ctx_lens, page_table, cache: KVCache, ws, tap_layers=(),
+                       taps=None, logits=None):
+        n = len(tap_layers)
+        arr = (ctypes.c_int32 * max(1, n))(*tap_layers)
+        _check(self.lib.dflash_target_forward(
+            self.h, _ptr(ids), _ptr(ctx_lens), _ptr(page_table), page_table.shape[1],
+            ids.shape[0], cache.num_pages, cache._kp, cache._vp,
+            ctypes.cast(arr, ctypes.c_void_p) if n else None, n, _ptr(taps), _ptr(logits),
+            _ptr(ws), ws.numel(), _stream()))
+
     def lm_head_argmax(self, hidden, tokens, ws, max_logit=None, lse=None, temperature=1.0):
         _check(self.lib.dflash_lm_head_argmax(self.h, _ptr(hidden), hidden.shape[0],
                                               float(temperature), _ptr(tokens), _ptr(max_logit),
@@ -216,6 +276,9 @@ class Drafter:
             _ptr(target_logits), _ptr(uniforms), float(temperature), draft.shape[0],
             _ptr(out_tokens), _ptr(n_accepted), _ptr(n_emitted), _ptr(ws), ws.numel(),
             _stream()))
+
+    def test_force_timeout(self, enable: bool):
+        _check(self.lib.dflash_test_force_timeout(self.h, int(bool(enable))))
 
     def device_error(self, clear=True) -> int:
         code = ctypes.c_int32()

@@ -50,6 +50,9 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// wait limit of the split-tile finishers under the forced-timeout test hook
+constexpr unsigned long long kForcedWaitNs = 10000000ull;  // 10 ms
+
 // ------------------------------------------------------------------ TMA descriptors
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -85,6 +88,36 @@ dflash_status encode_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64
   return DFLASH_OK;
 }
 
+// Packed FP8 matrix [rows, cols]: e4m3 codes with row stride round_up(cols, 16) bytes,
+// then rows fp32 scales at a 256-byte aligned offset.
+size_t fp8_ld(long long cols) { return (size_t)((cols + 15) / 16 * 16); }
+size_t fp8_scale_offset(long long rows, long long cols) {
+  return ((size_t)rows * fp8_ld(cols) + 255) & ~size_t(255);
+}
+size_t fp8_packed_bytes(long long rows, long long cols) {
+  return fp8_scale_offset(rows, cols) + (size_t)rows * sizeof(float);
+}
+
+// Codes of a packed FP8 matrix as a byte tensor, read in boxes of box_rows x 128 bytes
+// (128 values of k) with 128-byte swizzle; out-of-range reads give 0.
+dflash_status encode_fp8(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                         uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(DFLASH_ECUDA, "cuTensorMapEncodeTiled unavailable");
+  if (!aligned16(ptr) || rows == 0 || cols == 0)
+    return fail(DFLASH_EINVAL, "packed FP8 matrix %p (%llu x %llu) not TMA-compatible", ptr,
+                (unsigned long long)rows, (unsigned long long)cols);
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {fp8_ld(cols)};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DFLASH_ECUDA, "cuTensorMapEncodeTiled (fp8) failed (%d)", (int)r);
+  return DFLASH_OK;
+}
+
 // ------------------------------------------------------------------ workspace carving
 struct Carve {
   char* base;
@@ -113,6 +146,8 @@ struct dflash_handle_s {
   std::vector<CUtensorMap> m_q, m_k, m_v, m_o, m_gate, m_up, m_down;
   int* d_err = nullptr;
   float2* d_rope = nullptr;
+  bool force_timeout = false;  // test hook: split-tile finishers wait for too much
+  bool fp8 = false;            // projection weights are packed FP8 (per-row scales)
 };
 
 namespace {
@@ -143,6 +178,8 @@ GemmShape plan_shape(const H* h, const WSet& w, int M, int K, bool tc, int* grid
   GemmShape g = {};
   g.M = M;
   g.K = K;
+  g.wait_extra = h->force_timeout ? 1 : 0;
+  g.wait_ns = h->force_timeout ? kForcedWaitNs : kWaitNs;
   g.paired = w.paired;
   g.nseg = w.nseg;
   int t = 0;
@@ -154,7 +191,7 @@ GemmShape plan_shape(const H* h, const WSet& w, int M, int K, bool tc, int* grid
   g.seg_tile0[w.nseg] = t;
   if (w.paired) g.seg_tile0[1] = t;  // both halves of every tile come from segment 0's range
   g.n_tiles = t;
-  g.ks = ceil_div(K, kBK);
+  g.ks = ceil_div(K, h->fp8 ? 2 * kBK : kBK);   // an FP8 stage covers 128 k
   // stream-K: at least 4 units per CTA, and few enough CTAs per tile for the table of
   // the tile's finisher
   const long long per = std::max<long long>(4, (g.ks + 509) / 510);
@@ -162,6 +199,7 @@ GemmShape plan_shape(const H* h, const WSet& w, int M, int K, bool tc, int* grid
     return static_cast<int>(std::min<long long>(h->sms, (units + per - 1) / per));
   };
   int bn = tc ? pick_bn(M) : kF32BN;
+  if (h->fp8) bn = std::min(bn, 32);   // FP8 weights: the weight-streaming kernel only
   int grid = 0;
   if (tc && umma_bn(bn)) {
     // tcgen05 tiles of 128 or 256 rows, as whole tiles per CTA (waves of tiles) or as
@@ -234,6 +272,12 @@ dflash_status gemm(const H* h, const void* A, int M, int K, const WSet& w, EpiAr
     TRY(encode_bf16(&tmA, A, M, K, K, bn));
     WMaps wm;
     for (int s = 0; s < w.nseg; ++s) wm.m[s] = *w.maps[s];
+    if (h->fp8) {
+      for (int s = 0; s < w.nseg; ++s)
+        g.wscale[s] = reinterpret_cast<const float*>(static_cast<const char*>(w.ptrs[s]) +
+                                                     fp8_scale_offset(w.rows[s], K));
+      return launch_gemm_tc_f8(bn, EPI, tmA, wm, g, grid, e, st);
+    }
     if (umma_bn(bn)) return launch_gemm_umma(bn, EPI, tmA, wm, g, grid, e, st);
     if (bn <= 32) return launch_gemm_tc_lo(bn, EPI, tmA, wm, g, grid, e, st);
     return launch_gemm_tc_hi(bn, EPI, tmA, wm, g, grid, e, st);
@@ -253,7 +297,8 @@ dflash_status rmsnorm(const H* h, const Tin* x, const void* gain, T* y, int rows
   return launch(k_rmsnorm<T, Tin>, dim3(rows), dim3(kRowThreads), 0, st, x,
                 static_cast<float*>(nullptr), static_cast<const T*>(gain), y, h->c.d_model,
                 h->c.rms_eps, static_cast<const int*>(nullptr), static_cast<const T*>(nullptr), 0,
-                static_cast<const int*>(nullptr), 1, 0, static_cast<int*>(nullptr), h->d_err);
+                static_cast<const int*>(nullptr), 1, 0, static_cast<int*>(nullptr), h->d_err,
+                static_cast<const T*>(nullptr));
 }
 
 // ------------------------------------------------------------------ attention plan
@@ -274,10 +319,10 @@ struct AttnPlan {
   int pps, nsplit;
 };
 
-AttnPlan plan_attn(const H* h, int B, int max_pages) {
+AttnPlan plan_attn(const H* h, int B, int max_pages, bool causal = false) {
   const int kp = max_pages + 1;
   const long long groups = (long long)B * h->c.n_kv_heads;
-  if (use_attn_umma(h->c, B * h->c.block_size)) {
+  if (use_attn_umma(h->c, B * h->c.block_size) && !causal) {
     // tcgen05 kernel (two CTAs per SM at head_dim 64, one at 128), four pages per step:
     // whole steps per split and the fewest waves of CTAs times steps per CTA (plus about
     // three steps of per-CTA prologue and epilogue); among plans within 2 % of the best,
@@ -331,7 +376,9 @@ size_t elt(const H* h) { return h->bf16 ? 2 : 4; }
 DraftWs carve_draft(const H* h, Carve& cv, int B, int max_pages) {
   const auto& c = h->c;
   const size_t M = (size_t)B * c.block_size;
-  const AttnPlan ap = plan_attn(h, B, max_pages);
+  // split partials for the larger of the block's plan and a causal chunk's plan
+  const AttnPlan pb = plan_attn(h, B, max_pages), pc = plan_attn(h, B, max_pages, true);
+  const AttnPlan ap = pb.nsplit >= pc.nsplit ? pb : pc;
   const int QR = c.block_size * (c.n_q_heads / c.n_kv_heads);
   DraftWs w;
   w.ctl = cv.take<int>(kCtlWords);
@@ -346,6 +393,36 @@ DraftWs carve_draft(const H* h, Carve& cv, int B, int max_pages) {
   w.part_o = cv.take<float>((size_t)B * c.n_kv_heads * ap.nsplit * QR * c.head_dim);
   w.part_ml = cv.take<float>((size_t)B * c.n_kv_heads * ap.nsplit * QR * 2);
   w.gpart = cv.take<float>(gemm_part_floats(h, static_cast<int>(M)));
+  return w;
+}
+
+// a causal chunk of context rows for the input-fusion drafter: the block's buffers plus
+// the fusion's fp32 projection and its normed rows
+struct InputsWs {
+  DraftWs d;
+  float* u;
+  void* fused;
+};
+
+InputsWs carve_inputs(const H* h, Carve& cv, int B, int max_pages) {
+  InputsWs w;
+  w.d = carve_draft(h, cv, B, max_pages);
+  const size_t M = (size_t)B * h->c.block_size;
+  w.u = cv.take<float>(M * h->c.d_model);
+  w.fused = cv.take<char>(M * h->c.d_model * elt(h));
+  return w;
+}
+
+// a target chunk: the block's buffers plus the final hidden rows of the LM head
+struct TargetWs {
+  DraftWs d;
+  void* hfin;
+};
+
+TargetWs carve_target(const H* h, Carve& cv, int B, int max_pages) {
+  TargetWs w;
+  w.d = carve_draft(h, cv, B, max_pages);
+  w.hfin = cv.take<char>((size_t)B * h->c.block_size * h->c.d_model * elt(h));
   return w;
 }
 
@@ -429,6 +506,23 @@ dflash_status check_ws(const void* ws, size_t have, size_t need) {
   return DFLASH_OK;
 }
 
+// Every call on a handle enqueues work for the handle's device: that device must be the
+// current one (kernels, workspace and the device scratch array all live there).
+dflash_status check_device(const dflash_handle_s* h) {
+  int dev = -1;
+  CUDA_TRY(cudaGetDevice(&dev));
+  if (dev != h->dev)
+    return fail(DFLASH_EINVAL, "the handle belongs to device %d but device %d is current",
+                h->dev, dev);
+  return DFLASH_OK;
+}
+
+#define CHECK_HANDLE(h)                                                                  \
+  do {                                                                                   \
+    if (!(h)) return fail(DFLASH_EINVAL, "null handle");                                 \
+    TRY(check_device(h));                                                                \
+  } while (0)
+
 #define NEED(p, what)                                                                    \
   do {                                                                                   \
     if (!(p)) return fail(DFLASH_EINVAL, "%s is NULL", what);                            \
@@ -458,22 +552,82 @@ static dflash_status fuse_impl(H* h, const void* x_cat, int n, void* fused, floa
   return rmsnorm<float, float>(h, u, h->g_fuse, static_cast<float*>(fused), n, st);
 }
 
+static dflash_status inject_impl(H* h, const void* f, int n, const int32_t* positions,
+                                 const int32_t* slots, int32_t num_pages, void* const* k_pool,
+                                 void* const* v_pool, const InjectWs& w, cudaStream_t st) {
+  const auto& c = h->c;
+  // one GEMM per group of up to 8 layers: segments k_l | v_l
+  for (int l0 = 0; l0 < c.n_layers; l0 += kMaxSeg / 2) {
+    const int nl = std::min(kMaxSeg / 2, c.n_layers - l0);
+    WSet ws_;
+    for (int l = l0; l < l0 + nl; ++l) {
+      ws_.add(h->bf16 ? &h->m_k[l] : nullptr, h->w_k[l], c.n_kv_heads * c.head_dim);
+      ws_.add(h->bf16 ? &h->m_v[l] : nullptr, h->w_v[l], c.n_kv_heads * c.head_dim);
+    }
+    auto fill = [&](auto& e, auto* tag) {
+      using T = std::remove_pointer_t<decltype(tag)>;
+      e.pos = positions;
+      e.rope = h->d_rope;
+      e.max_pos = c.max_position;
+      e.S = c.block_size;
+      e.hq = c.n_q_heads;
+      e.hkv = c.n_kv_heads;
+      e.hd = c.head_dim;
+      for (int l = 0; l < nl; ++l) {
+        e.kpool[l] = static_cast<T*>(k_pool[l0 + l]);
+        e.vpool[l] = static_cast<T*>(v_pool[l0 + l]);
+      }
+      e.slots = slots;
+      e.num_slots = (long long)num_pages * kPage;
+      e.err = h->d_err;
+    };
+    if (h->bf16) {
+      EpiArgs<bf16> e = {};
+      fill(e, static_cast<bf16*>(nullptr));
+      TRY((gemm<EPI_KV, bf16>(h, f, n, c.d_model, ws_, e, w.gpart, w.ctl, st)));
+    } else {
+      EpiArgs<float> e = {};
+      fill(e, static_cast<float*>(nullptr));
+      TRY((gemm<EPI_KV, float>(h, f, n, c.d_model, ws_, e, w.gpart, w.ctl, st)));
+    }
+  }
+  return DFLASH_OK;
+}
+
+// One pass of the layer stack over S rows per sequence at positions ctx_lens[b] + i.
+// The drafter's block: token ids in, every row sees all S block keys, final norm out.
+// A causal chunk (context rows of the input-fusion drafter, target tokens): input rows
+// or ids, row i sees block keys 0..i, each layer's K/V of the rows go into the cache,
+// optional taps of the residual stream after given layers.
+struct StackOpts {
+  const int32_t* ids = nullptr;   // [B, S] token ids (embedding input), or
+  const void* rows = nullptr;     // [B*S, d] input rows
+  bool causal = false;
+  bool write_cache = false;
+  const int32_t* tap_layers = nullptr;  // host array, 1-based layer indices
+  int n_taps = 0;
+  void* taps = nullptr;           // [B*S, n_taps*d]
+  void* final_hidden = nullptr;   // [B*S, d] final RMSNorm output, or nullptr
+};
+
 template <typename T>
-static dflash_status draft_impl(H* h, const int32_t* block_ids, const int32_t* ctx_lens,
+static dflash_status draft_impl(H* h, const StackOpts& o, const int32_t* ctx_lens,
                                 const int32_t* page_table, int32_t max_pages, int32_t B,
                                 int32_t num_pages, void* const* k_pool, void* const* v_pool,
-                                void* final_hidden, const DraftWs& w, cudaStream_t st) {
+                                const DraftWs& w, cudaStream_t st) {
   const auto& c = h->c;
   const int S = c.block_size, M = B * S, d = c.d_model;
   const int qw = c.n_q_heads * c.head_dim, kvw = c.n_kv_heads * c.head_dim;
   const int G = c.n_q_heads / c.n_kv_heads, QR = S * G;
   T* n = static_cast<T*>(w.n);
-  // block embedding + first pre-attention norm + positions
+  // embedding (or input rows) + first pre-attention norm + positions
   TRY(launch(k_rmsnorm<T, float>, dim3(M), dim3(kRowThreads), 0, st,
              static_cast<const float*>(nullptr), w.x, static_cast<const T*>(h->g_attn[0]), n, d,
-             c.rms_eps, block_ids, static_cast<const T*>(h->embed), c.vocab, ctx_lens, S,
-             c.max_position, w.pos, h->d_err));
-  const AttnPlan ap = plan_attn(h, B, max_pages);
+             c.rms_eps, o.ids, static_cast<const T*>(h->embed), c.vocab, ctx_lens, S,
+             c.max_position, w.pos, h->d_err, static_cast<const T*>(o.rows)));
+  const AttnPlan ap = plan_attn(h, B, max_pages, o.causal);
+  // a chunk whose only output is the cache needs no attention or MLP in its last layer
+  const bool kv_only_last = o.write_cache && !o.final_hidden && o.n_taps == 0;
   for (int l = 0; l < c.n_layers; ++l) {
     {  // Q, K, V with RoPE
       WSet ws_;
@@ -494,6 +648,12 @@ static dflash_status draft_impl(H* h, const int32_t* block_ids, const int32_t* c
       e.err = h->d_err;
       TRY((gemm<EPI_QKV, T>(h, n, M, d, ws_, e, w.gpart, w.ctl, st)));
     }
+    if (o.write_cache)
+      TRY(launch(k_chunk_kv_to_cache<T>, dim3(M), dim3(kRowThreads), 0, st,
+                 static_cast<const T*>(w.kb), static_cast<const T*>(w.vb), ctx_lens, page_table,
+                 max_pages, num_pages, static_cast<T*>(k_pool[l]), static_cast<T*>(v_pool[l]), S,
+                 c.n_kv_heads, c.head_dim, h->d_err));
+    if (kv_only_last && l + 1 == c.n_layers) break;
     {  // attention over [context pages ; block]
       AttnArgs<T> a = {};
       a.q = static_cast<const T*>(w.q);
@@ -516,6 +676,7 @@ static dflash_status draft_impl(H* h, const int32_t* block_ids, const int32_t* c
       a.part_ml = w.part_ml;
       a.out = static_cast<T*>(w.o);
       a.err = h->d_err;
+      a.causal = o.causal ? 1 : 0;
       dim3 grid(ap.nsplit, c.n_kv_heads, B);
       if constexpr (std::is_same<T, bf16>::value) {
         AttnMaps mp;
@@ -525,7 +686,7 @@ static dflash_status draft_impl(H* h, const int32_t* block_ids, const int32_t* c
         const uint64_t blk_rows = (uint64_t)B * c.n_kv_heads * S;
         TRY(encode_bf16(&mp.kb, w.kb, blk_rows, c.head_dim, c.head_dim, kPage));
         TRY(encode_bf16(&mp.vb, w.vb, blk_rows, c.head_dim, c.head_dim, kPage));
-        if (use_attn_umma(c, M)) {
+        if (use_attn_umma(c, M) && !o.causal) {
           AuMaps am;
           am.k = mp.k;
           am.v = mp.v;
@@ -575,10 +736,14 @@ static dflash_status draft_impl(H* h, const int32_t* block_ids, const int32_t* c
       e.err = h->d_err;
       TRY((gemm<EPI_RESID, T>(h, w.act, M, c.ffn_dim, ws_, e, w.gpart, w.ctl, st)));
     }
+    for (int t = 0; t < o.n_taps; ++t)
+      if (o.tap_layers[t] == l + 1)
+        TRY(launch(k_tap<T>, dim3(M), dim3(kRowThreads), 0, st, static_cast<const float*>(w.x),
+                   d, static_cast<T*>(o.taps), o.n_taps * d, t * d));
     if (l + 1 < c.n_layers)
       TRY((rmsnorm<T, float>(h, w.x, h->g_attn[l + 1], n, M, st)));
-    else
-      TRY((rmsnorm<T, float>(h, w.x, h->g_final, static_cast<T*>(final_hidden), M, st)));
+    else if (o.final_hidden)
+      TRY((rmsnorm<T, float>(h, w.x, h->g_final, static_cast<T*>(o.final_hidden), M, st)));
   }
   return DFLASH_OK;
 }
@@ -666,6 +831,10 @@ dflash_status dflash_create(const dflash_config* cfg, const dflash_weights* w,
   if (kBM % c.head_dim) return fail(DFLASH_EUNSUPPORTED, "head_dim must divide 128");
   if (!(c.rope_theta > 0.f) || !(c.rms_eps >= 0.f)) return fail(DFLASH_EINVAL, "bad theta/eps");
   if (c.dtype != DFLASH_BF16 && c.dtype != DFLASH_F32) return fail(DFLASH_EINVAL, "bad dtype");
+  if (c.weight_format != DFLASH_WEIGHTS_NATIVE && c.weight_format != DFLASH_WEIGHTS_FP8)
+    return fail(DFLASH_EINVAL, "bad weight_format %d", c.weight_format);
+  if (c.weight_format == DFLASH_WEIGHTS_FP8 && c.dtype != DFLASH_BF16)
+    return fail(DFLASH_EUNSUPPORTED, "FP8 weights need the bf16 dtype");
   const int QR = c.block_size * (c.n_q_heads / c.n_kv_heads);
   const int kin = c.n_target_layers * c.target_width;
   if (c.dtype == DFLASH_BF16) {
@@ -685,14 +854,22 @@ dflash_status dflash_create(const dflash_config* cfg, const dflash_weights* w,
                                w->g_mlp, w->w_gate, w->w_up, w->w_down};
   for (auto a : arrs)
     if (!a) return fail(DFLASH_EINVAL, "per-layer weight array is NULL");
-  const void* singles[] = {w->w_fuse, w->g_fuse, w->g_final, w->embed, w->lm_head};
+  const void* singles[] = {w->g_final, w->embed, w->lm_head};
   for (auto p : singles) NEED(p, "weight");
+  // a handle without fusion weights is a plain transformer (e.g. a target model)
+  if ((w->w_fuse == nullptr) != (w->g_fuse == nullptr))
+    return fail(DFLASH_EINVAL, "w_fuse and g_fuse must both be given or both be NULL");
+  if (w->w_fuse) {
+    NEED(w->w_fuse, "w_fuse");
+    NEED(w->g_fuse, "g_fuse");
+  }
   for (auto a : arrs)
     for (int l = 0; l < c.n_layers; ++l) NEED(a[l], "layer weight");
 
   H* h = new H();
   h->c = c;
   h->bf16 = c.dtype == DFLASH_BF16;
+  h->fp8 = c.weight_format == DFLASH_WEIGHTS_FP8;
   cudaGetDevice(&h->dev);
   cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->dev);
   h->w_fuse = w->w_fuse; h->g_fuse = w->g_fuse; h->g_final = w->g_final;
@@ -710,19 +887,24 @@ dflash_status dflash_create(const dflash_config* cfg, const dflash_weights* w,
   };
   if (h->bf16) {
     const int d = c.d_model, qw = c.n_q_heads * c.head_dim, kvw = c.n_kv_heads * c.head_dim;
-    dflash_status s = encode_bf16(&h->m_fuse, h->w_fuse, d, kin, kin, kBM);
-    if (s == DFLASH_OK) s = encode_bf16(&h->m_lm, h->lm_head, c.vocab, d, d, kBM);
+    // a weight matrix [rows, cols] as TMA boxes of box_rows rows: bf16, or packed FP8
+    auto enc = [&](CUtensorMap* m, const void* p, int rows, int cols, int box_rows) {
+      return h->fp8 ? encode_fp8(m, p, rows, cols, box_rows)
+                    : encode_bf16(m, p, rows, cols, cols, box_rows);
+    };
+    dflash_status s = h->w_fuse ? enc(&h->m_fuse, h->w_fuse, d, kin, kBM) : DFLASH_OK;
+    if (s == DFLASH_OK) s = enc(&h->m_lm, h->lm_head, c.vocab, d, kBM);
     h->m_q.resize(c.n_layers); h->m_k.resize(c.n_layers); h->m_v.resize(c.n_layers);
     h->m_o.resize(c.n_layers); h->m_gate.resize(c.n_layers); h->m_up.resize(c.n_layers);
     h->m_down.resize(c.n_layers);
     for (int l = 0; l < c.n_layers && s == DFLASH_OK; ++l) {
-      s = encode_bf16(&h->m_q[l], h->w_q[l], qw, d, d, kBM);
-      if (s == DFLASH_OK) s = encode_bf16(&h->m_k[l], h->w_k[l], kvw, d, d, kBM);
-      if (s == DFLASH_OK) s = encode_bf16(&h->m_v[l], h->w_v[l], kvw, d, d, kBM);
-      if (s == DFLASH_OK) s = encode_bf16(&h->m_o[l], h->w_o[l], d, qw, qw, kBM);
-      if (s == DFLASH_OK) s = encode_bf16(&h->m_gate[l], h->w_gate[l], c.ffn_dim, d, d, kBM / 2);
-      if (s == DFLASH_OK) s = encode_bf16(&h->m_up[l], h->w_up[l], c.ffn_dim, d, d, kBM / 2);
-      if (s == DFLASH_OK) s = encode_bf16(&h->m_down[l], h->w_down[l], d, c.ffn_dim, c.ffn_dim, kBM);
+      s = enc(&h->m_q[l], h->w_q[l], qw, d, kBM);
+      if (s == DFLASH_OK) s = enc(&h->m_k[l], h->w_k[l], kvw, d, kBM);
+      if (s == DFLASH_OK) s = enc(&h->m_v[l], h->w_v[l], kvw, d, kBM);
+      if (s == DFLASH_OK) s = enc(&h->m_o[l], h->w_o[l], d, qw, kBM);
+      if (s == DFLASH_OK) s = enc(&h->m_gate[l], h->w_gate[l], c.ffn_dim, d, kBM / 2);
+      if (s == DFLASH_OK) s = enc(&h->m_up[l], h->w_up[l], c.ffn_dim, d, kBM / 2);
+      if (s == DFLASH_OK) s = enc(&h->m_down[l], h->w_down[l], d, c.ffn_dim, kBM);
     }
     if (s != DFLASH_OK) return bail(s);
   }
@@ -775,6 +957,16 @@ dflash_status dflash_workspace_size(dflash_handle h, int32_t max_rows, int32_t m
   }
   {
     Carve cv{nullptr};
+    carve_inputs(h, cv, std::max(max_batch, 1), std::max(max_pages, 1));
+    need = std::max(need, cv.off);
+  }
+  {
+    Carve cv{nullptr};
+    carve_target(h, cv, std::max(max_batch, 1), std::max(max_pages, 1));
+    need = std::max(need, cv.off);
+  }
+  {
+    Carve cv{nullptr};
     carve_verify(h, cv, std::max(max_batch, 1), true);
     need = std::max(need, cv.off);
   }
@@ -783,7 +975,7 @@ dflash_status dflash_workspace_size(dflash_handle h, int32_t max_rows, int32_t m
 }
 
 dflash_status dflash_workspace_init(dflash_handle h, void* ws, size_t ws_bytes, void* stream) {
-  if (!h) return fail(DFLASH_EINVAL, "null handle");
+  CHECK_HANDLE(h);
   TRY(check_ws(ws, ws_bytes, kCtlWords * sizeof(int)));
   CUDA_TRY(cudaMemsetAsync(ws, 0, kCtlWords * sizeof(int), static_cast<cudaStream_t>(stream)));
   return DFLASH_OK;
@@ -792,9 +984,10 @@ dflash_status dflash_workspace_init(dflash_handle h, void* ws, size_t ws_bytes, 
 dflash_status dflash_fuse_features(dflash_handle h, const void* x_cat, int32_t n, void* fused,
                                    void* ws, size_t ws_bytes, void* stream) {
   g_launches = 0;
-  if (!h) return fail(DFLASH_EINVAL, "null handle");
+  CHECK_HANDLE(h);
   if (n < 0) return fail(DFLASH_EINVAL, "n < 0");
   if (n == 0) return DFLASH_OK;
+  if (!h->w_fuse) return fail(DFLASH_EINVAL, "the handle has no fusion weights");
   NEED(x_cat, "x_cat");
   NEED(fused, "fused");
   Carve cv{static_cast<char*>(ws)};
@@ -808,12 +1001,13 @@ dflash_status dflash_inject_kv(dflash_handle h, const void* x_cat, const void* f
                                void* const* k_pool, void* const* v_pool, void* fused_out,
                                void* ws, size_t ws_bytes, void* stream) {
   g_launches = 0;
-  if (!h) return fail(DFLASH_EINVAL, "null handle");
+  CHECK_HANDLE(h);
   if (n < 0 || num_pages <= 0) return fail(DFLASH_EINVAL, "bad n or num_pages");
   if (n == 0) return DFLASH_OK;
   if ((x_cat == nullptr) == (fused == nullptr))
     return fail(DFLASH_EINVAL, "exactly one of x_cat and fused must be given");
   if (x_cat) NEED(x_cat, "x_cat");
+  if (x_cat && !h->w_fuse) return fail(DFLASH_EINVAL, "the handle has no fusion weights");
   if (fused) NEED(fused, "fused");
   if (fused_out) NEED(fused_out, "fused_out");
   NEED(positions, "positions");
@@ -823,7 +1017,6 @@ dflash_status dflash_inject_kv(dflash_handle h, const void* x_cat, const void* f
     NEED(k_pool[l], "k_pool[l]");
     NEED(v_pool[l], "v_pool[l]");
   }
-  const auto& c = h->c;
   Carve cv{static_cast<char*>(ws)};
   InjectWs w = carve_inject(h, cv, n);
   TRY(check_ws(ws, ws_bytes, cv.off));
@@ -834,42 +1027,7 @@ dflash_status dflash_inject_kv(dflash_handle h, const void* x_cat, const void* f
     TRY(fuse_impl(h, x_cat, n, dst, w.u, w.gpart, w.ctl, st));
     f = dst;
   }
-  // one GEMM per group of up to 8 layers: segments k_l | v_l
-  for (int l0 = 0; l0 < c.n_layers; l0 += kMaxSeg / 2) {
-    const int nl = std::min(kMaxSeg / 2, c.n_layers - l0);
-    WSet ws_;
-    for (int l = l0; l < l0 + nl; ++l) {
-      ws_.add(h->bf16 ? &h->m_k[l] : nullptr, h->w_k[l], c.n_kv_heads * c.head_dim);
-      ws_.add(h->bf16 ? &h->m_v[l] : nullptr, h->w_v[l], c.n_kv_heads * c.head_dim);
-    }
-    auto fill = [&](auto& e, auto* tag) {
-      using T = std::remove_pointer_t<decltype(tag)>;
-      e.pos = positions;
-      e.rope = h->d_rope;
-      e.max_pos = c.max_position;
-      e.S = c.block_size;
-      e.hq = c.n_q_heads;
-      e.hkv = c.n_kv_heads;
-      e.hd = c.head_dim;
-      for (int l = 0; l < nl; ++l) {
-        e.kpool[l] = static_cast<T*>(k_pool[l0 + l]);
-        e.vpool[l] = static_cast<T*>(v_pool[l0 + l]);
-      }
-      e.slots = slots;
-      e.num_slots = (long long)num_pages * kPage;
-      e.err = h->d_err;
-    };
-    if (h->bf16) {
-      EpiArgs<bf16> e = {};
-      fill(e, static_cast<bf16*>(nullptr));
-      TRY((gemm<EPI_KV, bf16>(h, f, n, c.d_model, ws_, e, w.gpart, w.ctl, st)));
-    } else {
-      EpiArgs<float> e = {};
-      fill(e, static_cast<float*>(nullptr));
-      TRY((gemm<EPI_KV, float>(h, f, n, c.d_model, ws_, e, w.gpart, w.ctl, st)));
-    }
-  }
-  return DFLASH_OK;
+  return inject_impl(h, f, n, positions, slots, num_pages, k_pool, v_pool, w, st);
 }
 
 dflash_status dflash_draft_block(dflash_handle h, const int32_t* block_ids,
@@ -878,7 +1036,7 @@ dflash_status dflash_draft_block(dflash_handle h, const int32_t* block_ids,
                                  void* const* k_pool, void* const* v_pool, void* final_hidden,
                                  void* ws, size_t ws_bytes, void* stream) {
   g_launches = 0;
-  if (!h) return fail(DFLASH_EINVAL, "null handle");
+  CHECK_HANDLE(h);
   if (batch < 0 || max_pages < 0 || num_pages <= 0) return fail(DFLASH_EINVAL, "bad sizes");
   if (batch == 0) return DFLASH_OK;
   NEED(block_ids, "block_ids");
@@ -896,18 +1054,342 @@ dflash_status dflash_draft_block(dflash_handle h, const int32_t* block_ids,
   TRY(check_ws(ws, ws_bytes, cv.off));
   if ((long long)batch * h->c.n_kv_heads > 2 * kTileWords) return fail(DFLASH_EUNSUPPORTED, "batch too large");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  StackOpts o;
+  o.ids = block_ids;
+  o.final_hidden = final_hidden;
   if (h->bf16)
-    return draft_impl<bf16>(h, block_ids, ctx_lens, page_table, max_pages, batch, num_pages,
-                            k_pool, v_pool, final_hidden, w, st);
-  return draft_impl<float>(h, block_ids, ctx_lens, page_table, max_pages, batch, num_pages,
-                           k_pool, v_pool, final_hidden, w, st);
+    return draft_impl<bf16>(h, o, ctx_lens, page_table, max_pages, batch, num_pages, k_pool,
+                            v_pool, w, st);
+  return draft_impl<float>(h, o, ctx_lens, page_table, max_pages, batch, num_pages, k_pool,
+                           v_pool, w, st);
+}
+
+}  // extern "C"
+
+namespace {
+// Host checks shared by the calls that run the layer stack over S rows per sequence.
+dflash_status check_stack_args(const H* h, const int32_t* ctx_lens, const int32_t* page_table,
+                               int32_t max_pages, int32_t batch, int32_t num_pages,
+                               void* const* k_pool, void* const* v_pool) {
+  if (batch < 0 || max_pages < 0 || num_pages <= 0) return fail(DFLASH_EINVAL, "bad sizes");
+  NEED(ctx_lens, "ctx_lens");
+  if (max_pages > 0) NEED(page_table, "page_table");
+  if (!k_pool || !v_pool) return fail(DFLASH_EINVAL, "pool arrays are NULL");
+  for (int l = 0; l < h->c.n_layers; ++l) {
+    NEED(k_pool[l], "k_pool[l]");
+    NEED(v_pool[l], "v_pool[l]");
+  }
+  if ((long long)batch * h->c.block_size > (1 << 20) ||
+      (long long)batch * h->c.n_kv_heads > 2 * kTileWords)
+    return fail(DFLASH_EUNSUPPORTED, "batch too large");
+  return DFLASH_OK;
+}
+}  // namespace
+
+extern "C" {
+
+dflash_status dflash_inject_inputs(dflash_handle h, const void* x_cat, const int32_t* ctx_lens,
+                                   const int32_t* page_table, int32_t max_pages, int32_t batch,
+                                   int32_t num_pages, void* const* k_pool, void* const* v_pool,
+                                   void* fused_out, void* ws, size_t ws_bytes, void* stream) {
+  g_launches = 0;
+  CHECK_HANDLE(h);
+  TRY(check_stack_args(h, ctx_lens, page_table, max_pages, batch, num_pages, k_pool, v_pool));
+  if (batch == 0) return DFLASH_OK;
+  if (!h->w_fuse) return fail(DFLASH_EINVAL, "the handle has no fusion weights");
+  NEED(x_cat, "x_cat");
+  if (fused_out) NEED(fused_out, "fused_out");
+  Carve cv{static_cast<char*>(ws)};
+  InputsWs w = carve_inputs(h, cv, batch, max_pages);
+  TRY(check_ws(ws, ws_bytes, cv.off));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int M = batch * h->c.block_size;
+  void* fused = fused_out ? fused_out : w.fused;
+  TRY(fuse_impl(h, x_cat, M, fused, w.u, w.d.gpart, w.d.ctl, st));
+  StackOpts o;
+  o.rows = fused;
+  o.causal = true;
+  o.write_cache = true;
+  if (h->bf16)
+    return draft_impl<bf16>(h, o, ctx_lens, page_table, max_pages, batch, num_pages, k_pool,
+                            v_pool, w.d, st);
+  return draft_impl<float>(h, o, ctx_lens, page_table, max_pages, batch, num_pages, k_pool,
+                           v_pool, w.d, st);
+}
+
+dflash_status dflash_target_forward(dflash_handle h, const int32_t* ids, const int32_t* ctx_lens,
+                                    const int32_t* page_table, int32_t max_pages, int32_t batch,
+                                    int32_t num_pages, void* const* k_pool, void* const* v_pool,
+                                    const int32_t* tap_layers, int32_t n_taps, void* taps,
+                                    float* logits, void* ws, size_t ws_bytes, void* stream) {
+  g_launches = 0;
+  CHECK_HANDLE(h);
+  TRY(check_stack_args(h, ctx_lens, page_table, max_pages, batch, num_pages, k_pool, v_pool));
+  if (batch == 0) return DFLASH_OK;
+  NEED(ids, "ids");
+  if (n_taps < 0 || (n_taps > 0 && (!tap_layers || !taps)))
+    return fail(DFLASH_EINVAL, "taps: n_taps %d with tap_layers %p, taps %p", n_taps,
+                (const void*)tap_layers, taps);
+  if (taps) NEED(taps, "taps");
+  for (int t = 0; t < n_taps; ++t)
+    if (tap_layers[t] < 1 || tap_layers[t] > h->c.n_layers)
+      return fail(DFLASH_EINVAL, "tap layer %d outside 1..%d", tap_layers[t], h->c.n_layers);
+  if (logits) NEED(logits, "logits");
+  Carve cv{static_cast<char*>(ws)};
+  TargetWs w = carve_target(h, cv, batch, max_pages);
+  TRY(check_ws(ws, ws_bytes, cv.off));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  StackOpts o;
+  o.ids = ids;
+  o.causal = true;
+  o.write_cache = true;
+  o.tap_layers = tap_layers;
+  o.n_taps = n_taps;
+  o.taps = taps;
+  o.final_hidden = logits ? w.hfin : nullptr;
+  const int M = batch * h->c.block_size;
+  if (h->bf16) {
+    TRY(draft_impl<bf16>(h, o, ctx_lens, page_table, max_pages, batch, num_pages, k_pool, v_pool,
+                         w.d, st));
+  } else {
+    TRY(draft_impl<float>(h, o, ctx_lens, page_table, max_pages, batch, num_pages, k_pool,
+                          v_pool, w.d, st));
+  }
+  if (!logits) return DFLASH_OK;
+  // the target's logits of every row, fp32 (verification reads them)
+  WSet ws_;
+  ws_.add(h->bf16 ? &h->m_lm : nullptr, h->lm_head, h->c.vocab);
+  if (h->bf16) {
+    EpiArgs<bf16> e = {};
+    e.y = logits;
+    e.ldy = h->c.vocab;
+    e.err = h->d_err;
+    return gemm<EPI_F32, bf16>(h, w.hfin, M, h->c.d_model, ws_, e, w.d.gpart, w.d.ctl, st);
+  }
+  EpiArgs<float> e = {};
+  e.y = logits;
+  e.ldy = h->c.vocab;
+  e.err = h->d_err;
+  return gemm<EPI_F32, float>(h, w.hfin, M, h->c.d_model, ws_, e, w.d.gpart, w.d.ctl, st);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ speculative loop
+namespace {
+// The loop's workspace: a region for the drafter's calls (block pass, LM head,
+// verification scratch, injection; they run one after another), a region for the
+// target's block pass, then the buffers that live from one call of the step to the next.
+struct SpecWs {
+  char* dreg;
+  char* treg;
+  void *hidden, *taps;
+  int *draft, *tids, *out, *nacc, *pos, *slots;
+  float *logits, *dmax;
+  size_t dreg_bytes, treg_bytes;
+};
+
+size_t region_bytes(const H* hd, int B, int max_pages) {
+  const int M = B * hd->c.block_size;
+  size_t need = 0;
+  auto upd = [&](auto f) {
+    Carve cv{nullptr};
+    f(cv);
+    need = std::max(need, cv.off);
+  };
+  upd([&](Carve& cv) { carve_draft(hd, cv, B, max_pages); });
+  upd([&](Carve& cv) { carve_head(hd, cv, M); });
+  upd([&](Carve& cv) { carve_inject(hd, cv, M); });
+  upd([&](Carve& cv) { carve_verify(hd, cv, B, false); });
+  return (need + 255) & ~size_t(255);
+}
+
+SpecWs carve_spec(const H* hd, const H* ht, Carve& cv, int B, int max_pages) {
+  const int M = B * hd->c.block_size;
+  SpecWs w;
+  w.dreg_bytes = region_bytes(hd, B, max_pages);
+  Carve ct{nullptr};
+  carve_target(ht, ct, B, max_pages);
+  w.treg_bytes = (ct.off + 255) & ~size_t(255);
+  w.dreg = cv.take<char>(w.dreg_bytes);
+  w.treg = cv.take<char>(w.treg_bytes);
+  w.hidden = cv.take<char>((size_t)M * hd->c.d_model * elt(hd));
+  w.taps = cv.take<char>((size_t)M * hd->c.n_target_layers * hd->c.target_width * elt(hd));
+  w.draft = cv.take<int>(M);
+  w.tids = cv.take<int>(M);
+  w.out = cv.take<int>(M);
+  w.nacc = cv.take<int>(B);
+  w.pos = cv.take<int>(M);
+  w.slots = cv.take<int>(M);
+  w.logits = cv.take<float>((size_t)M * ht->c.vocab);
+  w.dmax = cv.take<float>(M);
+  return w;
+}
+
+dflash_status check_pair(const H* hd, const H* ht) {
+  const auto &a = hd->c, &b = ht->c;
+  if (!hd->w_fuse) return fail(DFLASH_EINVAL, "the drafter handle has no fusion weights");
+  if (b.d_model != a.target_width || b.vocab != a.vocab || b.block_size != a.block_size ||
+      b.dtype != a.dtype || hd->dev != ht->dev)
+    return fail(DFLASH_EINVAL,
+                "target (d %d, vocab %d, block %d) does not match the drafter (target width "
+                "%d, vocab %d, block %d), or dtype/device differ",
+                b.d_model, b.vocab, b.block_size, a.target_width, a.vocab, a.block_size);
+  return DFLASH_OK;
+}
+
+template <typename T>
+dflash_status spec_impl(H* hd, H* ht, const dflash_spec_state& s, const SpecWs& w,
+                        cudaStream_t st) {
+  const int B = s.batch, S = hd->c.block_size, M = B * S, V = hd->c.vocab;
+  int* draft = s.drafts ? s.drafts : w.draft;
+  // 1. draft the block [anchor, mask, ...] over the drafter's cache
+  {
+    Carve cv{w.dreg};
+    DraftWs dw = carve_draft(hd, cv, B, s.max_pages);
+    StackOpts o;
+    o.ids = s.block_ids;
+    o.final_hidden = w.hidden;
+    TRY(draft_impl<T>(hd, o, s.ctx_lens, s.page_table, s.max_pages, B, s.num_pages, s.d_k_pool,
+                      s.d_v_pool, dw, st));
+  }
+  // 2. the drafter's tokens (LM head + argmax, logits never stored)
+  {
+    Carve cv{w.dreg};
+    HeadWs hw = carve_head(hd, cv, M);
+    TRY(head_impl<T>(hd, w.hidden, M, 1.0f, draft, w.dmax, nullptr, hw, st));
+  }
+  // 3. the target's pass over [anchor, drafts 1..S-1]: its cache, the tap features of
+  //    the block's tokens and fp32 logits of every row
+  TRY(launch(k_spec_target_ids, dim3(ceil_div(M, 128)), dim3(128), 0, st,
+             static_cast<const int*>(s.block_ids), static_cast<const int*>(draft), M, S,
+             w.tids));
+  {
+    Carve cv{w.treg};
+    TargetWs tw = carve_target(ht, cv, B, s.max_pages);
+    StackOpts o;
+    o.ids = w.tids;
+    o.causal = true;
+    o.write_cache = true;
+    o.tap_layers = s.tap_layers;
+    o.n_taps = hd->c.n_target_layers;
+    o.taps = w.taps;
+    o.final_hidden = tw.hfin;
+    TRY(draft_impl<T>(ht, o, s.ctx_lens, s.page_table, s.max_pages, B, s.num_pages, s.t_k_pool,
+                      s.t_v_pool, tw.d, st));
+    WSet ws_;
+    ws_.add(ht->bf16 ? &ht->m_lm : nullptr, ht->lm_head, V);
+    EpiArgs<T> e = {};
+    e.y = w.logits;
+    e.ldy = V;
+    e.err = ht->d_err;
+    TRY((gemm<EPI_F32, T>(ht, tw.hfin, M, ht->c.d_model, ws_, e, tw.d.gpart, tw.d.ctl, st)));
+  }
+  // 4. synthetic agreement (optional), then greedy verification with the anchor in slot 0
+  if (s.plant_u)
+    TRY(launch(k_spec_plant, dim3(M), dim3(kRowThreads), 0, st, w.logits,
+               static_cast<const int*>(draft), s.plant_u, s.plant_steps,
+               static_cast<const int*>(s.step), s.plant_p, S, V, M, hd->d_err));
+  {
+    Carve cv{w.dreg};
+    VerifyWs vw = carve_verify(hd, cv, B, false);
+    const int nch = verify_chunks(hd, M), chunk = chunk_of(hd, nch);
+    TRY(launch(k_verify_greedy<float>, dim3(nch, M), dim3(kRowThreads), 0, st,
+               static_cast<const float*>(w.logits), static_cast<const int*>(draft), S, V,
+               chunk, vw.pv, vw.pi, vw.ctl, w.out, w.nacc, s.n_emitted, hd->d_err, 1));
+  }
+  // 5. commit: emitted tokens, next anchor, context length, injection slots
+  TRY(launch(k_spec_commit, dim3(ceil_div(B, 64)), dim3(64), 0, st,
+             static_cast<const int*>(w.out), static_cast<const int*>(s.n_emitted), B, S,
+             s.mask_id, s.block_ids, s.ctx_lens, s.page_table, s.max_pages, w.pos, w.slots,
+             s.generated, s.max_new, s.n_generated, s.step, hd->d_err));
+  // 6. the block's target features into the drafter's cache (every row: rows past the
+  //    new context length are overwritten by the next step's injection)
+  {
+    Carve cv{w.dreg};
+    InjectWs iw = carve_inject(hd, cv, M);
+    TRY(fuse_impl(hd, w.taps, M, iw.fused, iw.u, iw.gpart, iw.ctl, st));
+    TRY(inject_impl(hd, iw.fused, M, w.pos, w.slots, s.num_pages, s.d_k_pool, s.d_v_pool, iw,
+                    st));
+  }
+  return DFLASH_OK;
+}
+}  // namespace
+
+extern "C" {
+
+dflash_status dflash_spec_workspace_size(dflash_handle drafter, dflash_handle target,
+                                         int32_t batch, int32_t max_pages, size_t* bytes) {
+  if (!drafter || !target || !bytes) return fail(DFLASH_EINVAL, "null argument");
+  if (batch <= 0 || max_pages <= 0) return fail(DFLASH_EINVAL, "bad sizes");
+  TRY(check_pair(drafter, target));
+  Carve cv{nullptr};
+  carve_spec(drafter, target, cv, batch, max_pages);
+  *bytes = cv.off;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_spec_workspace_init(dflash_handle drafter, dflash_handle target,
+                                         int32_t batch, int32_t max_pages, void* ws,
+                                         size_t ws_bytes, void* stream) {
+  CHECK_HANDLE(drafter);
+  CHECK_HANDLE(target);
+  TRY(check_pair(drafter, target));
+  Carve cv{static_cast<char*>(ws)};
+  SpecWs w = carve_spec(drafter, target, cv, batch, max_pages);
+  TRY(check_ws(ws, ws_bytes, cv.off));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CUDA_TRY(cudaMemsetAsync(w.dreg, 0, kCtlWords * sizeof(int), st));
+  CUDA_TRY(cudaMemsetAsync(w.treg, 0, kCtlWords * sizeof(int), st));
+  return DFLASH_OK;
+}
+
+dflash_status dflash_spec_step(dflash_handle drafter, dflash_handle target,
+                               const dflash_spec_state* s, void* ws, size_t ws_bytes,
+                               void* stream) {
+  g_launches = 0;
+  CHECK_HANDLE(drafter);
+  CHECK_HANDLE(target);
+  if (!s) return fail(DFLASH_EINVAL, "null state");
+  TRY(check_pair(drafter, target));
+  if (s->batch <= 0) return fail(DFLASH_EINVAL, "batch must be positive");
+  TRY(check_stack_args(drafter, s->ctx_lens, s->page_table, s->max_pages, s->batch,
+                       s->num_pages, s->d_k_pool, s->d_v_pool));
+  TRY(check_stack_args(target, s->ctx_lens, s->page_table, s->max_pages, s->batch,
+                       s->num_pages, s->t_k_pool, s->t_v_pool));
+  NEED(s->block_ids, "block_ids");
+  NEED(s->generated, "generated");
+  NEED(s->n_generated, "n_generated");
+  NEED(s->n_emitted, "n_emitted");
+  NEED(s->step, "step");
+  if (s->drafts) NEED(s->drafts, "drafts");
+  if (!s->tap_layers) return fail(DFLASH_EINVAL, "tap_layers is NULL");
+  for (int t = 0; t < drafter->c.n_target_layers; ++t)
+    if (s->tap_layers[t] < 1 || s->tap_layers[t] > target->c.n_layers)
+      return fail(DFLASH_EINVAL, "tap layer %d outside 1..%d", s->tap_layers[t],
+                  target->c.n_layers);
+  if (s->max_new <= 0) return fail(DFLASH_EINVAL, "max_new must be positive");
+  if (s->mask_id < 0 || s->mask_id >= drafter->c.vocab) return fail(DFLASH_EINVAL, "bad mask_id");
+  if (s->plant_u) {
+    NEED(s->plant_u, "plant_u");
+    if (s->plant_steps <= 0) return fail(DFLASH_EINVAL, "plant_steps must be positive");
+  }
+  if (drafter->c.block_size < 2) return fail(DFLASH_EUNSUPPORTED, "block_size must be >= 2");
+  const long long M = (long long)s->batch * drafter->c.block_size;
+  if (M > 65535) return fail(DFLASH_EUNSUPPORTED, "batch*block_size > 65535");
+  Carve cv{static_cast<char*>(ws)};
+  SpecWs w = carve_spec(drafter, target, cv, s->batch, s->max_pages);
+  TRY(check_ws(ws, ws_bytes, cv.off));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (drafter->bf16) return spec_impl<bf16>(drafter, target, *s, w, st);
+  return spec_impl<float>(drafter, target, *s, w, st);
 }
 
 dflash_status dflash_lm_head_argmax(dflash_handle h, const void* hidden, int32_t rows,
                                     float temperature, int32_t* tokens, float* max_logit,
                                     float* lse, void* ws, size_t ws_bytes, void* stream) {
   g_launches = 0;
-  if (!h) return fail(DFLASH_EINVAL, "null handle");
+  CHECK_HANDLE(h);
   if (rows < 0) return fail(DFLASH_EINVAL, "rows < 0");
   if (rows == 0) return DFLASH_OK;
   NEED(hidden, "hidden");
@@ -929,7 +1411,7 @@ dflash_status dflash_verify_greedy(dflash_handle h, const int32_t* draft,
                                    int32_t* n_accepted, int32_t* n_emitted, void* ws,
                                    size_t ws_bytes, void* stream) {
   g_launches = 0;
-  if (!h) return fail(DFLASH_EINVAL, "null handle");
+  CHECK_HANDLE(h);
   if (batch < 0) return fail(DFLASH_EINVAL, "batch < 0");
   if (batch == 0) return DFLASH_OK;
   NEED(draft, "draft");
@@ -948,10 +1430,10 @@ dflash_status dflash_verify_greedy(dflash_handle h, const int32_t* draft,
   if (h->bf16)
     return launch(k_verify_greedy<bf16>, dim3(nch, rows), dim3(kRowThreads), 0, st,
                   static_cast<const bf16*>(target_logits), draft, S, V, chunk, w.pv, w.pi, w.ctl,
-                  out_tokens, n_accepted, n_emitted, h->d_err);
+                  out_tokens, n_accepted, n_emitted, h->d_err, 0);
   return launch(k_verify_greedy<float>, dim3(nch, rows), dim3(kRowThreads), 0, st,
                 static_cast<const float*>(target_logits), draft, S, V, chunk, w.pv, w.pi, w.ctl,
-                out_tokens, n_accepted, n_emitted, h->d_err);
+                out_tokens, n_accepted, n_emitted, h->d_err, 0);
 }
 
 dflash_status dflash_verify_sample(dflash_handle h, const int32_t* draft, const void* final_hidden,
@@ -961,7 +1443,7 @@ dflash_status dflash_verify_sample(dflash_handle h, const int32_t* draft, const 
                                    int32_t* n_accepted, int32_t* n_emitted, void* ws,
                                    size_t ws_bytes, void* stream) {
   g_launches = 0;
-  if (!h) return fail(DFLASH_EINVAL, "null handle");
+  CHECK_HANDLE(h);
   if (batch < 0) return fail(DFLASH_EINVAL, "batch < 0");
   if (!(temperature > 0.f)) return fail(DFLASH_EINVAL, "temperature must be > 0");
   if (batch == 0) return DFLASH_OK;
@@ -988,10 +1470,35 @@ dflash_status dflash_verify_sample(dflash_handle h, const int32_t* draft, const 
 }
 
 dflash_status dflash_get_device_error(dflash_handle h, int32_t* code, int32_t clear) {
-  if (!h || !code) return fail(DFLASH_EINVAL, "null argument");
+  if (!code) return fail(DFLASH_EINVAL, "null argument");
+  CHECK_HANDLE(h);
   CUDA_TRY(cudaDeviceSynchronize());
   CUDA_TRY(cudaMemcpy(code, h->d_err, sizeof(int), cudaMemcpyDeviceToHost));
   if (clear) CUDA_TRY(cudaMemset(h->d_err, 0, sizeof(int)));
+  return DFLASH_OK;
+}
+
+dflash_status dflash_fp8_packed_bytes(int32_t rows, int32_t cols, size_t* bytes) {
+  if (!bytes || rows <= 0 || cols <= 0) return fail(DFLASH_EINVAL, "bad arguments");
+  *bytes = fp8_packed_bytes(rows, cols);
+  return DFLASH_OK;
+}
+
+dflash_status dflash_pack_fp8(const void* w, int32_t rows, int32_t cols, void* packed,
+                              void* stream) {
+  g_launches = 0;
+  if (rows <= 0 || cols <= 0) return fail(DFLASH_EINVAL, "bad sizes");
+  NEED(w, "w");
+  NEED(packed, "packed");
+  uint8_t* codes = static_cast<uint8_t*>(packed);
+  float* scales = reinterpret_cast<float*>(codes + fp8_scale_offset(rows, cols));
+  return launch(k_pack_fp8, dim3(rows), dim3(kRowThreads), 0, static_cast<cudaStream_t>(stream),
+                static_cast<const bf16*>(w), cols, codes, static_cast<int>(fp8_ld(cols)), scales);
+}
+
+dflash_status dflash_test_force_timeout(dflash_handle h, int32_t enable) {
+  CHECK_HANDLE(h);
+  h->force_timeout = enable != 0;
   return DFLASH_OK;
 }
 
@@ -1035,7 +1542,7 @@ extern "C" dflash_status dflash_verify_greedy_static(dflash_handle h, const int3
                                                      int32_t* out_tokens, int32_t* n_accepted,
                                                      int32_t* n_emitted, void* stream) {
   g_launches = 0;
-  if (!h) return fail(DFLASH_EINVAL, "null handle");
+  CHECK_HANDLE(h);
   if (batch < 0) return fail(DFLASH_EINVAL, "batch < 0");
   if (batch == 0) return DFLASH_OK;
   NEED(draft, "draft");
@@ -1070,8 +1577,8 @@ extern "C" dflash_status dflash_verify_greedy_static(dflash_handle h, const int3
   if (h->bf16)
     return launch(k_verify_greedy<bf16>, dim3(nch, rows), dim3(kRowThreads), 0, st,
                   static_cast<const bf16*>(target_logits), draft, S, V, chunk, pv, pi, ctr,
-                  out_tokens, n_accepted, n_emitted, h->d_err);
+                  out_tokens, n_accepted, n_emitted, h->d_err, 0);
   return launch(k_verify_greedy<float>, dim3(nch, rows), dim3(kRowThreads), 0, st,
                 static_cast<const float*>(target_logits), draft, S, V, chunk, pv, pi, ctr,
-                out_tokens, n_accepted, n_emitted, h->d_err);
+                out_tokens, n_accepted, n_emitted, h->d_err, 0);
 }

@@ -2,7 +2,8 @@
 //
 // For sequence b and kv head g the S*G query rows (block slot i, q head g*G + hh, row
 // i*G + hh) attend, with no mask, to the sequence's ctx_len cached context keys
-// (injected target features) followed by the block's own S keys.  Keys are walked a
+// (injected target features) followed by the block's own S keys (with `causal`, slot i
+// sees the block keys 0..i only: chunks of new context run through the layer stack).  Keys are walked a
 // 16-token page at a time; the work of one (b, g) is split over CTAs by contiguous
 // ranges of pages (split-context, "flash-decoding"), each CTA keeps an online softmax
 // (running max in the log2 domain, running sum, unnormalised output) and publishes
@@ -37,6 +38,10 @@ struct AttnArgs {
   float* part_ml;    // [B][hkv][nsplit][QR][2]
   T* out;            // [B*S][hq*hd]
   int* err;
+  // 0: every query row sees all S block keys (the drafter's block); 1: query row r
+  // (block slot r / G) sees block keys 0..r / G only (a causal chunk of new context or
+  // target tokens)
+  int causal;
 };
 
 // Tensor maps of the tcgen05 attention kernel: q as [B*hkv*QR, hd] with 128-row boxes,
@@ -246,6 +251,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       }
       const int pg = p0 + i;
       const int valid = (pg < np) ? min(kPage, T - pg * kPage) : a.S;
+      const bool cmask = a.causal && pg >= np;   // block keys past the row's own slot
       const uint32_t kbase = smem_u32(stages + s * C::STAGE);
       const uint32_t vbase = kbase + C::TILE;
       float sacc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
@@ -261,13 +267,15 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       // mask keys past `valid` (only a page's last keys can be), row max on raw scores
       // (the scale is positive), then scale and reference in one FMA per key: the log2
       // domain probabilities 2^(s*sc - m)
-      if (valid < kPage) {
+      if (valid < kPage || cmask) {
+        const int G = a.hq / a.hkv;
+        const int slot0 = cmask ? (qr0 + g8) / G : kPage, slot1 = cmask ? (qr0 + g8 + 8) / G : kPage;
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int key = n * 8 + 2 * t4 + (c & 1);
-            if (key >= valid) sacc[n][c] = -INFINITY;
+            if (key >= valid || key > (c < 2 ? slot0 : slot1)) sacc[n][c] = -INFINITY;
           }
       }
       float mx0 = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
@@ -398,7 +406,8 @@ static __global__ void __launch_bounds__(128) k_attn_f32(const AttnArgs<float> a
       int r = x / kPage, k = x % kPage;
       float s = 0.f;
       for (int d = 0; d < hd; ++d) s = fmaf(Qs[r * hd + d], Ks[k * hd + d], s);
-      Ss[x] = k < valid ? s * sc : -INFINITY;
+      const bool seen = k < valid && !(a.causal && pg >= np && k > r / (a.hq / a.hkv));
+      Ss[x] = seen ? s * sc : -INFINITY;
     }
     __syncthreads();
     for (int r = tid; r < QR; r += 128) {

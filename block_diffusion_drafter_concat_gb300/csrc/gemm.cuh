@@ -81,6 +81,14 @@ struct GemmShape {
   int seg_rows[kMaxSeg];  // rows of each weight matrix
   float* part;      // [grid][2][BN * kBM] partial tiles (split pieces)
   int* counters;    // one per output tile
+  // the finisher of a split tile waits for (contributors - 1 + wait_extra) publications
+  // for at most wait_ns: wait_extra is 0 except under the forced-timeout test hook,
+  // which asks for one publication more than can arrive
+  int wait_extra;
+  unsigned long long wait_ns;
+  // FP8 weights (k_gemm_tc<..., true>): per-segment row scales, applied to each
+  // contribution as it leaves the accumulators (null for bf16 / fp32 weights)
+  const float* wscale[kMaxSeg];
 };
 
 // ---------------------------------------------------------------------------- epilogue
@@ -372,11 +380,16 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
 }
 
 // ------------------------------------------------------------- tensor-core kernel
-template <int BN>
+// A pipeline stage: a 128-row weight box and the matching activation box(es).  bf16
+// weights: 64 k per stage (128 x 128 B); FP8 weights: 128 k per stage (128 x 128 B of
+// e4m3 codes) and two 64-k activation boxes.
+template <int BN, bool F8 = false>
 struct TcCfg {
-  static constexpr int NS = BN == 16 ? 10 : BN == 32 ? 8 : BN == 64 ? 6 : 4;
-  static constexpr int W_BYTES = kBM * kBK * 2;
-  static constexpr int A_BYTES = BN * kBK * 2;
+  static constexpr int KS = F8 ? 2 * kBK : kBK;          // k per stage
+  static constexpr int NS = F8 ? (BN == 16 ? 9 : 7)
+                               : (BN == 16 ? 10 : BN == 32 ? 8 : BN == 64 ? 6 : 4);
+  static constexpr int W_BYTES = kBM * kBK * 2;           // 16 KB either way
+  static constexpr int A_BYTES = BN * KS * 2;
   static constexpr int STAGE = W_BYTES + A_BYTES;
   static constexpr int PITCH = kBM + 4;
   static constexpr int CS_BYTES = BN * PITCH * 4;
@@ -463,6 +476,54 @@ struct UnitWalk {
   }
 };
 
+// Scale of weight row `wr` (0..127) of n-tile nt: its segment's row scale (paired
+// tiles: 64 rows of segment 0 then the same 64 rows of segment 1).  Rows past a
+// segment's end (zero-filled boxes) take 0.
+__device__ __forceinline__ float tile_row_scale(const GemmShape& g, int nt, int wr) {
+  int seg = 0, row;
+  if (g.paired) {
+    seg = wr >> 6;
+    row = nt * (kBM / 2) + (wr & 63);
+  } else {
+    while (seg + 1 < g.nseg && nt >= g.seg_tile0[seg + 1]) ++seg;
+    row = (nt - g.seg_tile0[seg]) * kBM + wr;
+  }
+  return row < g.seg_rows[seg] ? __ldg(g.wscale[seg] + row) : 0.f;
+}
+
+__device__ __forceinline__ uint2 lds_u2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint4 lds_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+// Two e4m3 codes (low byte first) as an f16 pair (exact: every e4m3 value is an f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+// A bf16 pair as an f16 pair (round to nearest; exact in f16's normal range).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+// D = A(16x16, row) * B(16x8, col) + D, f16 inputs, fp32 accumulation.
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
+      " {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // Greedy LM head: after this CTA's epilogues, count it; the last CTA of the grid turns
 // the rows' packed keys into tokens (and max logits) and clears keys and counter.
 template <typename T, typename Sync>
@@ -486,11 +547,17 @@ __device__ __forceinline__ void argmax_keys_finish(const EpiArgs<T>& e, int M, i
   if (tid == 0) *e.am_done = 0;
 }
 
-template <int BN, int EPI>
+// F8 = true: the weights are FP8 e4m3 codes with per-row scales (g.wscale); the MMA
+// runs on f16 operands (e4m3 and bf16 values are exact in f16 but for bf16 values
+// below 2^-14, whose few lowest bits f16 subnormals drop).  Within every 32-k chunk the
+// k index is permuted alike for both operands so that a lane reads 8 consecutive weight
+// bytes and 8 consecutive activations: MMA 1 takes k 8t..8t+3, MMA 2 k 8t+4..8t+7 of
+// lane group t (the contraction sums over every k once either way).
+template <int BN, int EPI, bool F8 = false>
 __global__ void __launch_bounds__(160, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ WMaps wm,
               const GemmShape g, const EpiArgs<bf16> e) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
@@ -525,17 +592,20 @@ __global__ void __launch_bounds__(160, 1)
       UnitWalk wc, ac;
       wc.start(g, u0);
       ac = wc;
+      // weight boxes are 128 bytes wide: 64 bf16 or 128 e4m3 values of k
       auto issue_w = [&](int s, const UnitWalk& w) {
         uint8_t* st = stages + s * C::STAGE;
         if (g.paired) {
-          tma_load_2d_hint(st, &wm.m[0], &full[s], w.ks * kBK, w.row, pol);
-          tma_load_2d_hint(st + C::W_BYTES / 2, &wm.m[1], &full[s], w.ks * kBK, w.row, pol);
+          tma_load_2d_hint(st, &wm.m[0], &full[s], w.ks * C::KS, w.row, pol);
+          tma_load_2d_hint(st + C::W_BYTES / 2, &wm.m[1], &full[s], w.ks * C::KS, w.row, pol);
         } else {
-          tma_load_2d_hint(st, &wm.m[w.seg], &full[s], w.ks * kBK, w.row, pol);
+          tma_load_2d_hint(st, &wm.m[w.seg], &full[s], w.ks * C::KS, w.row, pol);
         }
       };
       auto issue_a = [&](int s, const UnitWalk& w) {
-        tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmA, &full[s], w.ks * kBK, w.mb * BN);
+        uint8_t* at = stages + s * C::STAGE + C::W_BYTES;
+        tma_load_2d(at, &tmA, &full[s], w.ks * C::KS, w.mb * BN);
+        if constexpr (F8) tma_load_2d(at + BN * 128, &tmA, &full[s], w.ks * C::KS + kBK, w.mb * BN);
       };
       const int pre = min(C::NS, n_my);
       for (int i = 0; i < pre; ++i) {
@@ -606,6 +676,43 @@ __global__ void __launch_bounds__(160, 1)
       }
       const uint32_t wbase = smem_u32(stages + s * C::STAGE);
       const uint32_t abase = wbase + C::W_BYTES;
+      if constexpr (F8) {
+#pragma unroll
+        for (int kc = 0; kc < 4; ++kc) {
+          uint32_t a1[2][4], a2[2][4];
+#pragma unroll
+          for (int ms = 0; ms < 2; ++ms) {
+            const int row = warp * 32 + ms * 16 + g8;
+            const uint32_t off = ((kc * 32 + 8 * t4) & 15);
+            const uint2 w0 = lds_u2(wbase + swz128(row, kc * 2 + (t4 >> 1)) + off);
+            const uint2 w1 = lds_u2(wbase + swz128(row + 8, kc * 2 + (t4 >> 1)) + off);
+            a1[ms][0] = e4m3x2_to_f16x2(w0.x & 0xffffu);
+            a1[ms][1] = e4m3x2_to_f16x2(w1.x & 0xffffu);
+            a1[ms][2] = e4m3x2_to_f16x2(w0.x >> 16);
+            a1[ms][3] = e4m3x2_to_f16x2(w1.x >> 16);
+            a2[ms][0] = e4m3x2_to_f16x2(w0.y & 0xffffu);
+            a2[ms][1] = e4m3x2_to_f16x2(w1.y & 0xffffu);
+            a2[ms][2] = e4m3x2_to_f16x2(w0.y >> 16);
+            a2[ms][3] = e4m3x2_to_f16x2(w1.y >> 16);
+          }
+          // activations: box kc / 2, 16-byte chunk (kc % 2) * 4 + t of row nb * 8 + g8
+          const uint32_t ab = abase + (kc >> 1) * (BN * 128);
+#pragma unroll
+          for (int nb = 0; nb < BN / 8; ++nb) {
+            const uint4 v = lds_u4(ab + swz128(nb * 8 + g8, (kc & 1) * 4 + t4));
+            const uint32_t h0 = bf16x2_to_f16x2(v.x), h1 = bf16x2_to_f16x2(v.y);
+            const uint32_t h2 = bf16x2_to_f16x2(v.z), h3 = bf16x2_to_f16x2(v.w);
+#pragma unroll
+            for (int ms = 0; ms < 2; ++ms) {
+              mma_f16(acc[ms][nb], a1[ms], h0, h1);
+              mma_f16(acc[ms][nb], a2[ms], h2, h3);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        continue;
+      }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         uint32_t a[2][4];
@@ -629,17 +736,26 @@ __global__ void __launch_bounds__(160, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    // ---- tile (or piece of tile) done: accumulators -> Cs
+    // ---- tile (or piece of tile) done: accumulators -> Cs (FP8: times the row scales)
+    float rsc[2][2] = {{1.f, 1.f}, {1.f, 1.f}};
+    if constexpr (F8) {
+      const int ntl = t % g.n_tiles;
+#pragma unroll
+      for (int ms = 0; ms < 2; ++ms)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          rsc[ms][h] = tile_row_scale(g, ntl, warp * 32 + ms * 16 + g8 + 8 * h);
+    }
 #pragma unroll
     for (int ms = 0; ms < 2; ++ms)
 #pragma unroll
       for (int j = 0; j < NB; ++j) {
         int wr = warp * 32 + ms * 16 + g8;
         int ar = j * 8 + 2 * t4;
-        Cs[ar * C::PITCH + wr] = acc[ms][j][0];
-        Cs[(ar + 1) * C::PITCH + wr] = acc[ms][j][1];
-        Cs[ar * C::PITCH + wr + 8] = acc[ms][j][2];
-        Cs[(ar + 1) * C::PITCH + wr + 8] = acc[ms][j][3];
+        Cs[ar * C::PITCH + wr] = acc[ms][j][0] * rsc[ms][0];
+        Cs[(ar + 1) * C::PITCH + wr] = acc[ms][j][1] * rsc[ms][0];
+        Cs[ar * C::PITCH + wr + 8] = acc[ms][j][2] * rsc[ms][1];
+        Cs[(ar + 1) * C::PITCH + wr + 8] = acc[ms][j][3] * rsc[ms][1];
       }
     consumer_sync();
     const bool whole = (ks0 == 0) && (seg_end == tile_end);
@@ -672,8 +788,8 @@ __global__ void __launch_bounds__(160, 1)
         if (tid == 0) {
           tile_contributors(g.units, grid, g.ks, t, cslot);
           const unsigned long long t0 = global_ns();
-          while (ld_acquire_gpu(published) < nc - 1) {
-            if (global_ns() - t0 > kWaitNs) {
+          while (ld_acquire_gpu(published) < nc - 1 + g.wait_extra) {
+            if (global_ns() - t0 > g.wait_ns) {
               raise_error(e.err, DFLASH_DEV_TIMEOUT);
               break;
             }

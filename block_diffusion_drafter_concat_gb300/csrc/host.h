@@ -6,6 +6,8 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "attention.cuh"
 #include "gemm.cuh"
 
@@ -48,16 +50,29 @@ dflash_status set_smem(K kern, int bytes) {
   return DFLASH_OK;
 }
 
-template <int BN, int EPI>
+// cudaFuncSetAttribute applies to the current device only: `done` remembers, per kernel,
+// the devices (bit = ordinal, below 64) it has been set on; higher ordinals set it on
+// every launch.
+template <typename K>
+dflash_status set_smem_once(K kern, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(DFLASH_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return DFLASH_OK;
+  DFLASH_TRY(set_smem(kern, bytes));
+  done.fetch_or(bit, std::memory_order_acq_rel);
+  return DFLASH_OK;
+}
+
+template <int BN, int EPI, bool F8 = false>
 dflash_status launch_tc(const CUtensorMap& tmA, const WMaps& wm, const GemmShape& g, int grid,
                         const EpiArgs<bf16>& e, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    DFLASH_TRY(set_smem(k_gemm_tc<BN, EPI>, TcCfg<BN>::SMEM));
-    attr_set = true;
-  }
-  return launch(k_gemm_tc<BN, EPI>, dim3(grid), dim3(TcCfg<BN>::THREADS), TcCfg<BN>::SMEM, st,
-                tmA, wm, g, e);
+  using C = TcCfg<BN, F8>;
+  static std::atomic<unsigned long long> done{0};
+  DFLASH_TRY(set_smem_once(k_gemm_tc<BN, EPI, F8>, C::SMEM, done));
+  return launch(k_gemm_tc<BN, EPI, F8>, dim3(grid), dim3(C::THREADS), C::SMEM, st, tmA, wm, g,
+                e);
 }
 
 // tu_gemm_a.cu: BN 16 and 32; tu_gemm_b.cu: BN 64 and the fp32 kernels;
@@ -66,6 +81,10 @@ dflash_status launch_gemm_tc_lo(int bn, int epi, const CUtensorMap& tmA, const W
                                 const GemmShape& g, int grid, const EpiArgs<bf16>& e,
                                 cudaStream_t st);
 dflash_status launch_gemm_tc_hi(int bn, int epi, const CUtensorMap& tmA, const WMaps& wm,
+                                const GemmShape& g, int grid, const EpiArgs<bf16>& e,
+                                cudaStream_t st);
+// tu_gemm_f8.cu: FP8-weight instantiations, 16 and 32 activation rows per tile
+dflash_status launch_gemm_tc_f8(int bn, int epi, const CUtensorMap& tmA, const WMaps& wm,
                                 const GemmShape& g, int grid, const EpiArgs<bf16>& e,
                                 cudaStream_t st);
 // tu_gemm_c.cu: the tcgen05 kernel, 128 and 256 activation rows per tile

@@ -22,18 +22,21 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 }
 
 // y[m] = x[m] / sqrt(mean(x[m]^2) + eps) * g, one CTA per row.
-// With `ids`, x[m] is first set to the embedding row ids[m] (block embedding) and the
-// block position ctx_lens[m / S] + m % S is written to pos[m].
+// With `ids`, x[m] is first set to the embedding row ids[m] (block embedding), with
+// `rows` (and no ids) to rows[m] (input rows of a chunk of context), and in both cases
+// the position ctx_lens[m / S] + m % S is written to pos[m] and x[m] to xout.
 template <typename T, typename Tin>
 __global__ void __launch_bounds__(kRowThreads)
     k_rmsnorm(const Tin* __restrict__ xin, float* __restrict__ xout, const T* __restrict__ gain,
               T* __restrict__ y, int d, float eps, const int* __restrict__ ids,
               const T* __restrict__ embed, int vocab, const int* __restrict__ ctx_lens, int S,
-              int max_position, int* __restrict__ pos, int* err) {
+              int max_position, int* __restrict__ pos, int* err,
+              const T* __restrict__ rows = nullptr) {
   __shared__ float red[kRowThreads / 32];
   // the gains are weights (never written on the device): fetch them before the wait
   float gv[32];
-  const bool regs = (sizeof(Tin) == 4) && (d & 3) == 0 && d <= kRowThreads * 4 * 8 && !ids;
+  const bool regs = (sizeof(Tin) == 4) && (d & 3) == 0 && d <= kRowThreads * 4 * 8 && !ids &&
+                    !rows;
   if (regs) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -46,20 +49,20 @@ __global__ void __launch_bounds__(kRowThreads)
   pdl_launch_dependents();
   const int m = blockIdx.x;
   const Tin* src = xin + (long long)m * d;
-  if (ids) {
-    int id = ids[m];
+  if (ids || rows) {
+    int id = ids ? ids[m] : 0;
     const int b = m / S, i = m % S;
     const int p = ctx_lens[b] + i;
     if (threadIdx.x == 0) {
       pos[m] = p;
       if (p < 0 || p >= max_position || ctx_lens[b] < 0) raise_error(err, DFLASH_DEV_BAD_POSITION);
     }
-    if (id < 0 || id >= vocab) {
+    if (ids && (id < 0 || id >= vocab)) {
       if (threadIdx.x == 0) raise_error(err, DFLASH_DEV_BAD_INDEX);
       id = 0;
     }
     src = nullptr;
-    const T* e = embed + (long long)id * d;
+    const T* e = ids ? embed + (long long)id * d : rows + (long long)m * d;
     float ss = 0.f;
     for (int c = threadIdx.x; c < d; c += kRowThreads) {
       float v = to_f32<T>(e[c]);
@@ -141,16 +144,108 @@ static __global__ void __launch_bounds__(kRowThreads)
   if (max_logit && lane == 0) max_logit[m] = best;
 }
 
+// ------------------------------------------------------- chunk K/V into the cache
+// The K/V of a causal chunk (S rows per sequence, in the attention layout
+// [B][hkv][S][hd]) are written into the layer's cache pages at positions
+// ctx_lens[b] + i: page page_table[b][p / 16], offset p % 16.  grid (B*S), one CTA per
+// row; threads walk the row's hkv*hd K and V elements 16 bytes at a time.
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads)
+    k_chunk_kv_to_cache(const T* __restrict__ kb, const T* __restrict__ vb,
+                        const int* __restrict__ ctx_lens, const int* __restrict__ page_table,
+                        int max_pages, int num_pages, T* __restrict__ kpool,
+                        T* __restrict__ vpool, int S, int hkv, int hd, int* err) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int m = blockIdx.x, b = m / S, i = m % S;
+  const int p = ctx_lens[b] + i;
+  const int pi = p / kPage;
+  if (p < 0 || pi >= max_pages) {
+    if (threadIdx.x == 0) raise_error(err, DFLASH_DEV_BAD_INDEX);
+    return;
+  }
+  const int page = page_table[(long long)b * max_pages + pi];
+  if (page < 0 || page >= num_pages) {
+    if (threadIdx.x == 0) raise_error(err, DFLASH_DEV_BAD_INDEX);
+    return;
+  }
+  constexpr int VEC = 16 / sizeof(T);
+  const int per_head = hd / VEC;
+  for (int x = threadIdx.x; x < 2 * hkv * per_head; x += kRowThreads) {
+    const int kv = x / (hkv * per_head), rem = x % (hkv * per_head);
+    const int g = rem / per_head, c = (rem % per_head) * VEC;
+    const T* src = (kv ? vb : kb) + (((long long)b * hkv + g) * S + i) * hd + c;
+    T* dst = (kv ? vpool : kpool) + (((long long)page * hkv + g) * kPage + p % kPage) * hd + c;
+    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+  }
+}
+
+// ------------------------------------------------------------------ FP8 packing
+// One CTA per row of a bf16 [rows, cols] matrix: the smallest e with max|w| <= 448 * 2^e
+// (exact fp32 comparisons with powers of two), scale 2^e, codes e4m3(w * 2^-e) rounded
+// to nearest even (w * 2^-e is exact), zero codes in the row's padding up to ld.
+static __global__ void __launch_bounds__(kRowThreads)
+    k_pack_fp8(const bf16* __restrict__ w, int cols, uint8_t* __restrict__ codes, int ld,
+               float* __restrict__ scales) {
+  __shared__ float red[kRowThreads / 32];
+  __shared__ int se;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int r = blockIdx.x;
+  const bf16* row = w + (long long)r * cols;
+  float amax = 0.f;
+  for (int c = threadIdx.x; c < cols; c += kRowThreads) amax = fmaxf(amax, fabsf(to_f32<bf16>(row[c])));
+  amax = warp_max(amax);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = amax;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a = red[0];
+    for (int k = 1; k < kRowThreads / 32; ++k) a = fmaxf(a, red[k]);
+    int e = 0;
+    if (a > 0.f) {
+      e = ilogbf(a) - 8;                            // 448 = 1.75 * 2^8
+      while (a > ldexpf(448.f, e)) ++e;
+      while (a <= ldexpf(448.f, e - 1)) --e;
+    }
+    se = e;
+    scales[r] = ldexpf(1.f, e);
+  }
+  __syncthreads();
+  const int e = se;
+  uint8_t* out = codes + (long long)r * ld;
+  for (int c = threadIdx.x; c < ld; c += kRowThreads)
+    out[c] = c < cols ? static_cast<uint8_t>(__nv_cvt_float_to_fp8(ldexpf(to_f32<bf16>(row[c]), -e),
+                                                                    __NV_SATFINITE, __NV_E4M3))
+                      : 0;
+}
+
+// ------------------------------------------------------------------ layer taps
+// out[m, col0 + c] = x[m, c] (fp32 residual stream -> storage dtype) for c < d: the
+// hidden state after one layer, stored as one column block of a feature row.
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads)
+    k_tap(const float* __restrict__ x, int d, T* __restrict__ out, int ld_out, int col0) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int m = blockIdx.x;
+  for (int c = threadIdx.x; c < d; c += kRowThreads)
+    out[(long long)m * ld_out + col0 + c] = from_f32<T>(x[(long long)m * d + c]);
+}
+
 // ------------------------------------------------------------------ greedy verify
 // grid (chunks, B*S).  Each CTA takes the argmax (lowest index) of one vocab chunk of
 // one target row; the last CTA of a sequence reduces the chunks, walks the block and
-// writes the accepted prefix plus the bonus token.
+// writes the accepted prefix plus the bonus token.  `shift` = 0: row i verifies draft
+// slot i (every slot drafted); 1: row i verifies slot i + 1 (slot 0 holds the anchor
+// token, whose target row scores the first draft), so at most S - 1 are accepted.
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads)
     k_verify_greedy(const T* __restrict__ logits, const int* __restrict__ draft, int S, int V,
                     int chunk, float* __restrict__ part_v, int* __restrict__ part_i,
                     int* __restrict__ counters, int* __restrict__ out_tokens,
-                    int* __restrict__ n_acc, int* __restrict__ n_emit, int* err) {
+                    int* __restrict__ n_acc, int* __restrict__ n_emit, int* err,
+                    int shift) {
   __shared__ float sv[kRowThreads / 32];
   __shared__ int si[kRowThreads / 32];
   __shared__ int flag;
@@ -213,8 +308,8 @@ __global__ void __launch_bounds__(kRowThreads)
   __syncthreads();
   if (threadIdx.x == 0) {
     int n = 0;
-    while (n < S) {
-      int dft = draft[(long long)b * S + n];
+    while (n < S - shift) {
+      int dft = draft[(long long)b * S + shift + n];
       if (dft < 0 || dft >= V) { raise_error(err, DFLASH_DEV_BAD_INDEX); break; }
       if (dft != tok[n]) break;
       ++n;
@@ -532,6 +627,93 @@ __global__ void __launch_bounds__(kRowThreads)
   if (my_last >= 0) atomicMax(&lastnz, my_last);
   __syncthreads();
   if (threadIdx.x == 0) out_tokens[r] = found != 0x7fffffff ? found : lastnz;
+}
+
+// ------------------------------------------------------------- speculative loop
+// Target input of the block: the anchor (slot 0 of block_ids) then drafts 1..S-1.
+static __global__ void k_spec_target_ids(const int* __restrict__ block_ids,
+                                         const int* __restrict__ draft, int M, int S,
+                                         int* __restrict__ ids) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int m = blockIdx.x * blockDim.x + threadIdx.x;
+  if (m < M) ids[m] = (m % S == 0) ? block_ids[m] : draft[m];
+}
+
+// Synthetic agreement of the target with the drafter (a stand-in for a trained pair):
+// row i < S-1 of sequence b gets logit[draft[b, i+1]] = max of the row + 1 when
+// u[(step mod u_steps), b, i] < p.  grid (B*S), one CTA per row.
+static __global__ void __launch_bounds__(kRowThreads)
+    k_spec_plant(float* __restrict__ logits, const int* __restrict__ draft,
+                 const float* __restrict__ u, int u_steps, const int* __restrict__ step,
+                 float p, int S, int V, int M, int* err) {
+  __shared__ float red[kRowThreads / 32];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int m = blockIdx.x, i = m % S;
+  if (i == S - 1) return;
+  const int st = (*step) % u_steps;
+  if (!(u[(long long)st * M + m] < p)) return;
+  const int d = draft[m + 1];
+  if (d < 0 || d >= V) {
+    if (threadIdx.x == 0) raise_error(err, DFLASH_DEV_BAD_INDEX);
+    return;
+  }
+  float* row = logits + (long long)m * V;
+  float mx = -INFINITY;
+  for (int v = threadIdx.x; v < V; v += kRowThreads) mx = fmaxf(mx, row[v]);
+  mx = warp_max(mx);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = red[0];
+    for (int w = 1; w < kRowThreads / 32; ++w) t = fmaxf(t, red[w]);
+    row[d] = t + 1.0f;
+  }
+}
+
+// Commit of one verified block per sequence (one thread per sequence): the drafter's
+// injection positions and cache slots of the block's S rows (from the old context
+// length), the emitted tokens appended to `generated`, the next block's ids (the last
+// emitted token as the anchor, then mask ids) and the new context length; thread 0 of
+// CTA 0 advances the step counter.
+static __global__ void k_spec_commit(const int* __restrict__ out_tokens,
+                                     const int* __restrict__ n_emit, int B, int S, int mask_id,
+                                     int* __restrict__ block_ids, int* __restrict__ ctx_lens,
+                                     const int* __restrict__ page_table, int max_pages,
+                                     int* __restrict__ positions, int* __restrict__ slots,
+                                     int* __restrict__ generated, int max_new,
+                                     int* __restrict__ n_generated, int* __restrict__ step,
+                                     int* err) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b == 0 && step) *step += 1;
+  if (b >= B) return;
+  const int ctx = ctx_lens[b];
+  for (int i = 0; i < S; ++i) {
+    const int p = ctx + i, pi = p / kPage;
+    int page = 0;
+    if (p < 0 || pi >= max_pages || (page = page_table[(long long)b * max_pages + pi]) < 0) {
+      raise_error(err, DFLASH_DEV_BAD_INDEX);
+      page = 0;
+    }
+    positions[b * S + i] = p;
+    slots[b * S + i] = page * kPage + p % kPage;
+  }
+  const int ne = n_emit[b];
+  if (ne < 1 || ne > S) {   // verification did not finish (its error is already set)
+    raise_error(err, DFLASH_DEV_BAD_INDEX);
+    return;
+  }
+  const int g0 = n_generated[b];
+  for (int i = 0; i < ne; ++i)
+    if (g0 + i < max_new) generated[(long long)b * max_new + g0 + i] = out_tokens[b * S + i];
+  n_generated[b] = min(max_new, g0 + ne);
+  block_ids[b * S] = out_tokens[b * S + ne - 1];
+  for (int i = 1; i < S; ++i) block_ids[b * S + i] = mask_id;
+  ctx_lens[b] = ctx + ne;
 }
 
 }  // namespace dflash

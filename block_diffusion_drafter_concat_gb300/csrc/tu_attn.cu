@@ -6,11 +6,8 @@ namespace dflash {
 template <int HD, int NW>
 static dflash_status one(dim3 grid, int smem, const AttnMaps& mp, const AttnArgs<bf16>& a,
                          cudaStream_t st) {
-  static bool set = false;
-  if (!set) {
-    DFLASH_TRY(set_smem(k_attn_tc<HD, NW>, smem));
-    set = true;
-  }
+  static std::atomic<unsigned long long> done{0};
+  DFLASH_TRY(set_smem_once(k_attn_tc<HD, NW>, smem, done));
   return launch(k_attn_tc<HD, NW>, grid, dim3((NW + 1) * 32), smem, st, mp, a);
 }
 
@@ -35,11 +32,8 @@ dflash_status launch_attn_tc(int hd, int nw, dim3 grid, int smem, const AttnMaps
 }
 
 dflash_status launch_attn_f32(dim3 grid, int smem, const AttnArgs<float>& a, cudaStream_t st) {
-  static bool set = false;
-  if (!set) {
-    DFLASH_TRY(set_smem(k_attn_f32, 160 * 1024));
-    set = true;
-  }
+  static std::atomic<unsigned long long> done{0};
+  DFLASH_TRY(set_smem_once(k_attn_f32, 160 * 1024, done));
   return launch(k_attn_f32, grid, dim3(128), smem, st, a);
 }
 

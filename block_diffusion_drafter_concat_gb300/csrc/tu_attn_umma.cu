@@ -8,11 +8,8 @@ namespace dflash {
 template <int HD, bool KSPLIT>
 static dflash_status one(dim3 grid, const AuMaps& mp, const AttnArgs<bf16>& a, cudaStream_t st) {
   using C = AuCfg<HD, KSPLIT>;
-  static bool set = false;
-  if (!set) {
-    DFLASH_TRY(set_smem(k_attn_umma<HD, KSPLIT>, C::SMEM));
-    set = true;
-  }
+  static std::atomic<unsigned long long> done{0};
+  DFLASH_TRY(set_smem_once(k_attn_umma<HD, KSPLIT>, C::SMEM, done));
   return launch(k_attn_umma<HD, KSPLIT>, grid, dim3(C::THREADS), C::SMEM, st, mp, a);
 }
 

@@ -8,11 +8,8 @@ namespace dflash {
 template <int BN, int EPI>
 static dflash_status launch_um(const CUtensorMap& tmA, const WMaps& wm, const GemmShape& g,
                                int grid, const EpiArgs<bf16>& e, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    DFLASH_TRY(set_smem(k_gemm_umma<BN, EPI>, UmCfg<BN>::SMEM));
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> done{0};
+  DFLASH_TRY(set_smem_once(k_gemm_umma<BN, EPI>, UmCfg<BN>::SMEM, done));
   return launch(k_gemm_umma<BN, EPI>, dim3(grid), dim3(UmCfg<BN>::THREADS), UmCfg<BN>::SMEM, st,
                 tmA, wm, g, e);
 }

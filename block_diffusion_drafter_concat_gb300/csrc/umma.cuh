@@ -616,8 +616,8 @@ __global__ void __launch_bounds__(192, 1)
           if (et == 0) {
             tile_contributors(g.units, grid, g.ks, t, cslot);
             const unsigned long long t0 = global_ns();
-            while (ld_acquire_gpu(published) < ncontrib - 1) {
-              if (global_ns() - t0 > kWaitNs) {
+            while (ld_acquire_gpu(published) < ncontrib - 1 + g.wait_extra) {
+              if (global_ns() - t0 > g.wait_ns) {
                 raise_error(e.err, DFLASH_DEV_TIMEOUT);
                 break;
               }

@@ -13,7 +13,8 @@ import dataclasses
 import os
 from dataclasses import dataclass
 
-# rank r's sequences come from their own seed, so no two replicas draft the same batch
+# rank r's sequences come from their own stream seed, so no two replicas draft the same
+# batch; the weights (the workload's seed) are the same on every rank
 SEED_STRIDE = 7919
 
 
@@ -39,10 +40,11 @@ def from_env(env=None) -> Replica:
 
 
 def shard(workload, rank: int):
-    """The workload rank `rank` runs: same shapes, its own batch of sequences."""
+    """The workload rank `rank` runs: the same shapes and weights, its own batch of
+    sequences (context features, lengths, verify logits and uniforms)."""
     if rank == 0:
         return workload
-    return dataclasses.replace(workload, seed=workload.seed + SEED_STRIDE * rank)
+    return dataclasses.replace(workload, seq_seed=workload.sseed + SEED_STRIDE * rank)
 
 
 def barrier(rep: Replica) -> None:

@@ -34,7 +34,13 @@ def drafter_config(w: Workload) -> dict:
 
 
 class StepRunner:
-    def __init__(self, w: Workload, device="cuda", prefill=True, weights=None):
+    """variant "kv": the DFlash step (context features injected into every layer's K/V);
+    "input": the input-fusion variant (the S new context rows run through the layer
+    stack as input, dflash_inject_inputs, before the block is drafted)."""
+
+    def __init__(self, w: Workload, device="cuda", prefill=True, weights=None, variant="kv"):
+        assert variant in ("kv", "input")
+        self.variant = variant
         self.w = w
         self.device = device
         self.dt = inputs.torch_dtype(w)
@@ -61,6 +67,7 @@ class StepRunner:
                                                    device) for b in range(B)])
         self.block_ids = inputs.block_ids(w).to(device)
         self.ctx_lens = self.lens.to(torch.int32).to(device)
+        self.ctx_before = (self.lens - S).to(torch.int32).to(device)
         M, d = w.rows, w.d_model
         self.fused = torch.empty(M, d, dtype=self.dt, device=device)
         self.hidden = torch.empty(M, d, dtype=self.dt, device=device)
@@ -81,6 +88,8 @@ class StepRunner:
     def prefill(self):
         """Injects context positions [0, T_b - S) of every sequence (untimed setup)."""
         w = self.w
+        if self.variant == "input":
+            return self._prefill_inputs()
         for b in range(w.batch):
             t = int(self.lens[b]) - w.block_size
             for p0 in range(0, t, PREFILL_CHUNK):
@@ -91,6 +100,21 @@ class StepRunner:
                 self.drafter.inject_kv(p.to(torch.int32).to(self.device),
                                        s.to(torch.int32).to(self.device), self.cache, self.ws,
                                        x_cat=x)
+
+    def _prefill_inputs(self):
+        """Input fusion: the context runs through the layer stack in causal chunks of S
+        rows (identical to one causal pass).  Chunk c0 puts sequence b at position
+        min(c0, T_b - S): a sequence whose context is done recomputes its last chunk
+        (the same values), so no row leaves its pages."""
+        w, S = self.w, self.w.block_size
+        lens = [int(t) for t in self.lens]
+        x = torch.empty(w.rows, w.fuse_in, dtype=self.dt, device=self.device)
+        for c0 in range(0, max(lens) - S, S):
+            starts = [min(c0, t - S) for t in lens]
+            for b, p0 in enumerate(starts):
+                x[b * S:(b + 1) * S] = inputs.ctx_hidden(w, b, p0, p0 + S, self.device)
+            ctx = torch.tensor(starts, dtype=torch.int32, device=self.device)
+            self.drafter.inject_inputs(x, ctx, self.page_table, self.cache, self.ws)
 
     def plant(self, drafts, mask=None):
         """Regenerates the verify logits and plants agreement with `drafts` [B, S]."""
@@ -103,8 +127,12 @@ class StepRunner:
     def step(self):
         w, d = self.w, self.drafter
         n = 0
-        d.inject_kv(self.positions, self.slots, self.cache, self.ws, x_cat=self.x_step,
-                    fused_out=self.fused)
+        if self.variant == "input":
+            d.inject_inputs(self.x_step, self.ctx_before, self.page_table, self.cache, self.ws,
+                            fused_out=self.fused)
+        else:
+            d.inject_kv(self.positions, self.slots, self.cache, self.ws, x_cat=self.x_step,
+                        fused_out=self.fused)
         n += last_launch_count()
         d.draft_block(self.block_ids, self.ctx_lens, self.page_table, self.cache, self.hidden,
                       self.ws)
@@ -122,6 +150,43 @@ class StepRunner:
                             self.ws)
         n += last_launch_count()
         self.launches = n
+
+    def timed_calls(self, reps=3):
+        """Median device time (us) of each library call of an eager step, each timed
+        alone between CUDA events on the current stream."""
+        w, d = self.w, self.drafter
+        sample = w.temperature > 0
+        tau = w.temperature if sample else 1.0
+        calls = {
+            "inject": (lambda: d.inject_inputs(self.x_step, self.ctx_before, self.page_table,
+                                               self.cache, self.ws, fused_out=self.fused))
+                      if self.variant == "input" else
+                      (lambda: d.inject_kv(self.positions, self.slots, self.cache, self.ws,
+                                           x_cat=self.x_step, fused_out=self.fused)),
+            "draft_block": lambda: d.draft_block(self.block_ids, self.ctx_lens, self.page_table,
+                                                 self.cache, self.hidden, self.ws),
+            "lm_head_argmax": lambda: d.lm_head_argmax(self.hidden, self.draft.view(-1), self.ws,
+                                                       self.dmax, self.dlse if sample else None,
+                                                       tau),
+            "verify": (lambda: d.verify_sample(self.draft, self.hidden, self.dmax, self.dlse,
+                                               self.logits, self.uniforms, tau, self.out_tokens,
+                                               self.n_acc, self.n_emit, self.ws)) if sample else
+                      (lambda: d.verify_greedy(self.draft, self.logits, self.out_tokens,
+                                               self.n_acc, self.n_emit, self.ws)),
+        }
+        st = torch.cuda.current_stream()
+        out = {}
+        for name, fn in calls.items():
+            ts = []
+            for _ in range(reps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(st)
+                fn()
+                b.record(st)
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b) * 1e3)
+            out[name] = sorted(ts)[len(ts) // 2]
+        return out
 
     def capture(self):
         """Records step() into a CUDA graph (after one eager warm-up step)."""
@@ -180,3 +245,41 @@ def lm_head_bytes(w: Workload) -> int:
     the per-row token, max and log-sum-exp outputs."""
     e = 2 if w.dtype == "bf16" else 4
     return e * (w.vocab * w.d_model + w.rows * w.d_model) + w.rows * 12
+
+
+def main(argv=None):
+    """Runs a few eager steps of a named workload (the command that the ncu captures in
+    the profile summaries run):
+
+        python -m block_diffusion_drafter_concat_gb300.runner --workload NAME
+               [--layers N] [--steps K]
+    """
+    import argparse
+    import dataclasses
+
+    from workload import configs
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="qwen3-8b-shaped-b1")
+    ap.add_argument("--layers", type=int, default=0, help="drafter layers (0 = the workload's)")
+    ap.add_argument("--steps", type=int, default=3)
+    a = ap.parse_args(argv)
+    w = configs.BY_NAME[a.workload]
+    if a.layers:
+        w = dataclasses.replace(w, n_layers=a.layers)
+    r = StepRunner(w)
+    for _ in range(a.steps):
+        r.step()
+    torch.cuda.synchronize()
+    err = r.drafter.device_error()
+    print(f"{w.name} layers={w.n_layers}: {a.steps} steps, {r.launches} launches per step, "
+          f"device error {err}")
+    if err:
+        raise SystemExit(1)
+
+
+if __name__ == "__main__":
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    main()

@@ -35,6 +35,8 @@
  *     of range, a position past the RoPE table, a bounded wait that ran out) set the
  *     handle's error word, the kernel that found them returns early, and outputs of
  *     that call are unspecified; read and clear the word with dflash_get_device_error.
+ *   - A handle belongs to the device that was current at dflash_create; every call on
+ *     it must be made with that device current (EINVAL otherwise).
  *   - No call throws; the message of the last failing call on this thread is
  *     available from dflash_last_error().
  *   - KV cache: per drafter layer, one K pool and one V pool, each
@@ -70,6 +72,14 @@ typedef enum dflash_status {
 
 typedef enum dflash_dtype { DFLASH_F32 = 0, DFLASH_BF16 = 1 } dflash_dtype;
 
+/* Storage of the projection weights (fusion, Q/K/V/O, gate/up/down, LM head; the
+ * embedding and the norm gains stay in the dtype).  NATIVE: the config dtype.  FP8:
+ * packed FP8 E4M3 matrices (dflash_pack_fp8), bf16 configs only; their projections
+ * run on the weight-streaming kernel, whose tiles take at most 32 activation rows
+ * (larger row counts run as several such tiles). */
+typedef enum dflash_weight_format { DFLASH_WEIGHTS_NATIVE = 0, DFLASH_WEIGHTS_FP8 = 1 }
+    dflash_weight_format;
+
 /* Device error codes (the first error of a call wins). */
 enum {
   DFLASH_DEV_OK = 0,
@@ -89,11 +99,14 @@ typedef struct dflash_config {
   int32_t block_size, n_target_layers, target_width, page_size, max_position;
   float rope_theta, rms_eps;
   int32_t dtype; /* dflash_dtype of weights, activations, KV cache and target logits */
+  int32_t weight_format; /* dflash_weight_format of the projection weights             */
 } dflash_config;
 
 /* Borrowed device weights ([out, in] matrices, [d] RMSNorm gains).  Per-layer members
- * are host arrays of n_layers device pointers; the handle copies those arrays. */
+ * are host arrays of n_layers device pointers; the handle copies those arrays.  With
+ * weight_format FP8 the projection matrices are packed FP8 buffers (dflash_pack_fp8). */
 typedef struct dflash_weights {
+  /* both NULL: a handle without fusion (a plain transformer, e.g. a target model) */
   const void* w_fuse;   /* [d, n_target_layers*target_width]  feature fusion        */
   const void* g_fuse;   /* [d]                                 fusion RMSNorm gain   */
   const void* const* g_attn;  /* [d]              pre-attention RMSNorm gain       */
@@ -125,7 +138,8 @@ DFLASH_API dflash_status dflash_destroy(dflash_handle h);
 
 /* Workspace bytes for calls with at most max_rows rows (dflash_fuse_features /
  * dflash_inject_kv: n; dflash_draft_block / dflash_lm_head_argmax: batch*block_size),
- * at most max_batch sequences and page tables at most max_pages wide. */
+ * at most max_batch sequences (dflash_draft_block, dflash_inject_inputs,
+ * dflash_target_forward, verification) and page tables at most max_pages wide. */
 DFLASH_API dflash_status dflash_workspace_size(dflash_handle h, int32_t max_rows, int32_t max_batch,
                                     int32_t max_pages, size_t* bytes);
 
@@ -167,6 +181,113 @@ DFLASH_API dflash_status dflash_draft_block(dflash_handle h, const int32_t* bloc
                                  void* const* k_pool, void* const* v_pool,
                                  void* final_hidden, void* ws, size_t ws_bytes,
                                  void* stream);
+
+/* [DFlash FAQ 1 (opensource-hub.com/ko/library/z-lab-dflash): the input-fusion
+ * ablation, where the fused hidden features are the drafter's input rather than being
+ * injected into every layer's K/V; the FAQ attributes KV injection's shorter draft
+ * prefill to the context skipping that full per-token processing]
+ * Input-fusion counterpart of dflash_inject_kv for `batch` sequences of block_size new
+ * context rows each: x_cat [batch*block_size, n_target_layers*target_width] (row b*S+i
+ * = token ctx_lens[b] + i of sequence b) is fused as in dflash_fuse_features, and the
+ * fused rows are then the layer-0 input of the drafter's layer stack: each layer takes
+ * RMSNorm, Q/K/V + RoPE at positions ctx_lens[b] + i, causal attention over [the
+ * sequence's ctx_lens[b] cached tokens ; the new rows 0..i], output projection +
+ * residual, RMSNorm, SwiGLU MLP + residual, and writes its K/V of the new rows into its
+ * cache at those positions (the last layer stops after its K/V).  ctx_lens are the
+ * tokens already in the cache (the caller advances them by block_size afterwards);
+ * page_table / num_pages / pools as in dflash_draft_block, with pages allocated up to
+ * position ctx_lens[b] + block_size - 1.  fused_out [batch*block_size, d] (optional)
+ * receives the fused rows.  A context of any length is prefilled chunk by chunk
+ * (causal attention makes that identical to one pass; a ragged last chunk may carry
+ * padding rows, whose cache entries lie past the context and are overwritten later). */
+DFLASH_API dflash_status dflash_inject_inputs(dflash_handle h, const void* x_cat,
+                                   const int32_t* ctx_lens, const int32_t* page_table,
+                                   int32_t max_pages, int32_t batch, int32_t num_pages,
+                                   void* const* k_pool, void* const* v_pool, void* fused_out,
+                                   void* ws, size_t ws_bytes, void* stream);
+
+/* [DFlash wiki, 사용법: spec_generate(..., target=target); NVIDIA blog, how it works:
+ * the target verifies the drafted block in one parallel pass]  The target side of the
+ * speculative loop, for a handle created without fusion weights (w_fuse = g_fuse =
+ * NULL: a plain transformer with the same layer structure).  One causal pass over
+ * block_size tokens per sequence: ids [batch, block_size] at positions ctx_lens[b] + i,
+ * each layer attending causally over [the ctx_lens[b] cached tokens ; tokens 0..i] and
+ * writing its K/V of the tokens into its cache at those positions.  taps [batch*S,
+ * n_taps*d] (optional): column block t = the residual stream after layer tap_layers[t]
+ * (1-based, host array), rounded to the config dtype -- the multi-layer hidden features
+ * the drafter fuses.  logits [batch*S, vocab] fp32 (optional): the final RMSNorm and LM
+ * head of every token. */
+DFLASH_API dflash_status dflash_target_forward(dflash_handle h, const int32_t* ids,
+                                   const int32_t* ctx_lens, const int32_t* page_table,
+                                   int32_t max_pages, int32_t batch, int32_t num_pages,
+                                   void* const* k_pool, void* const* v_pool,
+                                   const int32_t* tap_layers, int32_t n_taps, void* taps,
+                                   float* logits, void* ws, size_t ws_bytes, void* stream);
+
+/* State of the greedy speculative loop (device pointers unless marked host).  Both
+ * caches hold the tokens before each sequence's anchor (ctx_lens[b] of them) and share
+ * one page table, whose pages must reach position ctx_lens[b] + block_size - 1 at every
+ * step. */
+typedef struct dflash_spec_state {
+  int32_t batch;
+  int32_t* block_ids;          /* [batch, S]: the anchor (last emitted token) in slot 0,
+                                  mask_id after it; rewritten by every step            */
+  int32_t* ctx_lens;           /* [batch]: tokens in both caches; advanced by each step */
+  const int32_t* page_table;   /* [batch, max_pages] (both caches)                      */
+  int32_t max_pages, num_pages;
+  void* const* d_k_pool;       /* host array [drafter n_layers] of drafter K pools      */
+  void* const* d_v_pool;
+  void* const* t_k_pool;       /* host array [target n_layers] of target K pools        */
+  void* const* t_v_pool;
+  const int32_t* tap_layers;   /* host [drafter n_target_layers]: the target layers
+                                  (1-based) whose outputs the drafter fuses, in order   */
+  int32_t mask_id;
+  int32_t* generated;          /* [batch, max_new]: emitted tokens, appended            */
+  int32_t max_new;
+  int32_t* n_generated;        /* [batch]: tokens in `generated` (stops at max_new)     */
+  int32_t* n_emitted;          /* [batch]: tokens the last step emitted (1..S)          */
+  int32_t* drafts;             /* [batch, S] or NULL: the last step's drafted tokens    */
+  int32_t* step;               /* [1]: step counter, advanced by every step             */
+  const float* plant_u;        /* [plant_steps, batch, S] or NULL: see dflash_spec_step */
+  int32_t plant_steps;
+  float plant_p;
+} dflash_spec_state;
+
+/* Workspace of dflash_spec_step for `batch` sequences and page tables max_pages wide;
+ * zero its control words once with dflash_spec_workspace_init before the first step
+ * (and again after a step that set a device error). */
+DFLASH_API dflash_status dflash_spec_workspace_size(dflash_handle drafter, dflash_handle target,
+                                         int32_t batch, int32_t max_pages, size_t* bytes);
+DFLASH_API dflash_status dflash_spec_workspace_init(dflash_handle drafter, dflash_handle target,
+                                         int32_t batch, int32_t max_pages, void* ws,
+                                         size_t ws_bytes, void* stream);
+
+/* [DFlash wiki, 사용법: spec_generate; NVIDIA blog, "How does DFlash speculative
+ * decoding work?": draft a block in one pass, verify it with the target in one pass,
+ * accept the longest valid prefix]  One step of greedy speculative decoding, entirely
+ * on the device (no host synchronisation, so a CUDA graph can hold it):
+ *   1. the drafter drafts the block [anchor, mask, ...] at positions ctx_lens[b] + i
+ *      over its cache (dflash_draft_block) and takes the LM-head argmax d_0..d_{S-1};
+ *   2. the target (a handle without fusion weights, d_model = the drafter's
+ *      target_width, same vocab, block_size and dtype) runs causally over [anchor,
+ *      d_1, ..., d_{S-1}] (dflash_target_forward): its cache, the tap features of the
+ *      block's tokens and fp32 logits;
+ *   3. with plant_u given, a synthetic stand-in for a trained drafter/target pair: row
+ *      i < S-1 of the target logits gets logit[d_{i+1}] = row max + 1 when
+ *      plant_u[step mod plant_steps, b, i] < plant_p;
+ *   4. t_i = argmax of target row i (lowest index); n = leading i < S-1 with
+ *      d_{i+1} = t_i; the step emits t_0..t_n (n accepted drafts and the target's
+ *      token) into `generated`, n_emitted[b] = n + 1;
+ *   5. the block's tap features are fused and injected into the drafter's cache at
+ *      positions ctx_lens[b] + i (rows past the accepted ones are overwritten later),
+ *      the anchor becomes t_n and ctx_lens[b] advances by n + 1.
+ * The emitted tokens are exactly the target's own greedy continuation (without
+ * planting).  Before the first step: both caches hold the context (prompt tokens but
+ * the last, e.g. by dflash_target_forward and dflash_inject_kv of its taps), the
+ * anchor is the prompt's last token and the workspace is initialised. */
+DFLASH_API dflash_status dflash_spec_step(dflash_handle drafter, dflash_handle target,
+                                          const dflash_spec_state* s, void* ws,
+                                          size_t ws_bytes, void* stream);
 
 /* [DFlash wiki: the drafter reuses the target's LM head] per row r of hidden
  * [rows, d]: tokens[r] = argmax_v (hidden W_lm^T)[r, v], lowest index among equal
@@ -221,6 +342,29 @@ DFLASH_API dflash_status dflash_verify_greedy_static(dflash_handle h, const int3
                                                      const void* target_logits, int32_t batch,
                                                      int32_t* out_tokens, int32_t* n_accepted,
                                                      int32_t* n_emitted, void* stream);
+
+/* [NVIDIA blog, Blackwell Ultra paragraph: low-precision tensor formats] Packed FP8
+ * form of a weight matrix [rows, cols] ([out, in]): e4m3 codes, row stride
+ * round_up(cols, 16) bytes, then at the next 256-byte boundary rows fp32 scales.  Row
+ * n's scale is the power of two s_n = 2^e, e the smallest integer with
+ * max_k |w[n,k]| <= 448 * 2^e (1 for an all-zero row), and its codes are
+ * e4m3(w[n,k] / s_n) rounded to nearest, ties to even (the division is exact), so the
+ * matrix stands for codes * s_n.  dflash_fp8_packed_bytes gives the buffer size;
+ * dflash_pack_fp8 quantizes a bf16 device matrix w into the device buffer `packed` on
+ * the current device (enqueued on stream). */
+DFLASH_API dflash_status dflash_fp8_packed_bytes(int32_t rows, int32_t cols, size_t* bytes);
+DFLASH_API dflash_status dflash_pack_fp8(const void* w, int32_t rows, int32_t cols, void* packed,
+                                         void* stream);
+
+/* Test hook for the bounded waits (no counterpart in the pages).  With enable != 0,
+ * the CTA that finishes a projection tile split between CTAs waits for one more
+ * published piece than can ever arrive, gives up after 10 ms, raises
+ * DFLASH_DEV_TIMEOUT in the error word and goes on (no copy is abandoned and no kernel
+ * leaves early; the outputs of such calls are unspecified).  Split tiles occur in
+ * every projection whose work is cut between CTAs (batch-1 blocks always are).  After
+ * disabling it, re-initialise the workspace (dflash_workspace_init) before the next
+ * call. */
+DFLASH_API dflash_status dflash_test_force_timeout(dflash_handle h, int32_t enable);
 
 /* Synchronizes the device, returns the handle's error word in *code (DFLASH_DEV_*)
  * and zeroes it when clear != 0. */

@@ -67,3 +67,25 @@ def step_sequence(w: Workload, W, b, prefix, logits_row, u_row=None):
     else:
         out = O.verify_greedy(r["draft"], logits_row)
     return (r["draft"],) + tuple(out)
+
+
+def draft_sequence_input(w: Workload, W, b):
+    """The input-fusion variant of draft_sequence: the whole context of sequence b runs
+    through the drafter's layer stack as input (causal), then the block is drafted.
+    Returns dict(fused, K, V, h, z, draft, margin, T)."""
+    T = int(inputs.ctx_lens(w)[b])
+    x = np64(inputs.ctx_hidden(w, b, 0, T))
+    ids = inputs.block_ids(w)[b].numpy()
+    r = O.draft_step_input_fusion(x, T, ids, W, w, w.dtype == "bf16")
+    r["T"] = T
+    return r
+
+
+def loop_weights(sw):
+    """Host copies of the loop's drafter weights (with the target's embedding and LM
+    head) and target weights."""
+    tw = {k: v.float().numpy() for k, v in inputs.target_weights(sw).items()}
+    dw = {n: inputs.weight(sw.drafter, n, s, k).float().numpy()
+          for n, s, k in inputs.weight_specs(sw.drafter) if n not in ("embed", "lm_head")}
+    dw["embed"], dw["lm_head"] = tw["embed"], tw["lm_head"]
+    return dw, tw

@@ -9,52 +9,13 @@ import torch
 from oracle import run as orun
 from workload import configs, inputs
 
-from gpu_helpers import check_drafts, check_greedy, gather_kv, head_parity, rel_err, tol
+from gpu_helpers import (capped_draft_check, check_greedy, gather_kv, head_parity,
+                         rel_err, tol)
+from parity_plan import MIN_CHECKED, report
 
 pytestmark = pytest.mark.gpu
 
-SMALL = {
-    "tiny-f32": configs.TINY,
-    "small-bf16-hd128": configs.small_bf16(),
-    "small-bf16-hd64-g8": configs.small_bf16(
-        name="small-bf16-hd64-g8", d_model=384, n_q_heads=16, n_kv_heads=2, head_dim=64,
-        ffn_dim=384, vocab=2176, batch=3, ctx_range=(16, 120), seed=12),
-    # batch 1 x block 16 rows (the 16-row projection tiles), two and one context splits
-    "small-bf16-b1": configs.small_bf16(
-        name="small-bf16-b1", batch=1, ctx_range=(150, 200), seed=14),
-    "small-bf16-b1-1split": configs.small_bf16(
-        name="small-bf16-b1-1split", batch=1, ctx_range=(40, 100), seed=15),
-    "small-bf16-b5-s8": configs.small_bf16(
-        name="small-bf16-b5-s8", block_size=8, batch=5, n_q_heads=4, n_kv_heads=2,
-        ctx_range=(8, 70), vocab=1000, seed=13),
-    # 96 and 320 block rows: the tcgen05 projection tiles (128 and 256 activation rows),
-    # the second with a ragged 64-row second m-block; every tile split between CTAs
-    "small-bf16-b6-tc128": configs.small_bf16(
-        name="small-bf16-b6-tc128", batch=6, ctx_range=(20, 90), seed=16),
-    "small-bf16-b20-tc256": configs.small_bf16(
-        name="small-bf16-b20-tc256", batch=20, ctx_range=(16, 64), seed=17),
-    # head_dim 64 with 96 and 80 block rows: attention on the tcgen05 kernel with 128 and
-    # 64 query rows per kv head, ragged contexts over several splits and steps
-    "small-bf16-hd64-g8-b6-tc": configs.small_bf16(
-        name="small-bf16-hd64-g8-b6-tc", d_model=384, n_q_heads=16, n_kv_heads=2,
-        head_dim=64, ffn_dim=384, vocab=2176, batch=6, ctx_range=(16, 250), seed=19),
-    "small-bf16-hd64-g4-b5-tc": configs.small_bf16(
-        name="small-bf16-hd64-g4-b5-tc", d_model=384, n_q_heads=8, n_kv_heads=2,
-        head_dim=64, ffn_dim=384, vocab=2176, batch=5, ctx_range=(20, 180), seed=20),
-    # one-page contexts (16 tokens: the split's single step holds the context page and
-    # the block, so the tcgen05 key-split lanes of the step's second half see no valid
-    # key) with 96 block rows at head_dim 128, and a mix of one- and two-page contexts
-    # with 80 block rows at head_dim 64 (64 query rows per kv head)
-    "small-bf16-b6-tc128-short": configs.small_bf16(
-        name="small-bf16-b6-tc128-short", batch=6, ctx_range=(16, 16), seed=22),
-    "small-bf16-hd64-g4-b5-short": configs.small_bf16(
-        name="small-bf16-hd64-g4-b5-short", d_model=384, n_q_heads=8, n_kv_heads=2,
-        head_dim=64, ffn_dim=384, vocab=2176, batch=5, ctx_range=(16, 24), seed=23),
-    # 256 rows with K = 1024 and a 32000-token vocabulary: whole tiles per CTA as well
-    "mid-bf16-b16-tc256": configs.small_bf16(
-        name="mid-bf16-b16-tc256", d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128,
-        ffn_dim=2816, vocab=32000, batch=16, ctx_range=(16, 48), seed=18),
-}
+SMALL = configs.PARITY_SMALL
 
 
 @pytest.fixture(scope="module")
@@ -82,6 +43,8 @@ def test_step_matches_oracle(built, name):
     d_gpu = r.draft.cpu().numpy()
     out, nacc, nemit = r.out_tokens.cpu().numpy(), r.n_acc.cpu(), r.n_emit.cpu()
     checked = 0
+    rows_checked = rows_out = 0
+    dz_max = 0.0
     for b, s in enumerate(seqs):
         T = s["T"]
         assert rel_err(fused[b], s["fused"][T - S:T]) < t
@@ -90,11 +53,17 @@ def test_step_matches_oracle(built, name):
             assert rel_err(gather_kv(r.cache.k[l], r.table_host, b, pos), s["K"][l]) < t
             assert rel_err(gather_kv(r.cache.v[l], r.table_host, b, pos), s["V"][l]) < t
         assert rel_err(hid[b], s["h"]) < t
-        slack, _ = head_parity(d_gpu[b], hid[b], W["lm_head"], s["z"])
-        check_drafts(d_gpu[b], s["draft"], s["margin"], slack)
+        dz, _ = head_parity(d_gpu[b], hid[b], W["lm_head"], s["z"])
+        c, o = capped_draft_check(name, d_gpu[b], s["draft"], s["margin"], dz)
+        rows_checked += c
+        rows_out += o
+        dz_max = max(dz_max, float(dz.max()))
         logits_row = r.logits[b].float().cpu().numpy()
         checked += check_greedy(out[b], nacc[b], nemit[b], d_gpu[b], logits_row)
     assert checked == w.batch
+    report(name, dict(test="step", dz_max=dz_max, rows_checked=rows_checked,
+                      rows_left_out=rows_out))
+    assert rows_checked >= MIN_CHECKED * (rows_checked + rows_out)
 
 
 @pytest.mark.parametrize("name", ["small-bf16-hd128", "small-bf16-b1", "small-bf16-b20-tc256"])

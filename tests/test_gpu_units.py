@@ -206,3 +206,41 @@ def test_host_validation_statuses(small):
     with pytest.raises(pkg.DFlashError) as e:
         d.lm_head_argmax(r.hidden[:, 1:], r.draft.view(-1), r.ws)   # misaligned rows
     assert e.value.status == pkg.EINVAL
+
+
+# 32 block rows (mma.sync projections, stream-K with split tiles at these sizes) and 320
+# rows with an 80000-token vocabulary (the tcgen05 LM head's 1250 tiles are planned as
+# stream-K ranges, which split tiles between CTAs)
+TIMEOUT_WORKLOADS = {
+    "small-bf16-hd128": configs.PARITY_SMALL["small-bf16-hd128"],
+    "timeout-tc256-v80k": configs.small_bf16(name="timeout-tc256-v80k", batch=20, vocab=80000,
+                                             ctx_range=(16, 64), seed=24),
+}
+
+
+@pytest.mark.parametrize("name", list(TIMEOUT_WORKLOADS))
+def test_forced_wait_timeout_is_reported_and_recovered(name):
+    """The bounded on-device waits: with the test hook on, every split-tile finisher
+    (mma.sync or tcgen05 projections) waits for one piece more than can arrive, gives up
+    after 10 ms and reports DFLASH_DEV_TIMEOUT instead of hanging; after the hook is off
+    and the workspace re-initialised, the next step is clean and bit-identical to one
+    made before."""
+    from block_diffusion_drafter_concat_gb300.runner import StepRunner
+    r = StepRunner(TIMEOUT_WORKLOADS[name])
+    d = r.drafter
+    r.step()
+    torch.cuda.synchronize()
+    assert d.device_error() == 0
+    h_ref, d_ref = r.hidden.clone(), r.draft.clone()
+    d.test_force_timeout(True)
+    try:
+        r.step()
+        assert d.device_error() == 3
+    finally:
+        d.test_force_timeout(False)
+    d.workspace_init(r.ws)
+    r.hidden.zero_()
+    r.step()
+    torch.cuda.synchronize()
+    assert d.device_error() == 0
+    assert torch.equal(r.hidden, h_ref) and torch.equal(r.draft, d_ref)

@@ -7,7 +7,7 @@ import pytest
 import torch.multiprocessing as mp
 
 from block_diffusion_drafter_concat_gb300 import replicas
-from workload import configs
+from workload import configs, inputs
 
 
 def _free_port():
@@ -30,8 +30,13 @@ def _rank_main(rank, world, port, out):
         slowest = replicas.max_over_ranks(rep, mine)
         value = replicas.aggregate(100, rep, slowest)
         w = replicas.shard(configs.QWEN3_8B_B1, rep.rank)
+        ws = replicas.shard(configs.small_bf16(), rep.rank)
+        wt = inputs.weights(ws)
+        digest = float(sum(t.float().sum() for t in wt.values()))
+        lens = inputs.ctx_lens(ws).tolist()
+        x0 = float(inputs.ctx_hidden(ws, 0, 0, 4).float().sum())
         replicas.barrier(rep)
-        out.put((rep.rank, slowest, value, w.seed, w.rows))
+        out.put((rep.rank, slowest, value, w.seed, w.rows, digest, lens, x0))
     finally:
         dist.destroy_process_group()
 
@@ -49,12 +54,15 @@ def test_two_gloo_ranks_agree_on_the_slowest_time():
     assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
     res = sorted(out.get(timeout=10) for _ in range(world))
     slowest = 0.5 + (world - 1)
-    for rank, t, value, seed, rows in res:
+    for rank, t, value, seed, rows, _, _, _ in res:
         assert t == pytest.approx(slowest)          # every rank sees the max, not its own
         assert value == pytest.approx(100 * world / slowest)
         assert rows == configs.QWEN3_8B_B1.rows
-    seeds = [s for _, _, _, s, _ in res]
-    assert seeds[0] == configs.QWEN3_8B_B1.seed and len(set(seeds)) == world
+        assert seed == configs.QWEN3_8B_B1.seed     # one weight seed on every rank
+    # replicas share the weights but draft different sequences
+    assert res[0][5] == res[1][5]
+    assert res[0][6] != res[1][6] and res[0][7] != res[1][7]
+    assert res[0][6] == inputs.ctx_lens(configs.small_bf16()).tolist()
 
 
 def test_single_process_needs_no_process_group():

@@ -37,6 +37,10 @@ class Workload:
     agree_p: float = 0.8         # planted draft/target agreement per position
     temperature: float = 0.0     # 0 = greedy verification
     seed: int = 0
+    # seed of the per-sequence streams (context lengths, page order, target features,
+    # verify logits, planting, uniforms); None = `seed`.  Weights always use `seed`, so
+    # replicas that change only this share the drafter's weights.
+    seq_seed: int | None = None
     mask_id: int = 0
     page_size: int = 16
     permute_pages: bool = False
@@ -44,6 +48,10 @@ class Workload:
     gain_std: float = 0.02
     hidden_std: float = 1.0
     extra: dict = field(default_factory=dict)
+
+    @property
+    def sseed(self) -> int:
+        return self.seed if self.seq_seed is None else self.seq_seed
 
     @property
     def fuse_in(self) -> int:
@@ -115,3 +123,104 @@ def small_bf16(**kw) -> Workload:
         batch=2, ctx_len=200, ctx_range=(37, 200), rope_theta=1e6, logit_std=2.0,
         agree_p=0.75, seed=11, permute_pages=True)
     return replace(base, **kw)
+
+
+# Workloads the oracle finishes in seconds that still span several projection tiles,
+# several context pages with a ragged last page, permuted pages and a ragged vocabulary
+# tail; each exercises one launch configuration of the kernels (named in its comment).
+PARITY_SMALL = {
+    "tiny-f32": TINY,
+    "small-bf16-hd128": small_bf16(),
+    "small-bf16-hd64-g8": small_bf16(
+        name="small-bf16-hd64-g8", d_model=384, n_q_heads=16, n_kv_heads=2, head_dim=64,
+        ffn_dim=384, vocab=2176, batch=3, ctx_range=(16, 120), seed=12),
+    # batch 1 x block 16 rows (the 16-row projection tiles), two and one context splits
+    "small-bf16-b1": small_bf16(
+        name="small-bf16-b1", batch=1, ctx_range=(150, 200), seed=14),
+    "small-bf16-b1-1split": small_bf16(
+        name="small-bf16-b1-1split", batch=1, ctx_range=(40, 100), seed=15),
+    "small-bf16-b5-s8": small_bf16(
+        name="small-bf16-b5-s8", block_size=8, batch=5, n_q_heads=4, n_kv_heads=2,
+        ctx_range=(8, 70), vocab=1000, seed=13),
+    # 96 and 320 block rows: the tcgen05 projection tiles (128 and 256 activation rows),
+    # the second with a ragged 64-row second m-block; every tile split between CTAs
+    "small-bf16-b6-tc128": small_bf16(
+        name="small-bf16-b6-tc128", batch=6, ctx_range=(20, 90), seed=16),
+    "small-bf16-b20-tc256": small_bf16(
+        name="small-bf16-b20-tc256", batch=20, ctx_range=(16, 64), seed=17),
+    # head_dim 64 with 96 and 80 block rows: attention on the tcgen05 kernel with 128 and
+    # 64 query rows per kv head, ragged contexts over several splits and steps
+    "small-bf16-hd64-g8-b6-tc": small_bf16(
+        name="small-bf16-hd64-g8-b6-tc", d_model=384, n_q_heads=16, n_kv_heads=2,
+        head_dim=64, ffn_dim=384, vocab=2176, batch=6, ctx_range=(16, 250), seed=19),
+    "small-bf16-hd64-g4-b5-tc": small_bf16(
+        name="small-bf16-hd64-g4-b5-tc", d_model=384, n_q_heads=8, n_kv_heads=2,
+        head_dim=64, ffn_dim=384, vocab=2176, batch=5, ctx_range=(20, 180), seed=20),
+    # one-page contexts (16 tokens: the split's single step holds the context page and
+    # the block, so the tcgen05 key-split lanes of the step's second half see no valid
+    # key) with 96 block rows at head_dim 128, and a mix of one- and two-page contexts
+    # with 80 block rows at head_dim 64 (64 query rows per kv head)
+    "small-bf16-b6-tc128-short": small_bf16(
+        name="small-bf16-b6-tc128-short", batch=6, ctx_range=(16, 16), seed=22),
+    "small-bf16-hd64-g4-b5-short": small_bf16(
+        name="small-bf16-hd64-g4-b5-short", d_model=384, n_q_heads=8, n_kv_heads=2,
+        head_dim=64, ffn_dim=384, vocab=2176, batch=5, ctx_range=(16, 24), seed=23),
+    # 256 rows with K = 1024 and a 32000-token vocabulary: whole tiles per CTA as well
+    "mid-bf16-b16-tc256": small_bf16(
+        name="mid-bf16-b16-tc256", d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128,
+        ffn_dim=2816, vocab=32000, batch=16, ctx_range=(16, 48), seed=18),
+}
+
+
+def one_layer(w: Workload) -> Workload:
+    """The same shapes with a single drafter layer (fewer compounding rounding points)."""
+    return replace(w, name=w.name + "-1l", n_layers=1)
+
+
+ONE_LAYER = {v.name: v for v in (one_layer(QWEN3_8B_B1), one_layer(LLAMA31_8B_B8),
+                                 one_layer(GPT_OSS_120B_B64))}
+
+
+@dataclass(frozen=True)
+class SpecWorkload:
+    """The greedy speculative loop: a drafter (its target_width = d_model) and a random
+    causal target transformer of the same width, heads, FFN and vocabulary with
+    `target_layers` layers; the drafter fuses the target's outputs after `tap_layers`
+    and reuses the target's embedding and LM head.  Every sequence starts from a
+    `prompt_len`-token random prompt; `plant_p` is the per-position probability of the
+    synthetic agreement that stands in for a trained drafter/target pair."""
+    name: str
+    drafter: Workload
+    target_layers: int
+    tap_layers: tuple
+    prompt_len: int
+    steps: int
+    plant_p: float
+
+    @property
+    def target(self) -> Workload:
+        return replace(self.drafter, name=self.name + "-target", n_layers=self.target_layers,
+                       seed=self.drafter.seed + 104729)
+
+    @property
+    def max_position(self) -> int:
+        # prompt, every step's block (up to S new tokens each) and one block of slack
+        return self.prompt_len + (self.steps + 2) * self.drafter.block_size
+
+
+SPEC_TINY = SpecWorkload(
+    name="spec-tiny-f32", drafter=replace(TINY, name="spec-tiny-f32-drafter", batch=2),
+    target_layers=4, tap_layers=(1, 2, 4), prompt_len=37, steps=6, plant_p=0.7)
+
+SPEC_SMALL_BF16 = SpecWorkload(
+    name="spec-small-bf16",
+    drafter=small_bf16(name="spec-small-bf16-drafter", target_width=512, batch=3, seed=31),
+    target_layers=4, tap_layers=(1, 2, 4), prompt_len=45, steps=6, plant_p=0.75)
+
+# Qwen3-8B-shaped drafter (5 layers) against a 36-layer Qwen3-8B-shaped random target:
+# five target layers spread over its depth are fused; agreement as in the batch-1 step
+SPEC_QWEN3_8B = SpecWorkload(
+    name="spec-qwen3-8b-shaped-b1", drafter=replace(QWEN3_8B_B1, name="spec-qwen3-8b-drafter"),
+    target_layers=36, tap_layers=(4, 11, 18, 25, 32), prompt_len=2048, steps=64, plant_p=0.8)
+
+SPEC = {s.name: s for s in (SPEC_TINY, SPEC_SMALL_BF16, SPEC_QWEN3_8B)}

@@ -56,7 +56,7 @@ def ctx_lens(w: Workload) -> torch.Tensor:
     if w.ctx_range is None:
         return torch.full((w.batch,), w.ctx_len, dtype=torch.int64)
     lo, hi = w.ctx_range
-    return synth.integers(w.seed, "ctx_len", (w.batch,), lo, hi)
+    return synth.integers(w.sseed, "ctx_len", (w.batch,), lo, hi)
 
 
 def page_table(w: Workload, lens=None):
@@ -67,7 +67,7 @@ def page_table(w: Workload, lens=None):
     lens = ctx_lens(w) if lens is None else lens
     npg = [-(-int(t) // w.page_size) for t in lens]
     total = sum(npg)
-    order = synth.permutation(w.seed, "pages", total) if w.permute_pages \
+    order = synth.permutation(w.sseed, "pages", total) if w.permute_pages \
         else torch.arange(total)
     table = torch.full((w.batch, w.max_pages), -1, dtype=torch.int32)
     off = 0
@@ -90,7 +90,7 @@ def ctx_hidden(w: Workload, b, p0, p1, device="cpu"):
     [l*target_width, (l+1)*target_width)."""
     shape = (w.batch * w.max_ctx, w.fuse_in)
     r0 = b * w.max_ctx + p0
-    return synth.normal(w.seed, "x_ctx", shape, std=w.hidden_std, dtype=torch_dtype(w),
+    return synth.normal(w.sseed, "x_ctx", shape, std=w.hidden_std, dtype=torch_dtype(w),
                         device=device, rows=(r0, r0 + (p1 - p0)))
 
 
@@ -102,18 +102,18 @@ def logits_noise(w: Workload, b0=0, b1=None, device="cpu"):
     """Unplanted target verify logits of sequences [b0, b1): [b1-b0, S, V]."""
     b1 = w.batch if b1 is None else b1
     shape = (w.batch * w.block_size, w.vocab)
-    z = synth.normal(w.seed, "logits", shape, std=w.logit_std, dtype=torch_dtype(w),
+    z = synth.normal(w.sseed, "logits", shape, std=w.logit_std, dtype=torch_dtype(w),
                      device=device, rows=(b0 * w.block_size, b1 * w.block_size))
     return z.view(b1 - b0, w.block_size, w.vocab)
 
 
 def plant_mask(w: Workload):
     """[B, S] bool: positions where the target agrees with the draft."""
-    return synth.uniform(w.seed, "plant", (w.batch, w.block_size)) < w.agree_p
+    return synth.uniform(w.sseed, "plant", (w.batch, w.block_size)) < w.agree_p
 
 
 def decoy_drafts(w: Workload):
-    return synth.integers(w.seed, "decoy", (w.batch, w.block_size), 0, w.vocab - 1)
+    return synth.integers(w.sseed, "decoy", (w.batch, w.block_size), 0, w.vocab - 1)
 
 
 def plant(w: Workload, logits, drafts, mask):
@@ -132,4 +132,34 @@ def plant(w: Workload, logits, drafts, mask):
 
 def uniforms(w: Workload, device="cpu"):
     """[B, S, 2] fp32: [..., 0] acceptance test, [..., 1] residual draw."""
-    return synth.uniform(w.seed, "uniforms", (w.batch, w.block_size, 2), device=device)
+    return synth.uniform(w.sseed, "uniforms", (w.batch, w.block_size, 2), device=device)
+
+
+# ------------------------------------------------------------- speculative loop
+def target_weights(sw, device="cpu"):
+    """The loop's target: every drafter layer weight name, the final gain, embedding
+    and LM head, from the target's own seed (no fusion weights)."""
+    wt = sw.target
+    return {n: weight(wt, n, s, k, device) for n, s, k in weight_specs(wt)
+            if n not in ("w_fuse", "g_fuse")}
+
+
+def loop_drafter_weights(sw, target_w, device="cpu"):
+    """The drafter's own weights with the target's embedding and LM head (reused)."""
+    w = sw.drafter
+    out = {n: weight(w, n, s, k, device) for n, s, k in weight_specs(w)
+           if n not in ("embed", "lm_head")}
+    out["embed"], out["lm_head"] = target_w["embed"], target_w["lm_head"]
+    return out
+
+
+def prompt_tokens(sw):
+    """[B, prompt_len] int64 random prompt tokens (host)."""
+    w = sw.drafter
+    return synth.integers(w.seed, "prompt", (w.batch, sw.prompt_len), 0, w.vocab - 1)
+
+
+def loop_uniforms(sw, device="cpu"):
+    """[steps, B, S] fp32 uniforms of the planted agreement, one per verified slot."""
+    w = sw.drafter
+    return synth.uniform(w.seed, "plant_loop", (sw.steps, w.batch, w.block_size), device=device)
