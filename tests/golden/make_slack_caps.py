@@ -87,7 +87,8 @@ def sequences_of(w):
     """The sequences whose rounding sensitivity is measured: every sequence of a small
     workload; for a large one the shortest, median and longest of the sequences the GPU
     tests compare with the full oracle."""
-    if w.name in configs.PARITY_SMALL:
+    small = w.name in configs.PARITY_SMALL or w.name.removesuffix("-fp8") in configs.PARITY_SMALL
+    if small or w.batch <= N_STUDIED:
         return list(range(w.batch))
     lens = inputs.ctx_lens(w).numpy()
     sample = parity_plan.sampled_sequences(lens)
@@ -146,6 +147,7 @@ def all_workloads():
     ws.update({w.name: w for w in configs.ALL if w.name not in ws})
     ws.update(configs.ONE_LAYER)
     ws.update({INPUT + n: ws[n] for n in INPUT_FUSION})
+    ws.update(configs.FP8)
     return ws
 
 
