@@ -609,6 +609,14 @@ def run_ours(args):
                                                     args.warmup, hbm, bf16_tf)
         line["input_fusion"]["kv_injection_ms_per_step"] = ms
         line["spec_loop"] = measure_spec_loop(SPEC_QWEN3_8B, args.steps, 3)
+        from workload.configs import FP8
+        f8 = measure_config(replicas.shard(FP8[w.name + "-fp8"], rank), min(args.steps, 50),
+                            args.warmup, hbm, bf16_tf)
+        f8["note"] = ("the same step with FP8 e4m3 projection weights (per-row power-of-two "
+                      "scales; activations and the rounding points as in bf16); roofline "
+                      "on the FP8 step's own bytes")
+        f8["bf16_ms_per_step"] = ms
+        line["fp8_weights"] = f8
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tc, n = oracle_timing(w, 30.0, 3, 1)
         line["cpu_baseline"] = {

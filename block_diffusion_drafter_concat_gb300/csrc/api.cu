@@ -195,8 +195,9 @@ GemmShape plan_shape(const H* h, const WSet& w, int M, int K, bool tc, int* grid
   // stream-K: at least 4 units per CTA, and few enough CTAs per tile for the table of
   // the tile's finisher
   const long long per = std::max<long long>(4, (g.ks + 509) / 510);
+  const long long ctas = (long long)h->sms * (h->fp8 ? 2 : 1);   // FP8: two CTAs per SM
   auto streamk_grid = [&](long long units) {
-    return static_cast<int>(std::min<long long>(h->sms, (units + per - 1) / per));
+    return static_cast<int>(std::min<long long>(ctas, (units + per - 1) / per));
   };
   int bn = tc ? pick_bn(M) : kF32BN;
   if (h->fp8) bn = std::min(bn, 32);   // FP8 weights: the weight-streaming kernel only
@@ -245,7 +246,7 @@ GemmShape plan_shape(const H* h, const WSet& w, int M, int K, bool tc, int* grid
 
 // split-tile partials: two slots per CTA of tiles with up to max_rows activation rows
 size_t gemm_part_floats(const H* h, int max_rows) {
-  return (size_t)h->sms * 2 * pick_bn(std::max(1, max_rows)) * kBM;
+  return (size_t)h->sms * (h->fp8 ? 2 : 1) * 2 * pick_bn(std::max(1, max_rows)) * kBM;
 }
 
 // Runs one projection: y = A W^T over the weight segments of `w`, epilogue EPI.
@@ -697,8 +698,7 @@ static dflash_status draft_impl(H* h, const StackOpts& o, const int32_t* ctx_len
                           ks ? 64 : 128));
           TRY(launch_attn_umma(c.head_dim, ks, grid, am, a, st));
         } else {
-          const int smem = 1024 + kAttnStages * (2 * kPage * c.head_dim * 2 + 16) + 16;
-          TRY(launch_attn_tc(c.head_dim, QR / 16, grid, smem, mp, a, st));
+          TRY(launch_attn_tc(c.head_dim, QR / 16, grid, attn_tc_smem(c.head_dim), mp, a, st));
         }
       } else {
         const int smem = (2 * QR * c.head_dim + 2 * kPage * c.head_dim + QR * kPage + 3 * QR) * 4;

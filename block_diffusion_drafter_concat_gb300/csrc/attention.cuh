@@ -127,6 +127,11 @@ __device__ __forceinline__ void attn_emit(const AttnArgs<T>& a, int b, int g, in
 // ------------------------------------------------------------------ bf16 tensor core
 constexpr int kAttnStages = 8;
 
+// Shared memory of the mma.sync attention kernel: the K/V ring and its barriers.
+__host__ __device__ constexpr int attn_tc_smem(int hd) {
+  return 1024 + kAttnStages * (2 * kPage * hd * 2 + 16) + 16;
+}
+
 template <int HD>
 struct AttnCfg {
   static constexpr int NS = kAttnStages;

@@ -386,8 +386,11 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
 template <int BN, bool F8 = false>
 struct TcCfg {
   static constexpr int KS = F8 ? 2 * kBK : kBK;          // k per stage
-  static constexpr int NS = F8 ? (BN == 16 ? 9 : 7)
+  // FP8: two CTAs per SM (two consumer warps per scheduler hide the conversions'
+  // latency), so each holds a shorter ring
+  static constexpr int NS = F8 ? (BN == 16 ? 4 : 3)
                                : (BN == 16 ? 10 : BN == 32 ? 8 : BN == 64 ? 6 : 4);
+  static constexpr int CTAS_PER_SM = F8 ? 2 : 1;
   static constexpr int W_BYTES = kBM * kBK * 2;           // 16 KB either way
   static constexpr int A_BYTES = BN * KS * 2;
   static constexpr int STAGE = W_BYTES + A_BYTES;
@@ -503,10 +506,21 @@ __device__ __forceinline__ uint4 lds_u4(uint32_t addr) {
                : "r"(addr));
   return v;
 }
-// Two e4m3 codes (low byte first) as an f16 pair (exact: every e4m3 value is an f16).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// Two e4m3 codes of a 32-bit word (bytes lo and lo + 1, the lower first) as an f16 pair
+// holding value * 2^-8, by integer bit placement: the code's exponent and mantissa bits
+// (eeee mmm) become the f16's low exponent and high mantissa bits and its sign the f16
+// sign.  e4m3 (bias 7) and f16 (bias 15) both read exponent field 0 as 0.mmm at the
+// lowest normal exponent, so normal and subnormal codes alike come out as exactly
+// value * 2^-8 (the scale carries the 2^8).  No conversion-pipe instruction is used.
+// Three instructions per pair: a byte permute puts each code in the low byte of a 16-bit
+// half with its sign replicated into the high byte, a shift by 7 moves the exponent and
+// mantissa bits into place (and a replicated sign bit to bit 15 of the half), and a mask
+// keeps exactly those bits.
+template <int LO>
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t word) {
+  uint32_t t;   // halves: byte LO | sign(byte LO) x 8, byte LO + 1 | sign(byte LO + 1) x 8
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(t) : "r"(word), "n"(LO == 0 ? 0x9180 : 0xB3A2));
+  return (t << 7) & 0xBF80BF80u;
 }
 // A bf16 pair as an f16 pair (round to nearest; exact in f16's normal range).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
@@ -548,13 +562,14 @@ __device__ __forceinline__ void argmax_keys_finish(const EpiArgs<T>& e, int M, i
 }
 
 // F8 = true: the weights are FP8 e4m3 codes with per-row scales (g.wscale); the MMA
-// runs on f16 operands (e4m3 and bf16 values are exact in f16 but for bf16 values
-// below 2^-14, whose few lowest bits f16 subnormals drop).  Within every 32-k chunk the
+// runs on f16 operands: the codes as value * 2^-8 (exact, e4m3x2_to_f16x2_scaled) and
+// the bf16 activations converted to f16 (exact but for values below 2^-14, whose few
+// lowest bits f16 subnormals drop); the accumulators are scaled by 2^8 * s_n.  Within every 32-k chunk the
 // k index is permuted alike for both operands so that a lane reads 8 consecutive weight
 // bytes and 8 consecutive activations: MMA 1 takes k 8t..8t+3, MMA 2 k 8t+4..8t+7 of
 // lane group t (the contraction sums over every k once either way).
 template <int BN, int EPI, bool F8 = false>
-__global__ void __launch_bounds__(160, 1)
+__global__ void __launch_bounds__(160, F8 ? 2 : 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ WMaps wm,
               const GemmShape g, const EpiArgs<bf16> e) {
   using C = TcCfg<BN, F8>;
@@ -602,10 +617,12 @@ __global__ void __launch_bounds__(160, 1)
           tma_load_2d_hint(st, &wm.m[w.seg], &full[s], w.ks * C::KS, w.row, pol);
         }
       };
+      // activation boxes are 128 bytes wide: 64 bf16 values of k, two per FP8 stage
       auto issue_a = [&](int s, const UnitWalk& w) {
         uint8_t* at = stages + s * C::STAGE + C::W_BYTES;
-        tma_load_2d(at, &tmA, &full[s], w.ks * C::KS, w.mb * BN);
-        if constexpr (F8) tma_load_2d(at + BN * 128, &tmA, &full[s], w.ks * C::KS + kBK, w.mb * BN);
+#pragma unroll
+        for (int j = 0; j < C::KS / kBK; ++j)
+          tma_load_2d(at + j * BN * 128, &tmA, &full[s], w.ks * C::KS + j * kBK, w.mb * BN);
       };
       const int pre = min(C::NS, n_my);
       for (int i = 0; i < pre; ++i) {
@@ -686,14 +703,14 @@ __global__ void __launch_bounds__(160, 1)
             const uint32_t off = ((kc * 32 + 8 * t4) & 15);
             const uint2 w0 = lds_u2(wbase + swz128(row, kc * 2 + (t4 >> 1)) + off);
             const uint2 w1 = lds_u2(wbase + swz128(row + 8, kc * 2 + (t4 >> 1)) + off);
-            a1[ms][0] = e4m3x2_to_f16x2(w0.x & 0xffffu);
-            a1[ms][1] = e4m3x2_to_f16x2(w1.x & 0xffffu);
-            a1[ms][2] = e4m3x2_to_f16x2(w0.x >> 16);
-            a1[ms][3] = e4m3x2_to_f16x2(w1.x >> 16);
-            a2[ms][0] = e4m3x2_to_f16x2(w0.y & 0xffffu);
-            a2[ms][1] = e4m3x2_to_f16x2(w1.y & 0xffffu);
-            a2[ms][2] = e4m3x2_to_f16x2(w0.y >> 16);
-            a2[ms][3] = e4m3x2_to_f16x2(w1.y >> 16);
+            a1[ms][0] = e4m3x2_to_f16x2_scaled<0>(w0.x);
+            a1[ms][1] = e4m3x2_to_f16x2_scaled<0>(w1.x);
+            a1[ms][2] = e4m3x2_to_f16x2_scaled<2>(w0.x);
+            a1[ms][3] = e4m3x2_to_f16x2_scaled<2>(w1.x);
+            a2[ms][0] = e4m3x2_to_f16x2_scaled<0>(w0.y);
+            a2[ms][1] = e4m3x2_to_f16x2_scaled<0>(w1.y);
+            a2[ms][2] = e4m3x2_to_f16x2_scaled<2>(w0.y);
+            a2[ms][3] = e4m3x2_to_f16x2_scaled<2>(w1.y);
           }
           // activations: box kc / 2, 16-byte chunk (kc % 2) * 4 + t of row nb * 8 + g8
           const uint32_t ab = abase + (kc >> 1) * (BN * 128);
@@ -744,7 +761,7 @@ __global__ void __launch_bounds__(160, 1)
       for (int ms = 0; ms < 2; ++ms)
 #pragma unroll
         for (int h = 0; h < 2; ++h)
-          rsc[ms][h] = tile_row_scale(g, ntl, warp * 32 + ms * 16 + g8 + 8 * h);
+          rsc[ms][h] = 256.f * tile_row_scale(g, ntl, warp * 32 + ms * 16 + g8 + 8 * h);
     }
 #pragma unroll
     for (int ms = 0; ms < 2; ++ms)

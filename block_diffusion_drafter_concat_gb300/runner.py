@@ -19,9 +19,12 @@ import torch
 from workload import inputs
 from workload.configs import Workload
 
-from . import BF16, F32, Drafter, KVCache, last_launch_count
+from . import BF16, F32, Drafter, KVCache, last_launch_count, pack_fp8
 
 PREFILL_CHUNK = 4096
+
+
+FP8_MATRICES = ("w_fuse", "w_q", "w_k", "w_v", "w_o", "w_gate", "w_up", "w_down", "lm_head")
 
 
 def drafter_config(w: Workload) -> dict:
@@ -30,7 +33,15 @@ def drafter_config(w: Workload) -> dict:
                 vocab=w.vocab, block_size=w.block_size, n_target_layers=w.n_target_layers,
                 target_width=w.target_width, page_size=w.page_size,
                 max_position=w.max_position, rope_theta=w.rope_theta, rms_eps=w.rms_eps,
-                dtype=BF16 if w.dtype == "bf16" else F32)
+                dtype=BF16 if w.dtype == "bf16" else F32,
+                weight_format=1 if w.weight_format == "fp8" else 0)
+
+
+def packed_weights(weights: dict) -> dict:
+    """Projection matrices replaced by their packed FP8 form (dflash_pack_fp8, on the
+    device); embedding and gains unchanged."""
+    return {n: pack_fp8(t) if n.split(".")[-1] in FP8_MATRICES else t
+            for n, t in weights.items()}
 
 
 class StepRunner:
@@ -46,6 +57,8 @@ class StepRunner:
         self.dt = inputs.torch_dtype(w)
         S, B = w.block_size, w.batch
         self.weights = weights if weights is not None else inputs.weights(w, device)
+        if w.weight_format == "fp8":
+            self.weights = packed_weights(self.weights)
         self.drafter = Drafter(drafter_config(w), self.weights)
         self.lens = inputs.ctx_lens(w)
         assert int(self.lens.min()) >= S, "each context must hold at least one block"
@@ -209,12 +222,17 @@ class StepRunner:
 # ---------------------------------------------------------------------- roofline model
 def weight_bytes(w: Workload) -> int:
     """Bytes of every weight one step streams once (the embedding contributes only the
-    block's rows)."""
+    block's rows).  FP8 projection matrices: one byte per element plus a 4-byte scale
+    per row."""
     e = 2 if w.dtype == "bf16" else 4
     d, F = w.d_model, w.ffn_dim
-    per_layer = (w.q_width * d + 2 * w.kv_width * d + d * w.q_width + 3 * F * d + 2 * d)
-    return e * (d * w.fuse_in + d + w.n_layers * per_layer + d + w.vocab * d
-                + w.rows * d)
+    mats = [(d, w.fuse_in)] + w.n_layers * [(w.q_width, d), (w.kv_width, d), (w.kv_width, d),
+                                            (d, w.q_width), (F, d), (F, d), (d, F)] + [(w.vocab, d)]
+    if w.weight_format == "fp8":
+        proj = sum(r * c + 4 * r for r, c in mats)
+    else:
+        proj = e * sum(r * c for r, c in mats)
+    return proj + e * (d + w.n_layers * 2 * d + d + w.rows * d)
 
 
 def step_bytes(w: Workload, lens=None) -> int:
@@ -264,7 +282,7 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=0, help="drafter layers (0 = the workload's)")
     ap.add_argument("--steps", type=int, default=3)
     a = ap.parse_args(argv)
-    w = configs.BY_NAME[a.workload]
+    w = configs.named(a.workload)
     if a.layers:
         w = dataclasses.replace(w, n_layers=a.layers)
     r = StepRunner(w)

@@ -21,8 +21,10 @@ def np64(t):
 
 def host_weights(w: Workload):
     """All drafter weights as fp32 numpy arrays (exact copies of the bf16/fp32 values;
-    numpy promotes them to fp64 inside every product)."""
-    return {n: inputs.weight(w, n, s, k).float().numpy() for n, s, k in inputs.weight_specs(w)}
+    numpy promotes them to fp64 inside every product).  For FP8 workloads the projection
+    matrices are the oracle's own dequantized FP8 form of those values."""
+    W = {n: inputs.weight(w, n, s, k).float().numpy() for n, s, k in inputs.weight_specs(w)}
+    return O.fp8_weights(W) if w.weight_format == "fp8" else W
 
 
 def context(w: Workload, W, b, p0, p1):

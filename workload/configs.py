@@ -42,6 +42,8 @@ class Workload:
     # replicas that change only this share the drafter's weights.
     seq_seed: int | None = None
     mask_id: int = 0
+    # projection weights: "native" (the dtype) or "fp8" (packed e4m3 with row scales)
+    weight_format: str = "native"
     page_size: int = 16
     permute_pages: bool = False
     weight_std: float = 0.02
@@ -224,3 +226,25 @@ SPEC_QWEN3_8B = SpecWorkload(
     target_layers=36, tap_layers=(4, 11, 18, 25, 32), prompt_len=2048, steps=64, plant_p=0.8)
 
 SPEC = {s.name: s for s in (SPEC_TINY, SPEC_SMALL_BF16, SPEC_QWEN3_8B)}
+
+
+def fp8(w: Workload, name=None) -> Workload:
+    """The same workload with its projection weights streamed as FP8 (e4m3, per-row
+    power-of-two scales)."""
+    return replace(w, name=(name or w.name) + "-fp8", weight_format="fp8")
+
+
+# FP8 weight streaming: 16-row blocks (batch 1), 32 rows (two blocks), 320 rows (many
+# 32-row tiles of the weight-streaming kernel), and the Qwen3-8B-shaped batch-1 step
+FP8 = {v.name: v for v in [fp8(PARITY_SMALL[k], k) for k in
+                           ("small-bf16-b1", "small-bf16-hd128", "small-bf16-b20-tc256")]
+       + [fp8(QWEN3_8B_B1)]}
+
+
+def named(name: str) -> Workload:
+    """Any workload defined here, by name (step workloads, parity workloads, one-layer
+    and FP8 variants)."""
+    for table in (BY_NAME, PARITY_SMALL, ONE_LAYER, FP8):
+        if name in table:
+            return table[name]
+    raise KeyError(name)
