@@ -240,6 +240,7 @@ def measure_config(w, steps, warmup, hbm, bf16_tf):
     from block_diffusion_drafter_concat_gb300.runner import (StepRunner, lm_head_bytes,
                                                             step_bytes, step_flops)
     r = StepRunner(w)
+    r.keep_fused = False
     r.step()
     torch.cuda.synchronize()
     r.plant(r.draft.cpu())
@@ -422,6 +423,7 @@ def run_ours(args):
 
     w = BY_NAME[args.config]
     r = StepRunner(replicas.shard(w, rank))
+    r.keep_fused = False   # the fused rows are an optional output the step does not need
     # one eager step, then plant the verify logits' agreement with this step's drafts
     r.step()
     torch.cuda.synchronize()

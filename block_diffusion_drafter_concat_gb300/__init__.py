@@ -22,7 +22,7 @@ DEV_ERRORS = {0: "ok", 1: "index out of range", 2: "position out of range", 3: "
 
 API = ["dflash_create", "dflash_destroy", "dflash_workspace_size", "dflash_workspace_init",
        "dflash_fuse_features", "dflash_inject_kv", "dflash_draft_block",
-       "dflash_inject_inputs", "dflash_target_forward", "dflash_spec_workspace_size",
+       "dflash_inject_draft", "dflash_inject_inputs", "dflash_target_forward", "dflash_spec_workspace_size",
        "dflash_spec_workspace_init", "dflash_spec_step",
        "dflash_lm_head_argmax", "dflash_verify_greedy", "dflash_verify_sample",
        "dflash_verify_greedy_static", "dflash_test_force_timeout", "dflash_fp8_packed_bytes",
@@ -87,6 +87,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "dflash_inject_kv": [P, P, P, i32, P, P, i32, PP, PP, P, P, sz, P],
         "dflash_draft_block": [P, P, P, P, i32, i32, i32, PP, PP, P, P, sz, P],
         "dflash_inject_inputs": [P, P, P, P, i32, i32, i32, PP, PP, P, P, sz, P],
+        "dflash_inject_draft": [P, P, i32, P, P, P, P, P, i32, i32, i32, PP, PP, P, P, P, sz, P],
         "dflash_spec_workspace_size": [P, P, i32, i32, ctypes.POINTER(sz)],
         "dflash_spec_workspace_init": [P, P, i32, i32, P, sz, P],
         "dflash_spec_step": [P, P, ctypes.POINTER(SpecState), P, sz, P],
@@ -239,6 +240,15 @@ class Drafter:
         _check(self.lib.dflash_draft_block(
             self.h, _ptr(block_ids), _ptr(ctx_lens), _ptr(page_table), page_table.shape[1],
             block_ids.shape[0], cache.num_pages, cache._kp, cache._vp, _ptr(final_hidden),
+            _ptr(ws), ws.numel(), _stream()))
+        return final_hidden
+
+    def inject_draft(self, x_cat, positions, slots, block_ids, ctx_lens, page_table,
+                     cache: KVCache, final_hidden, ws, fused_out=None):
+        _check(self.lib.dflash_inject_draft(
+            self.h, _ptr(x_cat), x_cat.shape[0], _ptr(positions), _ptr(slots), _ptr(block_ids),
+            _ptr(ctx_lens), _ptr(page_table), page_table.shape[1], block_ids.shape[0],
+            cache.num_pages, cache._kp, cache._vp, _ptr(fused_out), _ptr(final_hidden),
             _ptr(ws), ws.numel(), _stream()))
         return final_hidden
 

@@ -363,6 +363,9 @@ AttnPlan plan_attn(const H* h, int B, int max_pages, bool causal = false) {
 }
 
 // ------------------------------------------------------------------ workspace plans
+// rows of a block plus new context rows that one weight-streaming tile takes
+constexpr int kInjRows = 64;
+
 struct DraftWs {
   int* ctl;
   float* x;
@@ -370,6 +373,7 @@ struct DraftWs {
   int* pos;
   void *q, *kb, *vb, *o, *act;
   float *part_o, *part_ml, *gpart;
+  float* u;   // fusion projection of merged-injection rows (fp32)
 };
 
 size_t elt(const H* h) { return h->bf16 ? 2 : 4; }
@@ -384,7 +388,9 @@ DraftWs carve_draft(const H* h, Carve& cv, int B, int max_pages) {
   DraftWs w;
   w.ctl = cv.take<int>(kCtlWords);
   w.x = cv.take<float>(M * c.d_model);
-  w.n = cv.take<char>(M * c.d_model * elt(h));
+  // normed rows, then room for up to kInjRows fused context rows that a merged
+  // injection appends to the Q/K/V projection's activations
+  w.n = cv.take<char>((M + kInjRows) * c.d_model * elt(h));
   w.pos = cv.take<int>(M);
   w.q = cv.take<char>(M * c.n_q_heads * c.head_dim * elt(h));
   w.kb = cv.take<char>((M + 16) * c.n_kv_heads * c.head_dim * elt(h));
@@ -393,7 +399,8 @@ DraftWs carve_draft(const H* h, Carve& cv, int B, int max_pages) {
   w.act = cv.take<char>(M * c.ffn_dim * elt(h));
   w.part_o = cv.take<float>((size_t)B * c.n_kv_heads * ap.nsplit * QR * c.head_dim);
   w.part_ml = cv.take<float>((size_t)B * c.n_kv_heads * ap.nsplit * QR * 2);
-  w.gpart = cv.take<float>(gemm_part_floats(h, static_cast<int>(M)));
+  w.gpart = cv.take<float>(gemm_part_floats(h, std::max(static_cast<int>(M), kInjRows)));
+  w.u = cv.take<float>((size_t)kInjRows * c.d_model);
   return w;
 }
 
@@ -609,6 +616,11 @@ struct StackOpts {
   int n_taps = 0;
   void* taps = nullptr;           // [B*S, n_taps*d]
   void* final_hidden = nullptr;   // [B*S, d] final RMSNorm output, or nullptr
+  // merged injection: n_inj fused context rows (in the workspace after the block's
+  // normed rows) whose K/V every layer's Q/K/V projection writes to the cache
+  int n_inj = 0;
+  const int32_t* inj_pos = nullptr;
+  const int32_t* inj_slots = nullptr;
 };
 
 template <typename T>
@@ -647,7 +659,15 @@ static dflash_status draft_impl(H* h, const StackOpts& o, const int32_t* ctx_len
       e.kb = static_cast<T*>(w.kb);
       e.vb = static_cast<T*>(w.vb);
       e.err = h->d_err;
-      TRY((gemm<EPI_QKV, T>(h, n, M, d, ws_, e, w.gpart, w.ctl, st)));
+      if (o.n_inj) {   // + the new context rows: K/V into this layer's pages
+        e.n_inj = o.n_inj;
+        e.inj_pos = o.inj_pos;
+        e.inj_slots = o.inj_slots;
+        e.inj_kpool = static_cast<T*>(k_pool[l]);
+        e.inj_vpool = static_cast<T*>(v_pool[l]);
+        e.num_slots = (long long)num_pages * kPage;
+      }
+      TRY((gemm<EPI_QKV, T>(h, n, M + o.n_inj, d, ws_, e, w.gpart, w.ctl, st)));
     }
     if (o.write_cache)
       TRY(launch(k_chunk_kv_to_cache<T>, dim3(M), dim3(kRowThreads), 0, st,
@@ -678,6 +698,7 @@ static dflash_status draft_impl(H* h, const StackOpts& o, const int32_t* ctx_len
       a.out = static_cast<T*>(w.o);
       a.err = h->d_err;
       a.causal = o.causal ? 1 : 0;
+      a.fresh = o.n_inj;   // the injected rows are the sequences' newest positions
       dim3 grid(ap.nsplit, c.n_kv_heads, B);
       if constexpr (std::is_same<T, bf16>::value) {
         AttnMaps mp;
@@ -1030,6 +1051,30 @@ dflash_status dflash_inject_kv(dflash_handle h, const void* x_cat, const void* f
   return inject_impl(h, f, n, positions, slots, num_pages, k_pool, v_pool, w, st);
 }
 
+}  // extern "C"
+
+namespace {
+// Host checks shared by the calls that run the layer stack over S rows per sequence.
+dflash_status check_stack_args(const H* h, const int32_t* ctx_lens, const int32_t* page_table,
+                               int32_t max_pages, int32_t batch, int32_t num_pages,
+                               void* const* k_pool, void* const* v_pool) {
+  if (batch < 0 || max_pages < 0 || num_pages <= 0) return fail(DFLASH_EINVAL, "bad sizes");
+  NEED(ctx_lens, "ctx_lens");
+  if (max_pages > 0) NEED(page_table, "page_table");
+  if (!k_pool || !v_pool) return fail(DFLASH_EINVAL, "pool arrays are NULL");
+  for (int l = 0; l < h->c.n_layers; ++l) {
+    NEED(k_pool[l], "k_pool[l]");
+    NEED(v_pool[l], "v_pool[l]");
+  }
+  if ((long long)batch * h->c.block_size > (1 << 20) ||
+      (long long)batch * h->c.n_kv_heads > 2 * kTileWords)
+    return fail(DFLASH_EUNSUPPORTED, "batch too large");
+  return DFLASH_OK;
+}
+}  // namespace
+
+extern "C" {
+
 dflash_status dflash_draft_block(dflash_handle h, const int32_t* block_ids,
                                  const int32_t* ctx_lens, const int32_t* page_table,
                                  int32_t max_pages, int32_t batch, int32_t num_pages,
@@ -1064,29 +1109,60 @@ dflash_status dflash_draft_block(dflash_handle h, const int32_t* block_ids,
                            v_pool, w, st);
 }
 
-}  // extern "C"
-
-namespace {
-// Host checks shared by the calls that run the layer stack over S rows per sequence.
-dflash_status check_stack_args(const H* h, const int32_t* ctx_lens, const int32_t* page_table,
-                               int32_t max_pages, int32_t batch, int32_t num_pages,
-                               void* const* k_pool, void* const* v_pool) {
-  if (batch < 0 || max_pages < 0 || num_pages <= 0) return fail(DFLASH_EINVAL, "bad sizes");
-  NEED(ctx_lens, "ctx_lens");
-  if (max_pages > 0) NEED(page_table, "page_table");
-  if (!k_pool || !v_pool) return fail(DFLASH_EINVAL, "pool arrays are NULL");
-  for (int l = 0; l < h->c.n_layers; ++l) {
-    NEED(k_pool[l], "k_pool[l]");
-    NEED(v_pool[l], "v_pool[l]");
+dflash_status dflash_inject_draft(dflash_handle h, const void* x_cat, int32_t n_inj,
+                                  const int32_t* positions, const int32_t* slots,
+                                  const int32_t* block_ids, const int32_t* ctx_lens,
+                                  const int32_t* page_table, int32_t max_pages, int32_t batch,
+                                  int32_t num_pages, void* const* k_pool, void* const* v_pool,
+                                  void* fused_out, void* final_hidden, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  g_launches = 0;
+  CHECK_HANDLE(h);
+  const auto& c = h->c;
+  const long long M = (long long)batch * c.block_size;
+  // one weight-streaming tile holds the block and the new rows, and the attention is
+  // the mma.sync kernel (which fetches the fresh pages after its wait)
+  const bool merged = h->bf16 && batch > 0 && n_inj > 0 && M + n_inj <= kInjRows &&
+                      !use_attn_umma(c, static_cast<int>(M));
+  if (!merged) {
+    int total = 0;
+    TRY(dflash_inject_kv(h, x_cat, nullptr, n_inj, positions, slots, num_pages, k_pool, v_pool,
+                         fused_out, ws, ws_bytes, stream));
+    total += g_launches;
+    TRY(dflash_draft_block(h, block_ids, ctx_lens, page_table, max_pages, batch, num_pages,
+                           k_pool, v_pool, final_hidden, ws, ws_bytes, stream));
+    g_launches += total;
+    return DFLASH_OK;
   }
-  if ((long long)batch * h->c.block_size > (1 << 20) ||
-      (long long)batch * h->c.n_kv_heads > 2 * kTileWords)
-    return fail(DFLASH_EUNSUPPORTED, "batch too large");
-  return DFLASH_OK;
+  if (!h->w_fuse) return fail(DFLASH_EINVAL, "the handle has no fusion weights");
+  NEED(x_cat, "x_cat");
+  NEED(positions, "positions");
+  NEED(slots, "slots");
+  NEED(block_ids, "block_ids");
+  NEED(final_hidden, "final_hidden");
+  if (fused_out) NEED(fused_out, "fused_out");
+  TRY(check_stack_args(h, ctx_lens, page_table, max_pages, batch, num_pages, k_pool, v_pool));
+  Carve cv{static_cast<char*>(ws)};
+  DraftWs w = carve_draft(h, cv, batch, max_pages);
+  TRY(check_ws(ws, ws_bytes, cv.off));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // fused rows straight after the block's normed rows: the Q/K/V projections read both
+  char* rows = static_cast<char*>(w.n) + (size_t)M * c.d_model * elt(h);
+  TRY(fuse_impl(h, x_cat, n_inj, rows, w.u, w.gpart, w.ctl, st));
+  if (fused_out)
+    CUDA_TRY(cudaMemcpyAsync(fused_out, rows, (size_t)n_inj * c.d_model * elt(h),
+                             cudaMemcpyDeviceToDevice, st));
+  StackOpts o;
+  o.ids = block_ids;
+  o.final_hidden = final_hidden;
+  o.n_inj = n_inj;
+  o.inj_pos = positions;
+  o.inj_slots = slots;
+  return draft_impl<bf16>(h, o, ctx_lens, page_table, max_pages, batch, num_pages, k_pool,
+                          v_pool, w, st);
 }
-}  // namespace
 
-extern "C" {
+
 
 dflash_status dflash_inject_inputs(dflash_handle h, const void* x_cat, const int32_t* ctx_lens,
                                    const int32_t* page_table, int32_t max_pages, int32_t batch,

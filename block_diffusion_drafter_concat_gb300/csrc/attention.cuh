@@ -42,6 +42,10 @@ struct AttnArgs {
   // (block slot r / G) sees block keys 0..r / G only (a causal chunk of new context or
   // target tokens)
   int causal;
+  // the newest `fresh` context positions of every sequence were written by the
+  // predecessor kernel (context rows injected by the Q/K/V projection): their pages are
+  // fetched after the wait, not before (0: every context page predates it)
+  int fresh;
 };
 
 // Tensor maps of the tcgen05 attention kernel: q as [B*hkv*QR, hd] with 128-row boxes,
@@ -166,6 +170,10 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   if (split >= ns) return;                  // this split is past the sequence's keys
   const int p0 = split * a.pps, p1 = min(kp, p0 + a.pps);
   const int nmy = p1 - p0;
+  // stages fetched before the wait: context pages that predate the predecessor, within
+  // the first ring
+  const int fresh_pg = a.fresh > 0 ? max(0, T - a.fresh) / kPage : np;
+  const int pre = max(0, min(C::NS, min(np, fresh_pg) - p0));
 
   if (tid == 0) {
     for (int s = 0; s < C::NS; ++s) {
@@ -189,8 +197,9 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       for (int j = 0; j < cnt; ++j) {
         const int page_j = __shfl_sync(0xffffffffu, my_page, j);
         const int i = base + j;
-        // the block's own keys, and stages beyond the first ring, follow the wait
-        if (i == min(C::NS, np - p0)) pdl_wait();
+        // the block's own keys, fresh pages, and stages beyond the first ring follow
+        // the wait
+        if (i == pre) pdl_wait();
         if (lane == 0 && ok) {
           const int s = i % C::NS;
           if (i >= C::NS && !mbar_wait(&empty[s], ((i / C::NS) - 1) & 1)) {

@@ -69,6 +69,14 @@ struct EpiArgs {
   int* am_done;
   int* tok_out;
   float* max_out;
+  // EPI_QKV: the last n_inj of the M rows are new context rows (fused target features):
+  // their K (RoPE at inj_pos) and V go to the layer's cache pages at inj_slots, their Q
+  // is not stored
+  int n_inj;
+  const int* inj_pos;
+  const int* inj_slots;
+  T* inj_kpool;
+  T* inj_vpool;
   int* err;
 };
 
@@ -195,27 +203,41 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
           rbase[q] = -1;
           if (r >= mr) continue;
           const int m = m0 + r;
+          int slot = -1;
+          bool pool = EPI == EPI_KV;
           if constexpr (EPI == EPI_QKV) {
-            const int b = m / e.S, ii = m - (m / e.S) * e.S;
-            rbase[q] = ((long long)b * e.hkv * e.S + ii) * hd;   // + head * S * hd
+            if (m >= e.M - e.n_inj) {
+              pool = true;
+              slot = e.inj_slots[m - (e.M - e.n_inj)];
+            }
           } else {
-            const int slot = e.slots[m];
+            slot = e.slots[m];
+          }
+          if (pool) {
             if (slot < 0 || slot >= e.num_slots) { raise_error(e.err, DFLASH_DEV_BAD_INDEX); continue; }
             rbase[q] = ((long long)(slot / kPage) * e.hkv * kPage + slot % kPage) * hd;  // + head*16*hd
+            if constexpr (EPI == EPI_QKV) rbase[q] |= 1LL << 62;   // marks a cache row
+          } else {
+            const int b = m / e.S, ii = m - (m / e.S) * e.S;
+            rbase[q] = ((long long)b * e.hkv * e.S + ii) * hd;   // + head * S * hd
           }
         }
 #pragma unroll
         for (int q = 0; q < RB; ++q) {
           const int r = rb + q * nw;
           if (r >= mr || rbase[q] < 0) continue;
+          const bool to_pool = EPI == EPI_KV || (rbase[q] >> 62) != 0;
+          const long long base = rbase[q] & ((1LL << 62) - 1);
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             if (hv[k] >= e.hkv) continue;
             const float2 v = *reinterpret_cast<const float2*>(Cs + r * pitch + 2 * lane + 64 * k);
-            if constexpr (EPI == EPI_QKV) {
-              store_pair<T>(e.vb + rbase[q] + (long long)hv[k] * e.S * hd + jv[k], v.x, v.y);
+            if (to_pool) {
+              T* vp;
+              if constexpr (EPI == EPI_QKV) vp = e.inj_vpool; else vp = e.vpool[layer];
+              store_pair<T>(vp + base + (long long)hv[k] * kPage * hd + jv[k], v.x, v.y);
             } else {
-              store_pair<T>(e.vpool[layer] + rbase[q] + (long long)hv[k] * kPage * hd + jv[k], v.x, v.y);
+              store_pair<T>(e.vb + base + (long long)hv[k] * e.S * hd + jv[k], v.x, v.y);
             }
           }
         }
@@ -241,14 +263,27 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
       for (int rb = warp; rb < mr; rb += nw * RR) {
         int my_p = -1;
         long long my_base = 0;
+        int my_inj = 0;
         if (lane < RR) {
           const int r = rb + lane * nw;
           if (r < mr) {
             const int m = m0 + r;
-            const int p = e.pos[m];
+            const bool inj = EPI == EPI_QKV && m >= e.M - e.n_inj;   // a new context row
+            const int p = inj ? e.inj_pos[m - (e.M - e.n_inj)] : e.pos[m];
             bool ok = p >= 0 && p < e.max_pos;
             if (!ok) raise_error(e.err, DFLASH_DEV_BAD_POSITION);
-            if constexpr (EPI == EPI_QKV) {
+            if (inj) {
+              const int slot = e.inj_slots[m - (e.M - e.n_inj)];
+              if (kind == 0) {
+                ok = false;                                   // its Q is not needed
+              } else if (slot < 0 || slot >= e.num_slots) {
+                raise_error(e.err, DFLASH_DEV_BAD_INDEX);
+                ok = false;
+              } else {
+                my_base = ((long long)(slot / kPage) * e.hkv * kPage + slot % kPage) * hd;
+                my_inj = 1;
+              }
+            } else if constexpr (EPI == EPI_QKV) {
               const int b = m / e.S, ii = m - (m / e.S) * e.S;
               my_base = kind == 0 ? (((long long)b * e.hkv * e.S + ii) * G) * hd   // + (gk*S*G + hh)*hd
                                   : ((long long)b * e.hkv * e.S + ii) * hd;        // + head*S*hd
@@ -264,12 +299,13 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
             if (ok) my_p = p;
           }
         }
-        int pv[RR];
+        int pv[RR], injv[RR];
         long long rbase[RR];
 #pragma unroll
         for (int q = 0; q < RR; ++q) {
           pv[q] = __shfl_sync(0xffffffffu, my_p, q);
           rbase[q] = __shfl_sync(0xffffffffu, my_base, q);
+          injv[q] = __shfl_sync(0xffffffffu, my_inj, q);
         }
         float2 cs[RR][2];
 #pragma unroll
@@ -285,8 +321,9 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
               cs[q][k] = pv[q] >= 0 ? e.rope[(long long)pv[q] * half + jv[k]] : make_float2(0.f, 0.f);
           }
         }
-        auto dst_of = [&](int head, long long base) -> T* {
+        auto dst_of = [&](int head, long long base, int to_cache) -> T* {
           if constexpr (EPI == EPI_QKV) {
+            if (to_cache) return e.inj_kpool + base + (long long)head * kPage * hd;
             if (kind == 0) {
               const int gk = head / G, hh = head - gk * G;
               return e.q + base + ((long long)gk * e.S * G + hh) * hd;
@@ -309,14 +346,14 @@ __device__ void tile_epilogue(const float* Cs, int pitch, int BN, int m0, int nt
           }
           if (adj) {
             if (hv[0] >= nheads) continue;   // both indices belong to head hv[0]
-            T* dst = dst_of(hv[0], rbase[q]);
+            T* dst = dst_of(hv[0], rbase[q], injv[q]);
             store_pair<T>(dst + jv[0], y0[0], y0[1]);
             store_pair<T>(dst + jv[0] + half, y1[0], y1[1]);
           } else {
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
               if (hv[k] >= nheads) continue;
-              T* dst = dst_of(hv[k], rbase[q]);
+              T* dst = dst_of(hv[k], rbase[q], injv[q]);
               dst[jv[k]] = from_f32<T>(y0[k]);
               dst[jv[k] + half] = from_f32<T>(y1[k]);
             }

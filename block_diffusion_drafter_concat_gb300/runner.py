@@ -5,8 +5,8 @@ shape, the paged KV cache, the page table, the per-step inputs (the S newest tar
 hidden features of every sequence and the target's verify logits) and the outputs.
 ``step()`` enqueues the whole path as libdflash calls on the current stream:
 
-  dflash_inject_kv (fuse + inject the S new context rows of every sequence)
-  -> dflash_draft_block -> dflash_lm_head_argmax
+  dflash_inject_draft (fuse + inject the S new context rows of every sequence, then the
+  drafter's block pass)  -> dflash_lm_head_argmax
   -> dflash_verify_greedy, or dflash_verify_sample at temperature > 0.
 
 ``capture()`` records that sequence into a CUDA graph.  Inputs come from the seeded
@@ -94,6 +94,8 @@ class StepRunner:
         self.uniforms = inputs.uniforms(w, device=device)
         self.launches = 0
         self.graph = None
+        # copy the fused step rows out (parity tests read them; the benchmark does not)
+        self.keep_fused = True
         if prefill:
             self.prefill()
 
@@ -143,12 +145,15 @@ class StepRunner:
         if self.variant == "input":
             d.inject_inputs(self.x_step, self.ctx_before, self.page_table, self.cache, self.ws,
                             fused_out=self.fused)
+            n += last_launch_count()
+            d.draft_block(self.block_ids, self.ctx_lens, self.page_table, self.cache,
+                          self.hidden, self.ws)
         else:
-            d.inject_kv(self.positions, self.slots, self.cache, self.ws, x_cat=self.x_step,
-                        fused_out=self.fused)
-        n += last_launch_count()
-        d.draft_block(self.block_ids, self.ctx_lens, self.page_table, self.cache, self.hidden,
-                      self.ws)
+            # injection and draft in one call (W_k / W_v read once where the rows fit one
+            # weight-streaming tile)
+            d.inject_draft(self.x_step, self.positions, self.slots, self.block_ids,
+                           self.ctx_lens, self.page_table, self.cache, self.hidden, self.ws,
+                           fused_out=self.fused if self.keep_fused else None)
         n += last_launch_count()
         sample = w.temperature > 0
         tau = w.temperature if sample else 1.0
@@ -178,6 +183,10 @@ class StepRunner:
                                            x_cat=self.x_step, fused_out=self.fused)),
             "draft_block": lambda: d.draft_block(self.block_ids, self.ctx_lens, self.page_table,
                                                  self.cache, self.hidden, self.ws),
+            "inject_draft": lambda: d.inject_draft(self.x_step, self.positions, self.slots,
+                                                   self.block_ids, self.ctx_lens,
+                                                   self.page_table, self.cache, self.hidden,
+                                                   self.ws),
             "lm_head_argmax": lambda: d.lm_head_argmax(self.hidden, self.draft.view(-1), self.ws,
                                                        self.dmax, self.dlse if sample else None,
                                                        tau),

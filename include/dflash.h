@@ -182,6 +182,25 @@ DFLASH_API dflash_status dflash_draft_block(dflash_handle h, const int32_t* bloc
                                  void* final_hidden, void* ws, size_t ws_bytes,
                                  void* stream);
 
+/* [DFlash wiki, item 2; NVIDIA blog, how it works: the injected K/V come from the same
+ * key-value projections as the block's own]  dflash_inject_kv of n_inj new context rows
+ * (x_cat, positions, slots as there) followed by dflash_draft_block, in one call: the
+ * same results.  When the block's rows plus the new rows fit one weight-streaming tile
+ * (bf16, batch * block_size + n_inj <= 64) every layer's W_k and W_v are read once:
+ * that layer's Q/K/V projection runs over [the block's normed rows ; the fused new
+ * rows] and writes the new rows' K (RoPE) and V into the cache, and the attention
+ * fetches the pages of the newest n_inj positions of each sequence only after those
+ * writes (the new rows must be each sequence's newest context positions).  Otherwise
+ * the two calls run one after the other.  fused_out (optional) as in
+ * dflash_inject_kv. */
+DFLASH_API dflash_status dflash_inject_draft(dflash_handle h, const void* x_cat, int32_t n_inj,
+                                  const int32_t* positions, const int32_t* slots,
+                                  const int32_t* block_ids, const int32_t* ctx_lens,
+                                  const int32_t* page_table, int32_t max_pages, int32_t batch,
+                                  int32_t num_pages, void* const* k_pool, void* const* v_pool,
+                                  void* fused_out, void* final_hidden, void* ws, size_t ws_bytes,
+                                  void* stream);
+
 /* [DFlash FAQ 1 (opensource-hub.com/ko/library/z-lab-dflash): the input-fusion
  * ablation, where the fused hidden features are the drafter's input rather than being
  * injected into every layer's K/V; the FAQ attributes KV injection's shorter draft
