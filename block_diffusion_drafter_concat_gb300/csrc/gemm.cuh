@@ -11,8 +11,9 @@
 // Work is split "stream-K" style: the (m-block, n-tile, k-stage) units are cut into
 // one contiguous range per persistent CTA, so every SM streams the same number of
 // weight bytes whatever the shape.  A tile cut between CTAs is finished by the last
-// contributor to arrive, which sums the published partial tiles in contributor order
-// (deterministic) and runs the epilogue.  Weight boxes of the first stages are issued
+// contributor to count itself in, which sums the published partial tiles in contributor
+// order (deterministic) and runs the epilogue; each contributor publishes its piece
+// before it counts, so the finisher never waits.  Weight boxes of the first stages are issued
 // before griddepcontrol.wait, overlapping the previous kernel's tail.
 #pragma once
 
@@ -89,9 +90,9 @@ struct GemmShape {
   int seg_rows[kMaxSeg];  // rows of each weight matrix
   float* part;      // [grid][2][BN * kBM] partial tiles (split pieces)
   int* counters;    // one per output tile
-  // the finisher of a split tile waits for (contributors - 1 + wait_extra) publications
-  // for at most wait_ns: wait_extra is 0 except under the forced-timeout test hook,
-  // which asks for one publication more than can arrive
+  // wait_extra is 0 except under the forced-timeout test hook, which makes the finisher
+  // of a split tile wait, for at most wait_ns, for one count more than can arrive (the
+  // tcgen05 kernel's finisher waits for contributors - 1 + wait_extra publications)
   int wait_extra;
   unsigned long long wait_ns;
   // FP8 weights (k_gemm_tc<..., true>): per-segment row scales, applied to each
@@ -445,6 +446,14 @@ __device__ __forceinline__ void red_release_add(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Counting in after publishing: release orders this CTA's earlier writes (after a CTA
+// barrier) before the add, acquire makes the other counted CTAs' writes visible.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -790,112 +799,114 @@ __global__ void __launch_bounds__(160, F8 ? 2 : 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    // ---- tile (or piece of tile) done: accumulators -> Cs (FP8: times the row scales)
-    float rsc[2][2] = {{1.f, 1.f}, {1.f, 1.f}};
+    // ---- tile (or piece of tile) done (FP8: accumulators times the row scales)
     if constexpr (F8) {
       const int ntl = t % g.n_tiles;
 #pragma unroll
-      for (int ms = 0; ms < 2; ++ms)
+      for (int ms = 0; ms < 2; ++ms) {
+        const float s0 = 256.f * tile_row_scale(g, ntl, warp * 32 + ms * 16 + g8);
+        const float s1 = 256.f * tile_row_scale(g, ntl, warp * 32 + ms * 16 + g8 + 8);
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-          rsc[ms][h] = 256.f * tile_row_scale(g, ntl, warp * 32 + ms * 16 + g8 + 8 * h);
-    }
-#pragma unroll
-    for (int ms = 0; ms < 2; ++ms)
-#pragma unroll
-      for (int j = 0; j < NB; ++j) {
-        int wr = warp * 32 + ms * 16 + g8;
-        int ar = j * 8 + 2 * t4;
-        Cs[ar * C::PITCH + wr] = acc[ms][j][0] * rsc[ms][0];
-        Cs[(ar + 1) * C::PITCH + wr] = acc[ms][j][1] * rsc[ms][0];
-        Cs[ar * C::PITCH + wr + 8] = acc[ms][j][2] * rsc[ms][1];
-        Cs[(ar + 1) * C::PITCH + wr + 8] = acc[ms][j][3] * rsc[ms][1];
+        for (int j = 0; j < NB; ++j) {
+          acc[ms][j][0] *= s0; acc[ms][j][1] *= s0;
+          acc[ms][j][2] *= s1; acc[ms][j][3] *= s1;
+        }
       }
-    consumer_sync();
+    }
     const bool whole = (ks0 == 0) && (seg_end == tile_end);
     bool mine = true;
     if (!whole) {
-      // A tile split between CTAs: the last to arrive finishes it.  The others publish
-      // their piece and count themselves published; the finisher waits for them (they
-      // are running and wait on nothing), then sums every piece in contributor order,
-      // its own straight from shared memory.
+      // A tile split between CTAs.  Every contributor publishes its piece (in the
+      // accumulators' own fragment layout: each (ms, j) fragment of the 128 threads is
+      // 2 KB contiguous) and then counts itself in with one acquire-release add; the
+      // last to count finishes the tile, summing the pieces in contributor order, its
+      // own from registers.  Every piece is published before its count, so the
+      // finisher never waits.
       int* arrived = g.counters + t;
-      int* published = g.counters + kTileWords + t;
-      if (tid == 0) {
-        const int nc = tile_contributors(g.units, grid, g.ks, t, nullptr);
-        flag[0] = (atomicAdd(arrived, 1) == nc - 1);
-        flag[1] = nc;
-      }
+      const int slot = (u == u0) ? 0 : 1;
+      float4* dst = reinterpret_cast<float4*>(g.part + ((long long)cta * 2 + slot) * BN * kBM);
+#pragma unroll
+      for (int ms = 0; ms < 2; ++ms)
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+          dst[(ms * NB + j) * 128 + tid] =
+              make_float4(acc[ms][j][0], acc[ms][j][1], acc[ms][j][2], acc[ms][j][3]);
       consumer_sync();
-      mine = flag[0] != 0;
-      const int nc = flag[1];
-      if (!mine) {
-        const int slot = (u == u0) ? 0 : 1;
-        float* dst = g.part + ((long long)cta * 2 + slot) * BN * kBM;
-        for (int x = tid; x < BN * kBM / 4; x += 128) {
-          const int r = x / (kBM / 4), c4 = x % (kBM / 4);
-          reinterpret_cast<float4*>(dst)[x] = *reinterpret_cast<const float4*>(Cs + r * C::PITCH + c4 * 4);
-        }
-        consumer_sync();
-        if (tid == 0) red_release_add(published, 1);
-      } else {
-        if (tid == 0) {
-          tile_contributors(g.units, grid, g.ks, t, cslot);
+      if (tid == 0) {
+        const int nc = tile_contributors(g.units, grid, g.ks, t, cslot);
+        const bool last = atom_add_acq_rel_gpu(arrived, 1) == nc - 1;
+        if (last && g.wait_extra) {
+          // forced-timeout test hook: wait, boundedly, for one arrival more than can come
           const unsigned long long t0 = global_ns();
-          while (ld_acquire_gpu(published) < nc - 1 + g.wait_extra) {
+          while (ld_acquire_gpu(arrived) < nc + g.wait_extra) {
             if (global_ns() - t0 > g.wait_ns) {
               raise_error(e.err, DFLASH_DEV_TIMEOUT);
               break;
             }
           }
-          *arrived = 0;
-          *published = 0;
-          __threadfence();
         }
-        consumer_sync();
-        // every thread sums XN float4 positions; the loads of CR contributors for all of
-        // them (16 float4) are in flight together
-        constexpr int XN = BN * kBM / 4 / 128;
+        if (last) *arrived = 0;   // every contributor has counted: free for the next launch
+        flag[0] = last;
+        flag[1] = nc;
+      }
+      consumer_sync();
+      mine = flag[0] != 0;
+      if (mine) {
+        // the loads of CR contributors' pieces are in flight together
+        const int nc = flag[1];
+        constexpr int XN = 2 * NB;
         constexpr int CR = XN >= 16 ? 1 : 16 / XN;
-        float4 acc[XN];
+        float4 sum[XN];
 #pragma unroll
-        for (int q = 0; q < XN; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < XN; ++q) sum[q] = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int c0 = 0; c0 < nc; c0 += CR) {
           float4 v[CR][XN];
 #pragma unroll
-          for (int j = 0; j < CR; ++j) {
-            if (c0 + j >= nc) continue;
-            const int cs = cslot[c0 + j];
+          for (int jc = 0; jc < CR; ++jc) {
+            if (c0 + jc >= nc) continue;
+            const int cs = cslot[c0 + jc];
+            const float4* src = reinterpret_cast<const float4*>(g.part + (long long)cs * BN * kBM);
 #pragma unroll
             for (int q = 0; q < XN; ++q) {
-              const int x = tid + q * 128;
               if ((cs >> 1) == cta) {
-                const int r = x / (kBM / 4), c4 = x % (kBM / 4);
-                v[j][q] = *reinterpret_cast<const float4*>(Cs + r * C::PITCH + c4 * 4);
+                v[jc][q] = make_float4(acc[q / NB][q % NB][0], acc[q / NB][q % NB][1],
+                                       acc[q / NB][q % NB][2], acc[q / NB][q % NB][3]);
               } else {
-                v[j][q] = __ldcg(reinterpret_cast<const float4*>(g.part + (long long)cs * BN * kBM) + x);
+                v[jc][q] = __ldcg(src + q * 128 + tid);
               }
             }
           }
 #pragma unroll
-          for (int j = 0; j < CR; ++j) {
-            if (c0 + j >= nc) continue;
+          for (int jc = 0; jc < CR; ++jc) {
+            if (c0 + jc >= nc) continue;
 #pragma unroll
             for (int q = 0; q < XN; ++q) {
-              acc[q].x += v[j][q].x; acc[q].y += v[j][q].y;
-              acc[q].z += v[j][q].z; acc[q].w += v[j][q].w;
+              sum[q].x += v[jc][q].x; sum[q].y += v[jc][q].y;
+              sum[q].z += v[jc][q].z; sum[q].w += v[jc][q].w;
             }
           }
         }
-        consumer_sync();   // every own value read before Cs is overwritten
 #pragma unroll
         for (int q = 0; q < XN; ++q) {
-          const int x = tid + q * 128;
-          const int r = x / (kBM / 4), c4 = x % (kBM / 4);
-          *reinterpret_cast<float4*>(Cs + r * C::PITCH + c4 * 4) = acc[q];
+          acc[q / NB][q % NB][0] = sum[q].x; acc[q / NB][q % NB][1] = sum[q].y;
+          acc[q / NB][q % NB][2] = sum[q].z; acc[q / NB][q % NB][3] = sum[q].w;
         }
-        consumer_sync();
       }
+    }
+    if (mine) {
+      // accumulators -> Cs[activation row][output column]
+#pragma unroll
+      for (int ms = 0; ms < 2; ++ms)
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          const int wr = warp * 32 + ms * 16 + g8;
+          const int ar = j * 8 + 2 * t4;
+          Cs[ar * C::PITCH + wr] = acc[ms][j][0];
+          Cs[(ar + 1) * C::PITCH + wr] = acc[ms][j][1];
+          Cs[ar * C::PITCH + wr + 8] = acc[ms][j][2];
+          Cs[(ar + 1) * C::PITCH + wr + 8] = acc[ms][j][3];
+        }
+      consumer_sync();
     }
     if (mine) {
       const int mb = t / g.n_tiles, nt = t % g.n_tiles;
