@@ -268,10 +268,12 @@ def step_flops(w: Workload, lens=None) -> int:
 
 
 def lm_head_bytes(w: Workload) -> int:
-    """Algorithmic bytes of one LM-head launch: the head's weights, the hidden rows, and
-    the per-row token, max and log-sum-exp outputs."""
+    """Algorithmic bytes of one LM-head launch: the head's weights (FP8: one byte per
+    element plus a 4-byte scale per row), the hidden rows, and the per-row token, max and
+    log-sum-exp outputs."""
     e = 2 if w.dtype == "bf16" else 4
-    return e * (w.vocab * w.d_model + w.rows * w.d_model) + w.rows * 12
+    head = (w.vocab * w.d_model + 4 * w.vocab) if w.weight_format == "fp8" else e * w.vocab * w.d_model
+    return head + e * w.rows * w.d_model + w.rows * 12
 
 
 def main(argv=None):
