@@ -425,11 +425,12 @@ template <int BN, bool F8 = false>
 struct TcCfg {
   static constexpr int KS = F8 ? 2 * kBK : kBK;          // k per stage
   // FP8: two CTAs per SM (two consumer warps per scheduler hide the conversions'
-  // latency), so each holds a shorter ring.  bf16: rings of 8 (16 rows) and 6 (32 rows)
-  // stages leave room on the SM for a CTA of the next kernels (attention, RMSNorm,
+  // latency), so each holds a shorter ring (3 and 2 stages: 606 -> 598 us a batch-1
+  // step against 4 and 3; 2/2: 615, 3/3: 600).  bf16: rings of 8 (16 rows) and 6 (32
+  // rows) stages leave room on the SM for a CTA of the next kernels (attention, RMSNorm,
   // combine) to start while the projection drains: measured on GB300 at batch 1,
   // 718 -> 708 us a step against 10 and 8 stages (9/6: 713, 8/7: 712, 6/5: 709, 5/4: 734).
-  static constexpr int NS = F8 ? (BN == 16 ? 4 : 3)
+  static constexpr int NS = F8 ? (BN == 16 ? 3 : 2)
                                : (BN == 16 ? 8 : BN == 32 ? 6 : BN == 64 ? 6 : 4);
   static constexpr int CTAS_PER_SM = F8 ? 2 : 1;
   static constexpr int W_BYTES = kBM * kBK * 2;           // 16 KB either way
