@@ -162,7 +162,7 @@ struct AuCfg {
   // head_dim 128: one CTA per SM with a five-stage ring (two CTAs would leave room for
   // two 32 KB stages each, one step of lookahead: the loads, not the softmax, bound it)
   static constexpr int CPS = HD == 64 ? 2 : 1;     // CTAs per SM
-  static constexpr int NS = HD == 64 ? 4 : 5;      // ring stages
+  static constexpr int NS = 4;                     // ring stages (head_dim 128: 3 and 5 slower)
   static constexpr int NK = KSPLIT ? KT / 2 : KT;  // keys of a step per softmax thread
   static constexpr int Q_BYTES = 128 * HD * 2;
   static constexpr int KV_BLOCK = KT * 128;        // one 64-column block of K or V
