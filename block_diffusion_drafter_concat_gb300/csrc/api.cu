@@ -299,7 +299,8 @@ dflash_status rmsnorm(const H* h, const Tin* x, const void* gain, T* y, int rows
                 static_cast<float*>(nullptr), static_cast<const T*>(gain), y, h->c.d_model,
                 h->c.rms_eps, static_cast<const int*>(nullptr), static_cast<const T*>(nullptr), 0,
                 static_cast<const int*>(nullptr), 1, 0, static_cast<int*>(nullptr), h->d_err,
-                static_cast<const T*>(nullptr));
+                static_cast<const T*>(nullptr), static_cast<const Tin*>(nullptr),
+                static_cast<const T*>(nullptr), 0);
 }
 
 // ------------------------------------------------------------------ attention plan
@@ -542,8 +543,9 @@ dflash_status check_device(const dflash_handle_s* h) {
 
 }  // namespace
 
+// fused = RMSNorm(x_cat W_fuse^T) with gain g_fuse (norm = false: only u = x_cat W_fuse^T)
 static dflash_status fuse_impl(H* h, const void* x_cat, int n, void* fused, float* u,
-                               float* gpart, int* ctl, cudaStream_t st) {
+                               float* gpart, int* ctl, cudaStream_t st, bool norm = true) {
   const int kin = h->c.n_target_layers * h->c.target_width;
   WSet w;
   w.add(&h->m_fuse, h->w_fuse, h->c.d_model);
@@ -553,6 +555,7 @@ static dflash_status fuse_impl(H* h, const void* x_cat, int n, void* fused, floa
     e.ldy = h->c.d_model;
     e.err = h->d_err;
     TRY((gemm<EPI_F32, bf16>(h, x_cat, n, kin, w, e, gpart, ctl, st)));
+    if (!norm) return DFLASH_OK;
     return rmsnorm<bf16, float>(h, u, h->g_fuse, static_cast<bf16*>(fused), n, st);
   }
   EpiArgs<float> e = {};
@@ -560,6 +563,7 @@ static dflash_status fuse_impl(H* h, const void* x_cat, int n, void* fused, floa
   e.ldy = h->c.d_model;
   e.err = h->d_err;
   TRY((gemm<EPI_F32, float>(h, x_cat, n, kin, w, e, gpart, ctl, st)));
+  if (!norm) return DFLASH_OK;
   return rmsnorm<float, float>(h, u, h->g_fuse, static_cast<float*>(fused), n, st);
 }
 
@@ -624,6 +628,9 @@ struct StackOpts {
   int n_inj = 0;
   const int32_t* inj_pos = nullptr;
   const int32_t* inj_slots = nullptr;
+  // the fused rows before their RMSNorm (fp32): normalised by the step's first launch
+  // together with the block's embedding rows
+  const float* inj_u = nullptr;
 };
 
 template <typename T>
@@ -636,11 +643,14 @@ static dflash_status draft_impl(H* h, const StackOpts& o, const int32_t* ctx_len
   const int qw = c.n_q_heads * c.head_dim, kvw = c.n_kv_heads * c.head_dim;
   const int G = c.n_q_heads / c.n_kv_heads, QR = S * G;
   T* n = static_cast<T*>(w.n);
-  // embedding (or input rows) + first pre-attention norm + positions
-  TRY(launch(k_rmsnorm<T, float>, dim3(M), dim3(kRowThreads), 0, st,
+  // embedding (or input rows) + first pre-attention norm + positions (and the fused
+  // context rows' norm, rows M.. of the same launch)
+  const int n_u = o.inj_u ? o.n_inj : 0;
+  TRY(launch(k_rmsnorm<T, float>, dim3(M + n_u), dim3(kRowThreads), 0, st,
              static_cast<const float*>(nullptr), w.x, static_cast<const T*>(h->g_attn[0]), n, d,
              c.rms_eps, o.ids, static_cast<const T*>(h->embed), c.vocab, ctx_lens, S,
-             c.max_position, w.pos, h->d_err, static_cast<const T*>(o.rows)));
+             c.max_position, w.pos, h->d_err, static_cast<const T*>(o.rows), o.inj_u,
+             static_cast<const T*>(h->g_fuse), M));
   const AttnPlan ap = plan_attn(h, B, max_pages, o.causal);
   // a chunk whose only output is the cache needs no attention or MLP in its last layer
   const bool kv_only_last = o.write_cache && !o.final_hidden && o.n_taps == 0;
@@ -1151,18 +1161,22 @@ dflash_status dflash_inject_draft(dflash_handle h, const void* x_cat, int32_t n_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // fused rows straight after the block's normed rows: the Q/K/V projections read both
   char* rows = static_cast<char*>(w.n) + (size_t)M * c.d_model * elt(h);
-  TRY(fuse_impl(h, x_cat, n_inj, rows, w.u, w.gpart, w.ctl, st));
-  if (fused_out)
-    CUDA_TRY(cudaMemcpyAsync(fused_out, rows, (size_t)n_inj * c.d_model * elt(h),
-                             cudaMemcpyDeviceToDevice, st));
+  TRY(fuse_impl(h, x_cat, n_inj, rows, w.u, w.gpart, w.ctl, st, false));
   StackOpts o;
   o.ids = block_ids;
   o.final_hidden = final_hidden;
   o.n_inj = n_inj;
   o.inj_pos = positions;
   o.inj_slots = slots;
-  return draft_impl<bf16>(h, o, ctx_lens, page_table, max_pages, batch, num_pages, k_pool,
-                          v_pool, w, st);
+  o.inj_u = w.u;
+  TRY(draft_impl<bf16>(h, o, ctx_lens, page_table, max_pages, batch, num_pages, k_pool, v_pool,
+                       w, st));
+  // the fused rows stay where the first launch normalised them (no later launch writes
+  // them)
+  if (fused_out)
+    CUDA_TRY(cudaMemcpyAsync(fused_out, rows, (size_t)n_inj * c.d_model * elt(h),
+                             cudaMemcpyDeviceToDevice, st));
+  return DFLASH_OK;
 }
 
 

@@ -25,14 +25,24 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // With `ids`, x[m] is first set to the embedding row ids[m] (block embedding), with
 // `rows` (and no ids) to rows[m] (input rows of a chunk of context), and in both cases
 // the position ctx_lens[m / S] + m % S is written to pos[m] and x[m] to xout.
+// With `xin2`, the CTAs m >= m2 normalise a second set of rows in the same launch:
+// y[m] = xin2[m - m2] / rms * gain2 (the fused context rows that follow the block's
+// rows in the first projection's input).
 template <typename T, typename Tin>
 __global__ void __launch_bounds__(kRowThreads)
     k_rmsnorm(const Tin* __restrict__ xin, float* __restrict__ xout, const T* __restrict__ gain,
               T* __restrict__ y, int d, float eps, const int* __restrict__ ids,
               const T* __restrict__ embed, int vocab, const int* __restrict__ ctx_lens, int S,
-              int max_position, int* __restrict__ pos, int* err,
-              const T* __restrict__ rows = nullptr) {
+              int max_position, int* __restrict__ pos, int* err, const T* __restrict__ rows,
+              const Tin* __restrict__ xin2, const T* __restrict__ gain2, int m2) {
   __shared__ float red[kRowThreads / 32];
+  const int m = blockIdx.x;
+  if (xin2 && m >= m2) {
+    xin = xin2 - (long long)m2 * d;   // so that xin + m * d is row m - m2 of xin2
+    gain = gain2;
+    ids = nullptr;
+    rows = nullptr;
+  }
   // the gains are weights (never written on the device): fetch them before the wait
   float gv[32];
   const bool regs = (sizeof(Tin) == 4) && (d & 3) == 0 && d <= kRowThreads * 4 * 8 && !ids &&
@@ -47,7 +57,6 @@ __global__ void __launch_bounds__(kRowThreads)
   }
   pdl_wait();
   pdl_launch_dependents();
-  const int m = blockIdx.x;
   const Tin* src = xin + (long long)m * d;
   if (ids || rows) {
     int id = ids ? ids[m] : 0;
