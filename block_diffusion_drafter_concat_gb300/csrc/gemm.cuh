@@ -926,7 +926,7 @@ __global__ void __launch_bounds__(160, F8 ? 2 : 1)
 // fp32 workloads keep full fp32 products (no TF32): one CTA per (m-block, n-tile) of
 // 16 rows x 128 columns, FFMA over K, then the same epilogues.
 constexpr int kF32BN = 16;
-constexpr int kF32BK = 32;
+constexpr int kF32BK = 64;
 
 struct WPtrs {
   const float* p[kMaxSeg];
@@ -951,20 +951,41 @@ __global__ void __launch_bounds__(256)
   // thread -> (act row ar, 8 weight rows wr..wr+7 strided by 16)
   const int ar = tid % kF32BN, wr0 = tid / kF32BN;
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int k0 = 0; k0 < g.K; k0 += kF32BK) {
-    for (int x = tid; x < kF32BN * kF32BK; x += 256) {
-      int r = x / kF32BK, k = x % kF32BK;
-      int m = mb * kF32BN + r;
-      As[r][k] = (m < g.M && k0 + k < g.K) ? A[(long long)m * lda + k0 + k] : 0.f;
+  // The next k-tile is loaded into registers while this one is multiplied from shared
+  // memory (the loop is a chain of global round trips otherwise); k stays in ascending
+  // order, so the sums are those of the plain loop.
+  constexpr int NA = kF32BN * kF32BK / 256, NW = kBM * kF32BK / 256;
+  float ra[NA], rw[NW];
+  auto fetch = [&](int k0) {
+#pragma unroll
+    for (int q = 0; q < NA; ++q) {
+      const int x = tid + q * 256, r = x / kF32BK, k = x % kF32BK;
+      const int m = mb * kF32BN + r;
+      ra[q] = (m < g.M && k0 + k < g.K) ? A[(long long)m * lda + k0 + k] : 0.f;
     }
-    for (int x = tid; x < kBM * kF32BK; x += 256) {
-      int r = x / kF32BK, k = x % kF32BK;
-      int sg = g.paired ? (r < kBM / 2 ? 0 : 1) : seg;
-      int row = r0 + (g.paired ? r % (kBM / 2) : r);
-      Ws[r][k] = (row < g.seg_rows[sg] && k0 + k < g.K)
-                     ? Wseg.p[sg][(long long)row * g.K + k0 + k] : 0.f;
+#pragma unroll
+    for (int q = 0; q < NW; ++q) {
+      const int x = tid + q * 256, r = x / kF32BK, k = x % kF32BK;
+      const int sg = g.paired ? (r < kBM / 2 ? 0 : 1) : seg;
+      const int row = r0 + (g.paired ? r % (kBM / 2) : r);
+      rw[q] = (row < g.seg_rows[sg] && k0 + k < g.K) ? Wseg.p[sg][(long long)row * g.K + k0 + k]
+                                                       : 0.f;
+    }
+  };
+  fetch(0);
+  for (int k0 = 0; k0 < g.K; k0 += kF32BK) {
+#pragma unroll
+    for (int q = 0; q < NA; ++q) {
+      const int x = tid + q * 256;
+      As[x / kF32BK][x % kF32BK] = ra[q];
+    }
+#pragma unroll
+    for (int q = 0; q < NW; ++q) {
+      const int x = tid + q * 256;
+      Ws[x / kF32BK][x % kF32BK] = rw[q];
     }
     __syncthreads();
+    if (k0 + kF32BK < g.K) fetch(k0 + kF32BK);
 #pragma unroll 4
     for (int k = 0; k < kF32BK; ++k) {
       float a = As[ar][k];
