@@ -88,6 +88,27 @@ dflash_status encode_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64
   return DFLASH_OK;
 }
 
+// Row-major fp32 matrix [rows, inner] (row stride inner elements), written by TMA in
+// boxes of box_rows x 32 elements (128 bytes) with 128-byte swizzle.
+dflash_status encode_f32_store(CUtensorMap* m, void* ptr, uint64_t rows, uint64_t inner,
+                               uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(DFLASH_ECUDA, "cuTensorMapEncodeTiled unavailable");
+  if (!aligned16(ptr) || (inner * 4) % 16 != 0 || rows == 0 || inner < 32 || box_rows == 0 ||
+      box_rows > 256)
+    return fail(DFLASH_EINVAL, "fp32 tensor %p (%llu x %llu) not TMA-compatible", ptr,
+                (unsigned long long)rows, (unsigned long long)inner);
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 4};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DFLASH_ECUDA, "cuTensorMapEncodeTiled (f32) failed (%d)", (int)r);
+  return DFLASH_OK;
+}
+
 // Packed FP8 matrix [rows, cols]: e4m3 codes with row stride round_up(cols, 16) bytes,
 // then rows fp32 scales at a 256-byte aligned offset.
 size_t fp8_ld(long long cols) { return (size_t)((cols + 15) / 16 * 16); }
@@ -722,7 +743,7 @@ static dflash_status draft_impl(H* h, const StackOpts& o, const int32_t* ctx_len
         TRY(encode_bf16(&mp.kb, w.kb, blk_rows, c.head_dim, c.head_dim, kPage));
         TRY(encode_bf16(&mp.vb, w.vb, blk_rows, c.head_dim, c.head_dim, kPage));
         if (use_attn_umma(c, M) && !o.causal) {
-          AuMaps am;
+          AuMaps am = {};
           am.k = mp.k;
           am.v = mp.v;
           am.kb = mp.kb;
@@ -730,6 +751,10 @@ static dflash_status draft_impl(H* h, const StackOpts& o, const int32_t* ctx_len
           const bool ks = attn_ksplit(c);
           TRY(encode_bf16(&am.q, w.q, (uint64_t)B * c.n_kv_heads * QR, c.head_dim, c.head_dim,
                           ks ? 64 : 128));
+          // split partials of O leave the kernel as TMA stores of QR x 32 boxes
+          if (ap.nsplit > 1)
+            TRY(encode_f32_store(&am.po, w.part_o, (uint64_t)B * c.n_kv_heads * ap.nsplit * QR,
+                                 c.head_dim, QR));
           TRY(launch_attn_umma(c.head_dim, ks, grid, am, a, st));
         } else {
           TRY(launch_attn_tc(c.head_dim, QR / 16, grid, attn_tc_smem(c.head_dim), mp, a, st));

@@ -52,6 +52,7 @@ struct AttnArgs {
 // the pools and the block K/V with 16-row boxes.
 struct AuMaps {
   CUtensorMap q, k, v, kb, vb;
+  CUtensorMap po;   // split partial O as fp32 rows [.., hd], boxes of QR rows x 32 columns
 };
 
 struct AttnMaps {

@@ -114,13 +114,16 @@ __device__ __forceinline__ float exp2_row(float (&x)[N], float sc, float nref) {
 template <int N>
 __device__ __forceinline__ float max_tree(const float (&x)[N]);
 
-// bf16 pair hi (round to nearest even) and the pair of residuals lo = bf16(x - hi).
+// bf16 pair hi = the upper halves of (a, b) (truncation: one byte permute) and the pair
+// of residuals lo = bf16(x - hi), rounded to nearest even (x - hi is exact in fp32).
+// hi + lo is within 2^-16 of x relative (|x - hi| < 2^-7 |x|, lo's rounding 2^-9 of it).
 __device__ __forceinline__ void split_bf16x2_f2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  const float2 hf = __bfloat1622float2(h);
-  hi = *reinterpret_cast<uint32_t*>(&h);
+  const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+  hi = __byte_perm(ua, ub, 0x7632);
   float r0, r1;
-  f2_unpack(f2_sub(f2_pack(a, b), f2_pack(hf.x, hf.y)), r0, r1);
+  f2_unpack(f2_sub(f2_pack(a, b), f2_pack(__uint_as_float(ua & 0xffff0000u),
+                                          __uint_as_float(ub & 0xffff0000u))),
+            r0, r1);
   lo = pack_bf16x2(r0, r1);
 }
 
@@ -178,9 +181,31 @@ struct AuCfg {
   static constexpr uint32_t IDESC_O = umma_idesc_bf16<128, HD>() | (1u << 16);  // B MN-major
   static_assert(O_COL + HD <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
-  // key-split merge buffer (64 rows of O and (m, l)) reuses the K/V ring
-  static_assert(!KSPLIT || 64 * HD * 4 + 64 * 8 <= NS * STAGE, "merge buffer");
+  // After the last MMA the K/V ring is idle: the key-split merge buffer (64 rows of O and
+  // (m, l)) takes its first half, the staged split output (up to 128 rows x HD fp32, in
+  // 32-column slabs) the rest (key-split) or all of it
+  static constexpr int STG_OFF = KSPLIT ? NS * STAGE / 2 : 0;
+  static constexpr int MAX_QR = KSPLIT ? 64 : 128;
+  static_assert(!KSPLIT || 64 * HD * 4 + 64 * 8 <= STG_OFF, "merge buffer");
+  static_assert(STG_OFF + MAX_QR * HD * 4 <= NS * STAGE, "staged output");
+  static_assert(32 % PG == 0, "page ids of whole steps per 32 lanes");
 };
+
+// Byte pitch of one 32-column slab of the staged output: rows of 128 bytes, whole
+// 1024-byte swizzle atoms.
+__device__ __forceinline__ int stage_pitch(int QR) { return ((QR + 7) & ~7) * 128; }
+
+// Row `row` of slab `c` (32 fp32 values) into the staged output, 128-byte swizzled as a
+// TMA store of a box of 32 columns expects it (eight 16-byte chunks per row, chunk k at
+// position k ^ (row & 7): a warp's stores of one chunk hit distinct banks).
+__device__ __forceinline__ void stage_row32(uint8_t* stg, int c, int QR, int row,
+                                            const uint32_t (&v)[32]) {
+  uint8_t* slab = stg + c * stage_pitch(QR);
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    *reinterpret_cast<uint4*>(slab + swz128(row, k)) =
+        make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+}
 
 template <int HD, bool KSPLIT>
 __global__ void __launch_bounds__(192, AuCfg<HD, KSPLIT>::CPS)
@@ -203,7 +228,12 @@ __global__ void __launch_bounds__(192, AuCfg<HD, KSPLIT>::CPS)
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // context lengths and the page table predate the previous kernel (read before the wait)
+  // context lengths and the page table predate the previous kernel (read before the wait);
+  // warp 0 requests the page ids of the split's first 32 pages together with the length
+  // (entries past the sequence's pages are read, inside the table's row, but not used)
+  int tab0 = 0;
+  if (warp == 0 && split * a.pps + lane < a.max_pages)
+    tab0 = a.page_table[(long long)b * a.max_pages + split * a.pps + lane];
   const int T = a.ctx_lens[b];
   if (T < 0 || T > a.max_pages * kPage) {
     if (tid == 0) raise_error(a.err, DFLASH_DEV_BAD_INDEX);
@@ -265,14 +295,29 @@ __global__ void __launch_bounds__(192, AuCfg<HD, KSPLIT>::CPS)
         }
       }
     };
+    // Page ids 32 at a time (SPC steps), lane i holding page 32c + i of the split; the
+    // next 32 are requested SPC steps before they are needed, so that the ring's refills
+    // never wait on a page-table read.
+    constexpr int SPC = 32 / C::PG;
+    auto fetch_tab = [&](int j0) {
+      const int pg = p0 + j0 * C::PG + lane;
+      return (j0 < nsteps && pg < np && pg < p1)
+                 ? a.page_table[(long long)b * a.max_pages + pg]
+                 : 0;
+    };
+    int tab = tab0, tab_next = fetch_tab(SPC);
     for (int j = 0; j < nsteps && ok; ++j) {
       const int s = j % C::NS;
       const int pa = j * C::PG;                       // first page of the step in the split
       const int cnt = min(C::PG, npg - pa);
       if (j >= C::NS || p0 + pa + cnt > np) wait_then_q();
+      if (j > 0 && j % SPC == 0) {
+        tab = tab_next;
+        tab_next = fetch_tab(j + SPC);
+      }
+      const int tpage = __shfl_sync(0xffffffffu, tab, ((j % SPC) * C::PG + lane) & 31);
       int my_page = 0;
-      if (lane < cnt && p0 + pa + lane < np)
-        my_page = a.page_table[(long long)b * a.max_pages + p0 + pa + lane];
+      if (lane < cnt && p0 + pa + lane < np) my_page = tpage;
       if (lane == 0 && j >= C::NS && !mbar_wait(&kvempty[s], ((j / C::NS) - 1) & 1)) {
         raise_error(a.err, DFLASH_DEV_TIMEOUT);
         ok = false;
@@ -520,6 +565,10 @@ __global__ void __launch_bounds__(192, AuCfg<HD, KSPLIT>::CPS)
     if (ok && nsteps > 0 && !__all_sync(0xffffffffu, mbar_wait(ofull, (nsteps - 1) & 1))) ok = false;
     if (!ok && lane == 0) raise_error(a.err, DFLASH_DEV_TIMEOUT);
     tc_fence_after();
+    // split partials (o unnormalised) go out through shared memory and TMA stores of
+    // whole 32-column slabs; a single split's normalised output is written directly
+    const bool staged = a.nsplit > 1;
+    uint8_t* stg = stages + C::STG_OFF;
     if constexpr (KSPLIT) {
       // The K/V ring is idle (every MMA has completed): lanes 64-127 leave their O row
       // and (m, l) there, lanes 0-63 merge them into theirs.  Row q's columns are
@@ -552,12 +601,16 @@ __global__ void __launch_bounds__(192, AuCfg<HD, KSPLIT>::CPS)
           tmem_ld_wait();
           if (qrow < a.QR && ok) {
 #pragma unroll
-            for (int d = 0; d < 32; d += 2) {
-              const float o0 = __uint_as_float(ov[d]) * w1 +
-                               mo[qrow * HD + ((c * 32 + d + qrow) & (HD - 1))] * w2;
-              const float o1 = __uint_as_float(ov[d + 1]) * w1 +
-                               mo[qrow * HD + ((c * 32 + d + 1 + qrow) & (HD - 1))] * w2;
-              attn_emit<bf16>(a, b, g, split, qrow, c * 32 + d, o0, o1, l);
+            for (int d = 0; d < 32; ++d)
+              ov[d] = __float_as_uint(__uint_as_float(ov[d]) * w1 +
+                                      mo[qrow * HD + ((c * 32 + d + qrow) & (HD - 1))] * w2);
+            if (staged) {
+              stage_row32(stg, c, a.QR, qrow, ov);
+            } else {
+#pragma unroll
+              for (int d = 0; d < 32; d += 2)
+                attn_emit<bf16>(a, b, g, split, qrow, c * 32 + d, __uint_as_float(ov[d]),
+                                __uint_as_float(ov[d + 1]), l);
             }
           }
         }
@@ -571,11 +624,25 @@ __global__ void __launch_bounds__(192, AuCfg<HD, KSPLIT>::CPS)
         tmem_ld32(o_addr + c * 32, ov);
         tmem_ld_wait();
         if (r < a.QR && ok) {
+          if (staged) {
+            stage_row32(stg, c, a.QR, r, ov);
+          } else {
 #pragma unroll
-          for (int d = 0; d < 32; d += 2)
-            attn_emit<bf16>(a, b, g, split, r, c * 32 + d, __uint_as_float(ov[d]),
-                            __uint_as_float(ov[d + 1]), l);
+            for (int d = 0; d < 32; d += 2)
+              attn_emit<bf16>(a, b, g, split, r, c * 32 + d, __uint_as_float(ov[d]),
+                              __uint_as_float(ov[d + 1]), l);
+          }
         }
+      }
+    }
+    if (staged) {
+      fence_proxy_async_smem();
+      if (epi_sync_and(ok) && tid == 64) {
+        const int y = static_cast<int>((((long long)b * a.hkv + g) * a.nsplit + split) * a.QR);
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) tma_store_2d(&maps.po, stg + c * stage_pitch(a.QR), c * 32, y);
+        bulk_commit();
+        bulk_wait_read();
       }
     }
     if (!half && qrow < a.QR) {

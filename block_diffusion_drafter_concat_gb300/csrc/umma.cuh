@@ -151,6 +151,17 @@ struct UmCfg {
 };
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// The same barrier, returning whether `v` holds in all 128 threads.
+__device__ __forceinline__ bool epi_sync_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
 
 // Residual rows of one 32-row epilogue chunk for the four epilogue warps: warp w takes
 // rows w, w + 4, ..., w + 28 of the chunk, lane the four columns 4*lane .. 4*lane + 3 of
