@@ -272,29 +272,29 @@ __global__ void __launch_bounds__(192, AuCfg<HD, KSPLIT>::CPS)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
-    // Context pages are fetched before the wait; Q, the block's own keys and any stage
-    // that reuses the ring (its consumers need Q) come after it.
-    bool ok = true, waited = false;
+    // Q first, after the wait (the previous kernel writes it), then the K/V stages.  A
+    // CTA's first S needs Q and the first stage only, and one SM's loads arrive about in
+    // the order they were issued at its share of the bandwidth: behind a full ring, Q
+    // would come a ring's transfer time later (measured on GB300: Q after the ring
+    // 1426 us per Llama-shaped batch-8 step, after the first stage 1397 us, first 1395 us;
+    // gpt-oss-shaped batch 64: 4833 / 4796 / 4794 us).
+    bool ok = true;
     int issued = 0;
-    auto wait_then_q = [&]() {
-      if (waited) return;
-      pdl_wait();
-      waited = true;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(qfull, C::Q_BYTES);
+    pdl_wait();
+    if (lane == 0) {
+      mbar_arrive_expect_tx(qfull, C::Q_BYTES);
 #pragma unroll
-        for (int kb = 0; kb < C::KB; ++kb) {
-          if constexpr (KSPLIT) {
-            // the group's (up to) 64 query rows in tile rows 0-63 and again in 64-127
-            tma_load_2d(sq + kb * (128 * 128), &maps.q, qfull, kb * 64, (b * a.hkv + g) * a.QR);
-            tma_load_2d(sq + kb * (128 * 128) + 64 * 128, &maps.q, qfull, kb * 64,
-                        (b * a.hkv + g) * a.QR);
-          } else {
-            tma_load_2d(sq + kb * (128 * 128), &maps.q, qfull, kb * 64, (b * a.hkv + g) * a.QR);
-          }
+      for (int kb = 0; kb < C::KB; ++kb) {
+        if constexpr (KSPLIT) {
+          // the group's (up to) 64 query rows in tile rows 0-63 and again in 64-127
+          tma_load_2d(sq + kb * (128 * 128), &maps.q, qfull, kb * 64, (b * a.hkv + g) * a.QR);
+          tma_load_2d(sq + kb * (128 * 128) + 64 * 128, &maps.q, qfull, kb * 64,
+                      (b * a.hkv + g) * a.QR);
+        } else {
+          tma_load_2d(sq + kb * (128 * 128), &maps.q, qfull, kb * 64, (b * a.hkv + g) * a.QR);
         }
       }
-    };
+    }
     // Page ids 32 at a time (SPC steps), lane i holding page 32c + i of the split; the
     // next 32 are requested SPC steps before they are needed, so that the ring's refills
     // never wait on a page-table read.
@@ -310,7 +310,6 @@ __global__ void __launch_bounds__(192, AuCfg<HD, KSPLIT>::CPS)
       const int s = j % C::NS;
       const int pa = j * C::PG;                       // first page of the step in the split
       const int cnt = min(C::PG, npg - pa);
-      if (j >= C::NS || p0 + pa + cnt > np) wait_then_q();
       if (j > 0 && j % SPC == 0) {
         tab = tab_next;
         tab_next = fetch_tab(j + SPC);
@@ -362,7 +361,6 @@ __global__ void __launch_bounds__(192, AuCfg<HD, KSPLIT>::CPS)
       }
       issued = j + 1;
     }
-    wait_then_q();
     if (lane == 0) {
       // never leave with copies in flight
       mbar_wait(qfull, 0);
