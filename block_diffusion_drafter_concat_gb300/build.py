@@ -18,7 +18,7 @@ OBJDIR = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--compiler-options", "-fPIC",
          "-Xcompiler", "-fvisibility=hidden"]
-UNITS = ["api.cu", "tu_gemm_a.cu", "tu_gemm_b.cu", "tu_gemm_c.cu", "tu_gemm_f8.cu", "tu_attn.cu",
+UNITS = ["api.cu", "tu_gemm_a.cu", "tu_gemm_b.cu", "tu_gemm_c.cu", "tu_gemm_d.cu", "tu_gemm_f8.cu", "tu_attn.cu",
          "tu_attn_umma.cu"]
 
 

@@ -193,6 +193,9 @@ struct WSet {
 // Activation rows per tile: up to 64 rows the projections stream weights past an
 // mma.sync tile; beyond that they are dense contractions for the tcgen05 kernel.
 int pick_bn(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256; }
+
+// tcgen05 projections that take whole 256-row tiles run on SM pairs (cta_group::2)
+constexpr bool kPairTiles = true;
 bool umma_bn(int bn) { return bn >= 128; }
 
 GemmShape plan_shape(const H* h, const WSet& w, int M, int K, bool tc, int* grid_out) {
@@ -261,6 +264,20 @@ GemmShape plan_shape(const H* h, const WSet& w, int M, int K, bool tc, int* grid
   g.m_blocks = ceil_div(M, bn);
   g.units = (long long)g.m_blocks * g.n_tiles * g.ks;
   if (grid == 0) grid = streamk_grid(g.units);
+  if (kPairTiles && tc && bn == 256 && g.tile_mode && !h->fp8) {
+    // whole 256-row tiles on SM pairs: a pair takes an activation block against two
+    // weight tiles (each SM loads its weight box and half the activation box), in as many
+    // waves of pairs as the single-CTA plan had of tiles.  Measured on GB300 (cold, one
+    // Qwen3-shaped layer at 512 rows): O 45.3 -> 37 us, Q/K/V and gate/up unchanged (48
+    // and 89 us: not bound by operand delivery); graph steps: batch 32 2306 -> 2294 us,
+    // gpt-oss batch 64 4775 -> 4751 us.  128-row tiles on pairs were slower (Llama
+    // batch 8 1393 -> 1431 us) and stay on single CTAs.
+    const long long t2 = (long long)g.m_blocks * ((g.n_tiles + 1) / 2);
+    const long long pairs = std::max<long long>(1, h->sms / 2);
+    const long long waves = (t2 + pairs - 1) / pairs;
+    g.pair = 1;
+    grid = static_cast<int>(2 * ((t2 + waves - 1) / waves));
+  }
   *grid_out = std::max(1, grid);
   return g;
 }
@@ -291,7 +308,7 @@ dflash_status gemm(const H* h, const void* A, int M, int K, const WSet& w, EpiAr
   if constexpr (std::is_same<T, bf16>::value) {
     CUtensorMap tmA;
     const int bn = g.bn;
-    TRY(encode_bf16(&tmA, A, M, K, K, bn));
+    TRY(encode_bf16(&tmA, A, M, K, K, g.pair ? bn / 2 : bn));
     WMaps wm;
     for (int s = 0; s < w.nseg; ++s) wm.m[s] = *w.maps[s];
     if (h->fp8) {
@@ -300,7 +317,9 @@ dflash_status gemm(const H* h, const void* A, int M, int K, const WSet& w, EpiAr
                                                      fp8_scale_offset(w.rows[s], K));
       return launch_gemm_tc_f8(bn, EPI, tmA, wm, g, grid, e, st);
     }
-    if (umma_bn(bn)) return launch_gemm_umma(bn, EPI, tmA, wm, g, grid, e, st);
+    if (umma_bn(bn))
+      return g.pair ? launch_gemm_umma_pairs(bn, EPI, tmA, wm, g, grid, e, st)
+                    : launch_gemm_umma(bn, EPI, tmA, wm, g, grid, e, st);
     if (bn <= 32) return launch_gemm_tc_lo(bn, EPI, tmA, wm, g, grid, e, st);
     return launch_gemm_tc_hi(bn, EPI, tmA, wm, g, grid, e, st);
   } else {

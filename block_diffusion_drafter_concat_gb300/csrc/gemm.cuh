@@ -85,6 +85,7 @@ struct GemmShape {
   int M, K, n_tiles, ks, m_blocks, paired, nseg;
   int bn;          // activation rows per tile
   int tile_mode;   // 1: CTAs take whole tiles (no split); 0: stream-K unit ranges
+  int pair;        // tcgen05 whole tiles on SM pairs (two weight tiles per pair)
   long long units;
   int seg_tile0[kMaxSeg + 1];
   int seg_rows[kMaxSeg];  // rows of each weight matrix

@@ -43,6 +43,31 @@ dflash_status launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
   return DFLASH_OK;
 }
 
+// The same for clusters of two CTAs (SM pairs): the grid must be even.
+template <typename... KArgs, typename... Args>
+dflash_status launch_pairs(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           cudaStream_t st, Args... args) {
+  if (grid.x % 2 != 0) return fail(DFLASH_EINVAL, "SM-pair launch with an odd grid (%u)", grid.x);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  if (e != cudaSuccess) return fail(DFLASH_ECUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+  count_launch();
+  return DFLASH_OK;
+}
+
 template <typename K>
 dflash_status set_smem(K kern, int bytes) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -91,6 +116,10 @@ dflash_status launch_gemm_tc_f8(int bn, int epi, const CUtensorMap& tmA, const W
 dflash_status launch_gemm_umma(int bn, int epi, const CUtensorMap& tmA, const WMaps& wm,
                                const GemmShape& g, int grid, const EpiArgs<bf16>& e,
                                cudaStream_t st);
+// tu_gemm_d.cu: the same on SM pairs (whole tiles, an even grid of CTAs)
+dflash_status launch_gemm_umma_pairs(int bn, int epi, const CUtensorMap& tmA, const WMaps& wm,
+                                     const GemmShape& g, int grid, const EpiArgs<bf16>& e,
+                                     cudaStream_t st);
 dflash_status launch_gemm_f32(int epi, dim3 grid, const float* A, int lda, const WPtrs& w,
                               const GemmShape& g, const EpiArgs<float>& e, cudaStream_t st);
 dflash_status launch_attn_tc(int hd, int nw, dim3 grid, int smem, const AttnMaps& mp,

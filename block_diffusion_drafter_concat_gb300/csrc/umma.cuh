@@ -92,6 +92,91 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       : "memory");
 }
 
+// ---- SM pairs (a cluster of two CTAs, tcgen05 with cta_group::2).  Every tcgen05
+// instruction of a pair kernel names cta_group::2: one warp of each CTA allocates (and
+// frees) the same TMEM columns together; the even CTA issues the MMAs, which read the
+// A rows 0-127 and the first half of B's rows from its own shared memory and A rows
+// 128-255 and B's second half from its peer's (same offsets), and each CTA's TMEM gets
+// its 128 rows of D.
+__device__ __forceinline__ void tmem_alloc2(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the barrier at `bar`'s offset in both CTAs of the pair when every
+// tcgen05 operation this thread issued so far is done.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+// The same, on this CTA's barrier only.
+__device__ __forceinline__ void umma_commit_pair_local(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of this CTA's shared variable `p` in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+// Every thread of both CTAs (arrive with release, wait with acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// Arrive on a barrier given by its cluster address (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr)
+               : "memory");
+}
+// 2-D tiled copy global -> this CTA's shared memory whose completion is counted on a
+// barrier of either CTA of the pair (`bar_cl`: cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m, uint32_t bar_cl,
+                                                 int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(bar_cl), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_pair_hint(void* dst, const CUtensorMap* m,
+                                                      uint32_t bar_cl, int x, int y,
+                                                      uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(bar_cl), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
 // 32 consecutive 32-bit TMEM columns of this warp's 32 lanes (lane i of the warp reads
 // TMEM lane (taddr >> 16) + i).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
@@ -129,12 +214,16 @@ __device__ __forceinline__ void tmem_st_wait() {
 }
 
 // ------------------------------------------------------------------ configuration
-template <int BN>
+template <int BN, bool P2 = false>
 struct UmCfg {
   static_assert(BN == 128 || BN == 256, "tcgen05 tiles take 128 or 256 activation rows");
-  static constexpr int NS = BN == 256 ? 4 : 6;       // pipeline stages
+  // SM pairs: each CTA's stages hold its own 128 weight rows and half the tile's
+  // activation rows (the MMA reads the other half from the peer): two thirds of the
+  // bytes per stage for the same MMA work per SM (256-row tiles), so more stages fit
+  static constexpr int NS = P2 ? (BN == 256 ? 6 : 8) : (BN == 256 ? 4 : 6);   // stages
   static constexpr int W_BYTES = kBM * kBK * 2;      // 16 KB weight box(es)
-  static constexpr int A_BYTES = BN * kBK * 2;       // activation box
+  static constexpr int A_ROWS = P2 ? BN / 2 : BN;    // activation rows in this CTA
+  static constexpr int A_BYTES = A_ROWS * kBK * 2;   // activation box
   static constexpr int STAGE = W_BYTES + A_BYTES;
   static constexpr int CH = 32;                      // activation rows per epilogue chunk
   static constexpr int PITCH = kBM + 4;
@@ -145,7 +234,8 @@ struct UmCfg {
   static constexpr int ROWS_BYTES = 256 * (4 + 8);     // rotary epilogue: positions, offsets
   static constexpr int SMEM = 1024 + NS * STAGE + CS_BYTES + NBAR * 8 + 32 + MAXC * 4 + ROWS_BYTES;
   static constexpr int THREADS = 192;
-  static constexpr uint32_t IDESC = umma_idesc_bf16<kBM, BN>();
+  // M = the pair's 256 weight rows (P2) or 128, N = BN activation rows
+  static constexpr uint32_t IDESC = umma_idesc_bf16<P2 ? 2 * kBM : kBM, BN>();
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(STAGE % 1024 == 0 && W_BYTES % 1024 == 0, "swizzle atoms stay 1024-aligned");
 };
@@ -245,11 +335,18 @@ __device__ __forceinline__ void resid_apply(const float4 (&x)[8], const float* C
 }
 
 
-template <int BN, int EPI>
+// P2: whole tiles on SM pairs (clusters of two CTAs).  A pair takes pair tiles (an
+// activation block against two adjacent weight tiles, one per CTA; for an odd tile count
+// the last pair tile's second weight tile is a phantom that computes the first again and
+// stores nothing).  Both CTAs load their own weight box and half of the activation box
+// into their stages, counted on the even CTA's full barriers; the even CTA issues the
+// M = 256 MMAs and commits stages, accumulators and completion to both CTAs' barriers;
+// each CTA's epilogue drains its own TMEM and counts itself on the even CTA's barrier.
+template <int BN, int EPI, bool P2 = false>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_umma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ WMaps wm,
                 const GemmShape g, const EpiArgs<bf16> e) {
-  using C = UmCfg<BN>;
+  using C = UmCfg<BN, P2>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -268,8 +365,17 @@ __global__ void __launch_bounds__(192, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grid = gridDim.x, cta = blockIdx.x;
-  long long u0, u1;
-  if (g.tile_mode) {
+  long long u0 = 0, u1 = 0;     // unit range (single CTAs)
+  long long pt0 = 0, pt1 = 0;   // pair tiles (pairs)
+  const int ntp = (g.n_tiles + 1) >> 1;   // pair tiles per activation block
+  uint32_t rank = 0;
+  if constexpr (P2) {
+    rank = cluster_rank();
+    const long long T2 = static_cast<long long>(g.m_blocks) * ntp;
+    const int npair = grid >> 1, pr = cta >> 1;
+    pt0 = T2 * pr / npair;
+    pt1 = T2 * (pr + 1) / npair;
+  } else if (g.tile_mode) {
     // whole tiles: CTA c takes tiles [T*c/grid, T*(c+1)/grid)
     const long long T = g.units / g.ks;
     u0 = T * cta / grid * g.ks;
@@ -277,7 +383,15 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     cta_range(g.units, cta, grid, u0, u1);
   }
-  const int n_my = static_cast<int>(u1 - u0);
+  const int n_my = P2 ? static_cast<int>((pt1 - pt0) * g.ks) : static_cast<int>(u1 - u0);
+  // pair tile pt -> this CTA's tile (mb * n_tiles + nt) and whether it is a real one
+  auto pair_tile = [&](long long pt, bool& real) -> int {
+    const int mb = static_cast<int>(pt / ntp), t2 = static_cast<int>(pt - static_cast<long long>(mb) * ntp);
+    int nt = 2 * t2 + static_cast<int>(rank);
+    real = nt < g.n_tiles;
+    if (!real) nt -= 1;
+    return mb * g.n_tiles + nt;
+  };
 
   if (tid == 0) {
     for (int s = 0; s < C::NS; ++s) {
@@ -286,21 +400,109 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], P2 ? 8 : 4);   // the epilogue warps of both CTAs (pairs)
     }
     mbar_init(done, 1);
     mbar_fence_init();
   }
   if (warp == 1) {
-    tmem_alloc(tbase, C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (P2) {
+      tmem_alloc2(tbase, C::TMEM_COLS);
+      tmem_relinquish2();
+    } else {
+      tmem_alloc(tbase, C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // pairs: both CTAs' barriers are initialised before either signals the other's
+  if constexpr (P2) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tbase;
 
-  if (warp == 0) {
+  if (P2 && warp == 0) {
+    // ------------------------------------------------------------ TMA producer (pairs)
+    if (lane == 0 && n_my > 0) {
+      tma_prefetch_desc(&tmA);
+      const uint64_t pol = policy_evict_first();
+      // this CTA's units in order: the ks stages of each of its pair tiles
+      struct PW {
+        UnitWalk w;
+        long long pt;
+        int k;
+      };
+      auto pw_start = [&](PW& p) {
+        p.pt = pt0;
+        p.k = 0;
+        bool real;
+        p.w.start(g, static_cast<long long>(pair_tile(p.pt, real)) * g.ks);
+      };
+      auto pw_next = [&](PW& p) {
+        if (++p.k < g.ks) {
+          p.w.next(g);
+          return;
+        }
+        p.k = 0;
+        if (++p.pt < pt1) {
+          bool real;
+          p.w.start(g, static_cast<long long>(pair_tile(p.pt, real)) * g.ks);
+        }
+      };
+      PW wc, ac;
+      pw_start(wc);
+      ac = wc;
+      auto bar_of = [&](int s) { return cluster_addr(&full[s], 0); };   // the even CTA's
+      auto issue_w = [&](int s, const UnitWalk& w) {
+        uint8_t* st = stages + s * C::STAGE;
+        if (g.paired) {
+          tma_load_2d_pair_hint(st, &wm.m[0], bar_of(s), w.ks * kBK, w.row, pol);
+          tma_load_2d_pair_hint(st + C::W_BYTES / 2, &wm.m[1], bar_of(s), w.ks * kBK, w.row, pol);
+        } else {
+          tma_load_2d_pair_hint(st, &wm.m[w.seg], bar_of(s), w.ks * kBK, w.row, pol);
+        }
+      };
+      auto issue_a = [&](int s, const UnitWalk& w) {
+        tma_load_2d_pair(stages + s * C::STAGE + C::W_BYTES, &tmA, bar_of(s), w.ks * kBK,
+                         w.mb * BN + static_cast<int>(rank) * C::A_ROWS);
+      };
+      // the even CTA expects both CTAs' bytes of every stage
+      const int pre = min(C::NS, n_my);
+      for (int i = 0; i < pre; ++i) {
+        if (rank == 0) mbar_arrive_expect_tx(&full[i], 2 * C::STAGE);
+        issue_w(i, wc.w);
+        pw_next(wc);
+      }
+      pdl_wait();  // activations are written by the previous kernel
+      for (int i = 0; i < pre; ++i) {
+        issue_a(i, ac.w);
+        pw_next(ac);
+      }
+      int issued = pre;
+      int s = pre % C::NS;
+      uint32_t par = (pre / C::NS) & 1;
+      for (int i = pre; i < n_my; ++i) {
+        // the stage is free in this CTA once the pair's MMAs have read it
+        if (!mbar_wait(&empty[s], par ^ 1)) {
+          raise_error(e.err, DFLASH_DEV_TIMEOUT);
+          break;
+        }
+        if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE);
+        issue_w(s, wc.w);
+        issue_a(s, ac.w);
+        pw_next(wc);
+        pw_next(ac);
+        issued = i + 1;
+        if (++s == C::NS) { s = 0; par ^= 1; }
+      }
+      // never leave with copies in flight: the even CTA's full barriers count both CTAs'
+      // copies, and the odd CTA leaves only after the even one (final cluster barrier)
+      if (rank == 0)
+        for (int i = max(0, issued - C::NS); i < issued; ++i)
+          mbar_wait(&full[i % C::NS], (i / C::NS) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && n_my > 0) {
       tma_prefetch_desc(&tmA);
@@ -352,6 +554,43 @@ __global__ void __launch_bounds__(192, 1)
         mbar_wait(&full[i % C::NS], (i / C::NS) & 1);
     }
     __syncwarp();  // the warp reaches the final barrier converged
+  } else if (P2 && warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (pairs)
+    if (lane == 0 && rank == 0) {
+      bool ok = true;
+      int i = 0, piece = 0;
+      for (long long pt = pt0; pt < pt1; ++pt, ++piece) {
+        const int ab = piece & 1, use = piece >> 1;
+        // both CTAs' epilogues must have drained this accumulator's previous tile
+        if (ok && use > 0 && !mbar_wait(&tempty[ab], (use - 1) & 1)) {
+          raise_error(e.err, DFLASH_DEV_TIMEOUT);
+          ok = false;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(ab * BN);
+        for (int k = 0; k < g.ks; ++k, ++i) {
+          const int s = i % C::NS;
+          if (ok && !mbar_wait(&full[s], (i / C::NS) & 1)) {
+            raise_error(e.err, DFLASH_DEV_TIMEOUT);
+            ok = false;
+          }
+          if (ok) {
+            tc_fence_after();
+            const uint32_t wb = smem_u32(stages + s * C::STAGE);
+            const uint32_t ab_ = wb + C::W_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              umma_bf16_pair(d, umma_desc_sw128(wb + kk * 32), umma_desc_sw128(ab_ + kk * 32),
+                             C::IDESC, (k | kk) != 0);
+          }
+          umma_commit_pair(&empty[s]);   // frees the stage in both CTAs
+        }
+        umma_commit_pair(&tfull[ab]);    // the tile is complete in both CTAs' TMEM
+      }
+      umma_commit_pair_local(done);
+      mbar_wait(done, 0);
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -404,14 +643,31 @@ __global__ void __launch_bounds__(192, 1)
     bool ok = true;
     pdl_wait();
     pdl_launch_dependents();
-    long long u = u0;
+    long long u = u0, pt = pt0;
     int piece = 0;
-    while (u < u1) {
-      const int t = static_cast<int>(u / g.ks);
-      const int ks0 = static_cast<int>(u % g.ks);
+    // pairs: the accumulator is handed back on the even CTA's barrier
+    const uint32_t tempty_cl = P2 ? cluster_addr(tempty, 0) : 0u;
+    while (P2 ? pt < pt1 : u < u1) {
+      bool real = true;
+      const int t = P2 ? pair_tile(pt, real) : static_cast<int>(u / g.ks);
+      const int ks0 = P2 ? 0 : static_cast<int>(u % g.ks);
       const long long tile_end = static_cast<long long>(t + 1) * g.ks;
-      const long long seg_end = min(tile_end, u1);
+      const long long seg_end = P2 ? tile_end : min(tile_end, u1);
       const int ab = piece & 1, use = piece >> 1;
+      if (P2 && !real) {
+        // a phantom tile: wait for the accumulator and hand it back at once
+        if (ok && !__all_sync(0xffffffffu, mbar_wait(&tfull[ab], use & 1))) {
+          if (lane == 0) raise_error(e.err, DFLASH_DEV_TIMEOUT);
+          ok = false;
+        }
+        tc_fence_after();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_cl + static_cast<uint32_t>(ab * 8));
+        ++pt;
+        ++piece;
+        continue;
+      }
       const uint32_t tacc = tmem + lane_base + static_cast<uint32_t>(ab * BN);
       const int mb = t / g.n_tiles, nt = t - mb * g.n_tiles;
       const int m_first = mb * BN;
@@ -495,7 +751,10 @@ __global__ void __launch_bounds__(192, 1)
         if (c == nch - 1) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[ab]);
+          if (lane == 0) {
+            if constexpr (P2) mbar_arrive_cluster(tempty_cl + static_cast<uint32_t>(ab * 8));
+            else mbar_arrive(&tempty[ab]);
+          }
         }
       };
 
@@ -680,17 +939,21 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       u = seg_end;
+      ++pt;
       ++piece;
     }
     if constexpr (EPI == EPI_ARGKEY) argmax_keys_finish(e, g.M, et, 128, flag, epi_sync);
   }
 
-  // ---- teardown: every role is here, every MMA has completed; free TMEM
+  // ---- teardown: every role is here, every MMA has completed; free TMEM (pairs: both
+  // CTAs are here, so the even CTA's MMAs have read the last of either CTA's stages)
   tc_fence_before();
   __syncthreads();
+  if constexpr (P2) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    if constexpr (P2) tmem_dealloc2(tmem, C::TMEM_COLS);
+    else tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
