@@ -186,7 +186,7 @@ struct AuCfg {
   // 32-column slabs) the rest (key-split) or all of it
   static constexpr int STG_OFF = KSPLIT ? NS * STAGE / 2 : 0;
   static constexpr int MAX_QR = KSPLIT ? 64 : 128;
-  static_assert(!KSPLIT || 64 * HD * 4 + 64 * 8 <= STG_OFF, "merge buffer");
+  static_assert(!KSPLIT || 64 * HD * 4 + 2 * 64 * 8 <= STG_OFF, "merge buffer");
   static_assert(STG_OFF + MAX_QR * HD * 4 <= NS * STAGE, "staged output");
   static_assert(32 % PG == 0, "page ids of whole steps per 32 lanes");
 };
@@ -568,48 +568,56 @@ __global__ void __launch_bounds__(192, AuCfg<HD, KSPLIT>::CPS)
     const bool staged = a.nsplit > 1;
     uint8_t* stg = stages + C::STG_OFF;
     if constexpr (KSPLIT) {
-      // The K/V ring is idle (every MMA has completed): lanes 64-127 leave their O row
-      // and (m, l) there, lanes 0-63 merge them into theirs.  Row q's columns are
-      // rotated by q so that a warp's 32 stores of one column hit 32 banks.
-      float* mo = reinterpret_cast<float*>(stages);               // [64][HD]
-      float* mml = mo + 64 * HD;                                  // [64][2]
-      if (half) {
+      // The K/V ring is idle (every MMA has completed).  Lanes r and r + 64 hold the same
+      // query row; each hands the other, through shared memory, the half of its O row
+      // that the other merges (lanes 0-63 merge columns [0, HD/2), lanes 64-127 columns
+      // [HD/2, HD)), with its (m, l).  Row q's columns are rotated by q so that a warp's
+      // 32 stores of one column hit 32 banks.  Both halves form the merged state in the
+      // same order (the key-0..31 half's terms first).
+      constexpr int HH = HD / 2;
+      float* mo = reinterpret_cast<float*>(stages);               // [2][64][HH]
+      float* mml = mo + 2 * 64 * HH;                              // [2][64][2]
+      float* mine = mo + half * 64 * HH;
+      const float* other = mo + (1 - half) * 64 * HH;
+      const int give0 = half ? 0 : HH, keep0 = half ? HH : 0;     // columns handed over, kept
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(o_addr + c * 32, ov);
-          tmem_ld_wait();
+      for (int c = 0; c < HH / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(o_addr + give0 + c * 32, ov);
+        tmem_ld_wait();
 #pragma unroll
-          for (int d = 0; d < 32; ++d) mo[qrow * HD + ((c * 32 + d + qrow) & (HD - 1))] = __uint_as_float(ov[d]);
-        }
-        mml[2 * qrow] = mref;
-        mml[2 * qrow + 1] = l;
+        for (int d = 0; d < 32; ++d)
+          mine[qrow * HH + ((c * 32 + d + qrow) & (HH - 1))] = __uint_as_float(ov[d]);
       }
+      mml[half * 128 + 2 * qrow] = mref;
+      mml[half * 128 + 2 * qrow + 1] = l;
       epi_sync();
-      if (!half) {
-        const float m2 = mml[2 * qrow], l2 = mml[2 * qrow + 1];
-        const float M = fmaxf(mref, m2);
-        const float w1 = exp2f(mref - M), w2 = exp2f(m2 - M);
-        l = l * w1 + l2 * w2;
-        mref = M;
+      const float m2 = mml[(1 - half) * 128 + 2 * qrow], l2 = mml[(1 - half) * 128 + 2 * qrow + 1];
+      const float M = fmaxf(mref, m2);
+      const float w1 = exp2f(mref - M), w2 = exp2f(m2 - M);
+      // (m0, l0, w0): the key-0..31 half's state, whichever thread this is
+      const float wa = half ? w2 : w1, wb = half ? w1 : w2;
+      l = half ? l2 * wa + l * wb : l * wa + l2 * wb;
+      mref = M;
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(o_addr + c * 32, ov);
-          tmem_ld_wait();
-          if (qrow < a.QR && ok) {
+      for (int c = 0; c < HH / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(o_addr + keep0 + c * 32, ov);
+        tmem_ld_wait();
+        if (qrow < a.QR && ok) {
 #pragma unroll
-            for (int d = 0; d < 32; ++d)
-              ov[d] = __float_as_uint(__uint_as_float(ov[d]) * w1 +
-                                      mo[qrow * HD + ((c * 32 + d + qrow) & (HD - 1))] * w2);
-            if (staged) {
-              stage_row32(stg, c, a.QR, qrow, ov);
-            } else {
+          for (int d = 0; d < 32; ++d) {
+            const float own = __uint_as_float(ov[d]);
+            const float oth = other[qrow * HH + ((c * 32 + d + qrow) & (HH - 1))];
+            ov[d] = __float_as_uint(half ? oth * wa + own * wb : own * wa + oth * wb);
+          }
+          if (staged) {
+            stage_row32(stg, keep0 / 32 + c, a.QR, qrow, ov);
+          } else {
 #pragma unroll
-              for (int d = 0; d < 32; d += 2)
-                attn_emit<bf16>(a, b, g, split, qrow, c * 32 + d, __uint_as_float(ov[d]),
-                                __uint_as_float(ov[d + 1]), l);
-            }
+            for (int d = 0; d < 32; d += 2)
+              attn_emit<bf16>(a, b, g, split, qrow, keep0 + c * 32 + d, __uint_as_float(ov[d]),
+                              __uint_as_float(ov[d + 1]), l);
           }
         }
       }
