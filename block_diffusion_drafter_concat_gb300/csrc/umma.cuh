@@ -24,9 +24,12 @@
 //               rotary entries) one chunk ahead, the first chunk's while the
 //               accumulator is still being computed.
 // Two TMEM accumulators let the MMA of the next tile piece run under the epilogue of
-// the previous one.  Every mbarrier wait is bounded; a wait that gives up raises the
-// device error word and its role stops waiting, so the CTA always reaches the final
-// barrier and frees its TMEM.
+// the previous one.  Projections that take whole 256-row tiles run on SM pairs
+// (clusters of two CTAs, cta_group::2, see k_gemm_umma's P2 form): each SM holds its own
+// weight rows and half of the activation rows, one thread of the even CTA issues
+// M = 256 MMAs over both SMs' stages.  Every mbarrier wait is bounded; a wait that gives
+// up raises the device error word and its role stops waiting, so the CTA always reaches
+// the final barrier (pairs: both CTAs, then the cluster barrier) and frees its TMEM.
 #pragma once
 
 #include "gemm.cuh"
