@@ -856,88 +856,169 @@ __global__ void __launch_bounds__(192, 1)
           epi_sync();
         }
       } else {
-        // A piece of a tile split between CTAs.  The order of arrival picks the CTA that
-        // finishes the tile: the others publish their partial tile ([BN][kBM] fp32 in
-        // their slot) and count themselves published; the finisher waits for them (they
-        // are already running and wait on nothing), keeps its own partial in TMEM and
-        // sums all contributions in contributor order, so the result does not depend on
-        // who arrived last.
-        const int slot = (u == u0) ? 0 : 1;
-        int* arrived = g.counters + t;
-        int* published = g.counters + kTileWords + t;
-        if (et == 0) {
-          const int ncontrib = tile_contributors(g.units, grid, g.ks, t, nullptr);
-          flag[0] = (atomicAdd(arrived, 1) == ncontrib - 1);
-          flag[1] = ncontrib;
-        }
-        epi_sync();
-        const bool finisher = flag[0] != 0;
-        const int ncontrib = flag[1];
-        if (!finisher) {
-          // partial slot layout [activation row][weight row]: for each row the 32 lanes
-          // of a warp write (and the finisher reads) one whole 128-byte line
-          float* dst = g.part + (static_cast<long long>(cta) * 2 + slot) * BN * kBM;
-          for (int c = 0; c < nch; ++c) {
-            uint32_t v[32];
-            read_chunk(c, v);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) dst[(c * C::CH + j) * kBM + feat] = __uint_as_float(v[j]);
-          }
-          epi_sync();
-          if (et == 0) red_release_add(published, 1);
-        } else {
-          if (et == 0) {
-            tile_contributors(g.units, grid, g.ks, t, cslot);
-            const unsigned long long t0 = global_ns();
-            while (ld_acquire_gpu(published) < ncontrib - 1 + g.wait_extra) {
-              if (global_ns() - t0 > g.wait_ns) {
-                raise_error(e.err, DFLASH_DEV_TIMEOUT);
-                break;
-              }
+        if constexpr (BN == 128) {
+          // A piece of a tile split between CTAs.  Every contributor publishes its partial
+          // tile ([BN][kBM] fp32 in its slot) and then counts itself in (acquire-release);
+          // the one that brings the count to the number of contributors finishes the tile
+          // from every published piece, in contributor order, so the result does not depend
+          // on who arrived last and the finisher never waits.  (Under the forced-timeout
+          // test hook it waits, bounded, for a count that cannot be reached.)
+          const int slot = (u == u0) ? 0 : 1;
+          int* arrived = g.counters + t;
+          {
+            // partial slot layout [activation row][weight row]: for each row the 32 lanes
+            // of a warp write (and the finisher reads) one whole 128-byte line
+            float* dst = g.part + (static_cast<long long>(cta) * 2 + slot) * BN * kBM;
+            for (int c = 0; c < nch; ++c) {
+              uint32_t v[32];
+              read_chunk(c, v);
+  #pragma unroll
+              for (int j = 0; j < 32; ++j) dst[(c * C::CH + j) * kBM + feat] = __uint_as_float(v[j]);
             }
-            *arrived = 0;
-            *published = 0;
-            __threadfence();
           }
           epi_sync();
-          for (int c = 0; c < nch; ++c) {
-            uint32_t own[32];
-            read_chunk(c, own);
-            float acc[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-            // contributors two at a time: 64 coalesced loads in flight per thread
-            for (int c0 = 0; c0 < ncontrib; c0 += 2) {
-              float pv[2][32];
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const int ci = c0 + k;
-                if (ci < ncontrib && (cslot[ci] >> 1) != cta) {
-                  const float* src = g.part + static_cast<long long>(cslot[ci]) * BN * kBM +
-                                     (c * C::CH) * kBM + feat;
-#pragma unroll
-                  for (int j = 0; j < 32; ++j) pv[k][j] = __ldcg(src + j * kBM);
+          if (et == 0) {
+            const int ncontrib = tile_contributors(g.units, grid, g.ks, t, nullptr);
+            __threadfence();
+            const bool last = atom_add_acq_rel_gpu(arrived, 1) == ncontrib - 1;
+            flag[0] = last;
+            flag[1] = ncontrib;
+            if (last) {
+              tile_contributors(g.units, grid, g.ks, t, cslot);
+              if (g.wait_extra) {
+                const unsigned long long t0 = global_ns();
+                while (ld_acquire_gpu(arrived) < ncontrib + g.wait_extra) {
+                  if (global_ns() - t0 > g.wait_ns) {
+                    raise_error(e.err, DFLASH_DEV_TIMEOUT);
+                    break;
+                  }
                 }
               }
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const int ci = c0 + k;
-                if (ci >= ncontrib) continue;
-                if ((cslot[ci] >> 1) == cta) {
-#pragma unroll
-                  for (int j = 0; j < 32; ++j) acc[j] += __uint_as_float(own[j]);
-                } else {
-#pragma unroll
+              *arrived = 0;
+              __threadfence();
+            }
+          }
+          epi_sync();
+          if (flag[0]) {
+            const int ncontrib = flag[1];
+            for (int c = 0; c < nch; ++c) {
+              float acc[32];
+  #pragma unroll
+              for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+              // contributors two at a time: 64 coalesced loads in flight per thread
+              for (int c0 = 0; c0 < ncontrib; c0 += 2) {
+                float pv[2][32];
+  #pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                  const int ci = c0 + k;
+                  if (ci < ncontrib) {
+                    const float* src = g.part + static_cast<long long>(cslot[ci]) * BN * kBM +
+                                       (c * C::CH) * kBM + feat;
+  #pragma unroll
+                    for (int j = 0; j < 32; ++j) pv[k][j] = __ldcg(src + j * kBM);
+                  }
+                }
+  #pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                  if (c0 + k >= ncontrib) continue;
+  #pragma unroll
                   for (int j = 0; j < 32; ++j) acc[j] += pv[k][j];
                 }
               }
+  #pragma unroll
+              for (int j = 0; j < 32; ++j) Cs[j * C::PITCH + feat] = acc[j];
+              epi_sync();
+              tile_epilogue<bf16, EPI>(Cs, C::PITCH, C::CH, m_first + c * C::CH, nt, g, e, et,
+                                       128);
+              epi_sync();
             }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) Cs[j * C::PITCH + feat] = acc[j];
+          }
+        } else {
+          // 256-row tiles keep the arrival-first finish: publishing every piece,
+          // the finisher's too, measured slower there (Qwen3-shaped batch 32 +9 us)
+          // A piece of a tile split between CTAs.  The order of arrival picks the CTA that
+          // finishes the tile: the others publish their partial tile ([BN][kBM] fp32 in
+          // their slot) and count themselves published; the finisher waits for them (they
+          // are already running and wait on nothing), keeps its own partial in TMEM and
+          // sums all contributions in contributor order, so the result does not depend on
+          // who arrived last.
+          const int slot = (u == u0) ? 0 : 1;
+          int* arrived = g.counters + t;
+          int* published = g.counters + kTileWords + t;
+          if (et == 0) {
+            const int ncontrib = tile_contributors(g.units, grid, g.ks, t, nullptr);
+            flag[0] = (atomicAdd(arrived, 1) == ncontrib - 1);
+            flag[1] = ncontrib;
+          }
+          epi_sync();
+          const bool finisher = flag[0] != 0;
+          const int ncontrib = flag[1];
+          if (!finisher) {
+            // partial slot layout [activation row][weight row]: for each row the 32 lanes
+            // of a warp write (and the finisher reads) one whole 128-byte line
+            float* dst = g.part + (static_cast<long long>(cta) * 2 + slot) * BN * kBM;
+            for (int c = 0; c < nch; ++c) {
+              uint32_t v[32];
+              read_chunk(c, v);
+  #pragma unroll
+              for (int j = 0; j < 32; ++j) dst[(c * C::CH + j) * kBM + feat] = __uint_as_float(v[j]);
+            }
             epi_sync();
-            tile_epilogue<bf16, EPI>(Cs, C::PITCH, C::CH, m_first + c * C::CH, nt, g, e, et,
-                                     128);
+            if (et == 0) red_release_add(published, 1);
+          } else {
+            if (et == 0) {
+              tile_contributors(g.units, grid, g.ks, t, cslot);
+              const unsigned long long t0 = global_ns();
+              while (ld_acquire_gpu(published) < ncontrib - 1 + g.wait_extra) {
+                if (global_ns() - t0 > g.wait_ns) {
+                  raise_error(e.err, DFLASH_DEV_TIMEOUT);
+                  break;
+                }
+              }
+              *arrived = 0;
+              *published = 0;
+              __threadfence();
+            }
             epi_sync();
+            for (int c = 0; c < nch; ++c) {
+              uint32_t own[32];
+              read_chunk(c, own);
+              float acc[32];
+  #pragma unroll
+              for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+              // contributors two at a time: 64 coalesced loads in flight per thread
+              for (int c0 = 0; c0 < ncontrib; c0 += 2) {
+                float pv[2][32];
+  #pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                  const int ci = c0 + k;
+                  if (ci < ncontrib && (cslot[ci] >> 1) != cta) {
+                    const float* src = g.part + static_cast<long long>(cslot[ci]) * BN * kBM +
+                                       (c * C::CH) * kBM + feat;
+  #pragma unroll
+                    for (int j = 0; j < 32; ++j) pv[k][j] = __ldcg(src + j * kBM);
+                  }
+                }
+  #pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                  const int ci = c0 + k;
+                  if (ci >= ncontrib) continue;
+                  if ((cslot[ci] >> 1) == cta) {
+  #pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[j] += __uint_as_float(own[j]);
+                  } else {
+  #pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[j] += pv[k][j];
+                  }
+                }
+              }
+  #pragma unroll
+              for (int j = 0; j < 32; ++j) Cs[j * C::PITCH + feat] = acc[j];
+              epi_sync();
+              tile_epilogue<bf16, EPI>(Cs, C::PITCH, C::CH, m_first + c * C::CH, nt, g, e, et,
+                                       128);
+              epi_sync();
+            }
           }
         }
       }

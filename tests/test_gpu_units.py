@@ -215,6 +215,9 @@ TIMEOUT_WORKLOADS = {
     "small-bf16-hd128": configs.PARITY_SMALL["small-bf16-hd128"],
     "timeout-tc256-v80k": configs.small_bf16(name="timeout-tc256-v80k", batch=20, vocab=80000,
                                              ctx_range=(16, 64), seed=24),
+    # 96 rows: the tcgen05 kernel's 128-row tiles, whose split finish counts after publishing
+    "timeout-tc128-v80k": configs.small_bf16(name="timeout-tc128-v80k", batch=6, vocab=80000,
+                                             ctx_range=(16, 64), seed=25),
 }
 
 
