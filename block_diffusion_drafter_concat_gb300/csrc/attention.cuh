@@ -61,7 +61,10 @@ struct AttnMaps {
 
 // Combine of the published splits, grid (ceil(QR / 8), hkv, B), 8 rows x hd/4 threads:
 // out[r] = sum_s w_s o_s / sum_s w_s l_s with w_s = 2^(m_s - max m), splits in order.
-template <typename T>
+// SF: splits whose loads are in flight at once (16 for many splits; 4 when a launch has
+// at most 4, where the registers of 16 would only cut the occupancy).  The splits are
+// merged one after another in either case, so SF does not change the result.
+template <typename T, int SF>
 __global__ void __launch_bounds__(256) k_attn_combine(const AttnArgs<T> a) {
   pdl_wait();
   pdl_launch_dependents();
@@ -76,8 +79,7 @@ __global__ void __launch_bounds__(256) k_attn_combine(const AttnArgs<T> a) {
   const long long grp = (long long)b * a.hkv + g;
   const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + grp * a.nsplit * a.QR;
   const float4* po = reinterpret_cast<const float4*>(a.part_o + grp * a.nsplit * a.QR * a.hd);
-  // one pass in split order with a running maximum (loads of 16 splits in flight)
-  constexpr int SF = 16;
+  // one pass in split order with a running maximum (loads of SF splits in flight)
   float M = -INFINITY, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s0 = 0; s0 < ns; s0 += SF) {

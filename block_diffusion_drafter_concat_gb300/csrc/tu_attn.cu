@@ -40,7 +40,8 @@ dflash_status launch_attn_f32(dim3 grid, int smem, const AttnArgs<float>& a, cud
 template <typename T>
 static dflash_status combine(int B, const AttnArgs<T>& a, cudaStream_t st) {
   dim3 grid((a.QR + 7) / 8, a.hkv, B);
-  return launch(k_attn_combine<T>, grid, dim3(8 * a.hd / 4), 0, st, a);
+  if (a.nsplit <= 4) return launch(k_attn_combine<T, 4>, grid, dim3(8 * a.hd / 4), 0, st, a);
+  return launch(k_attn_combine<T, 16>, grid, dim3(8 * a.hd / 4), 0, st, a);
 }
 dflash_status launch_attn_combine(int B, const AttnArgs<bf16>& a, cudaStream_t st) {
   return combine(B, a, st);
