@@ -61,8 +61,8 @@ struct AttnMaps {
 
 // Combine of the published splits, grid (ceil(QR / 8), hkv, B), 8 rows x hd/4 threads:
 // out[r] = sum_s w_s o_s / sum_s w_s l_s with w_s = 2^(m_s - max m), splits in order.
-// SF: splits whose loads are in flight at once (16 for many splits; 4 when a launch has
-// at most 4, where the registers of 16 would only cut the occupancy).  The splits are
+// SF: splits whose loads are in flight at once (16 for many splits; 4 or 8 when a launch
+// has at most that many, where the registers of 16 would only cut the occupancy).  The splits are
 // merged one after another in either case, so SF does not change the result.
 template <typename T, int SF>
 __global__ void __launch_bounds__(256) k_attn_combine(const AttnArgs<T> a) {

@@ -41,6 +41,7 @@ template <typename T>
 static dflash_status combine(int B, const AttnArgs<T>& a, cudaStream_t st) {
   dim3 grid((a.QR + 7) / 8, a.hkv, B);
   if (a.nsplit <= 4) return launch(k_attn_combine<T, 4>, grid, dim3(8 * a.hd / 4), 0, st, a);
+  if (a.nsplit <= 8) return launch(k_attn_combine<T, 8>, grid, dim3(8 * a.hd / 4), 0, st, a);
   return launch(k_attn_combine<T, 16>, grid, dim3(8 * a.hd / 4), 0, st, a);
 }
 dflash_status launch_attn_combine(int B, const AttnArgs<bf16>& a, cudaStream_t st) {
